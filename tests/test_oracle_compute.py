@@ -1,0 +1,228 @@
+"""Pins for the oracle's GEMM, argmax and acceptance walks (CPU only)."""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import w12_oracle as O
+from speculative_decoding_verification_w12_gb300 import synthetic as S
+
+
+# ---------------------------------------------------------------------------
+# GEMM
+# ---------------------------------------------------------------------------
+
+def test_gemm_identity_blocks_return_x():
+    K = 256
+    W = np.zeros((K, K), dtype=np.uint16)
+    W[np.arange(K), np.arange(K)] = 0x3F80            # 1.0 on the diagonal, zeros elsewhere
+    X = S.activations_bf16(16, K)
+    Y = O.gemm(X, O.pack(W))
+    np.testing.assert_array_equal(Y, S.bf16_bits_to_f32(X).astype(np.float64))
+
+
+def test_gemm_small_integers_exact():
+    g = S.rng(21)
+    M, N, K = 5, 128, 384
+    Xi = g.integers(-8, 9, size=(M, K))
+    Wi = g.integers(-8, 9, size=(N, K))
+    X = S.f32_to_bf16_bits(Xi.astype(np.float32))
+    W = S.f32_to_bf16_bits(Wi.astype(np.float32))
+    Y = O.gemm(X, O.pack(W))
+    exact = [[sum(int(Xi[m, k]) * int(Wi[n, k]) for k in range(K)) for n in range(N)] for m in range(M)]
+    np.testing.assert_array_equal(Y, np.array(exact, dtype=np.float64))
+
+
+def test_gemm_brute_force_exact_rational():
+    M, N, K = 2, 128, 128
+    X = S.activations_bf16(M, K, seed=31)
+    W = S.weights_bf16(N, K, seed=32)
+    W[0, :7] = 0                                      # exceptions inside the contraction
+    W[1, 3] = 0x0001                                  # a subnormal weight
+    Y = O.gemm(X, O.pack(W))
+    xf = S.bf16_bits_to_f32(X)
+    wf = S.bf16_bits_to_f32(W)
+    for m in range(M):
+        for n in range(0, N, 9):
+            exact = sum(Fraction(float(xf[m, k])) * Fraction(float(wf[n, k])) for k in range(K))
+            assert abs(Y[m, n] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
+
+
+# ---------------------------------------------------------------------------
+# argmax
+# ---------------------------------------------------------------------------
+
+def test_argmax_planted_unique_max_and_gap():
+    g = S.rng(41)
+    L = g.standard_normal((6, 1000))
+    cols = [3, 999, 0, 500, 77, 123]
+    for r, c in enumerate(cols):
+        L[r, c] = 50.0 + r
+    idx, gap = O.argmax_rows(L)
+    np.testing.assert_array_equal(idx, cols)
+    for r in range(6):
+        srt = np.sort(L[r])
+        assert gap[r] == srt[-1] - srt[-2]
+
+
+def test_argmax_exact_ties_take_lowest_index():
+    L = np.zeros((3, 10))
+    L[0, [2, 5, 9]] = 1.0
+    L[1, :] = -3.0
+    L[2, [9, 4]] = 7.5
+    idx, gap = O.argmax_rows(L)
+    np.testing.assert_array_equal(idx, [2, 0, 4])
+    np.testing.assert_array_equal(gap, [0.0, 0.0, 0.0])
+
+
+# ---------------------------------------------------------------------------
+# greedy block acceptance
+# ---------------------------------------------------------------------------
+
+def _greedy_def(d, t, T_rows):
+    L = next((j for j in range(len(d)) if d[j] != t[j]), len(d))
+    return L, (t[L] if L < T_rows else -1)
+
+
+@pytest.mark.parametrize("T_rows", [4, 5])
+def test_verify_greedy_brute_force_v3_t4(T_rows):
+    T, V = 4, 3
+    drafts = list(itertools.product(range(V), repeat=T))
+    targets = list(itertools.product(range(V), repeat=T_rows))
+    for t in targets:
+        D = np.array(drafts, dtype=np.int32)
+        tgt = np.tile(np.array(t, dtype=np.int32), len(drafts))
+        acc, bonus = O.verify_greedy(D, tgt, T_rows)
+        for b, d in enumerate(drafts):
+            L, bo = _greedy_def(d, t, T_rows)
+            assert acc[b] == L and bonus[b] == bo
+
+
+def test_verify_greedy_edge_lengths():
+    T = 16
+    tgt = np.arange(100, 100 + 17, dtype=np.int32)
+    d_all = tgt[:16].reshape(1, 16)
+    acc, bonus = O.verify_greedy(d_all, tgt[:16], 16)
+    assert acc[0] == 16 and bonus[0] == -1                 # full block, no row after it
+    acc, bonus = O.verify_greedy(d_all, tgt, 17)
+    assert acc[0] == 16 and bonus[0] == 116                # T_rows = T+1 always has a bonus
+    d0 = d_all.copy()
+    d0[0, 0] = 5
+    acc, bonus = O.verify_greedy(d0, tgt[:16], 16)
+    assert acc[0] == 0 and bonus[0] == 100
+
+
+def test_verify_greedy_planted_lengths():
+    B, T = 64, 16
+    g = S.rng(51)
+    tgt = g.integers(0, 4096, B * T).astype(np.int32)
+    L = S.accept_lengths_uniform(B, T)
+    d = S.plant_block_drafts(tgt, B, T, T, L, 4096)
+    acc, _ = O.verify_greedy(d, tgt, T)
+    np.testing.assert_array_equal(acc, L)
+
+
+# ---------------------------------------------------------------------------
+# tree acceptance
+# ---------------------------------------------------------------------------
+
+def _tree_brute(parents, draft, target):
+    """Enumerate every root-to-node path; keep fully matching ones."""
+    T = len(parents)
+    best = (0, 0)
+    for x in range(T):
+        p = [x]
+        while p[-1] != 0:
+            p.append(int(parents[p[-1]]))
+        p = p[::-1]
+        if all(draft[p[i]] == target[p[i - 1]] for i in range(1, len(p))):
+            d = len(p) - 1
+            if d > best[0] or (d == best[0] and x < best[1]):
+                best = (d, x)
+    return best
+
+
+def test_verify_tree_brute_force_small_trees():
+    g = S.rng(61)
+    for _ in range(400):
+        T = int(g.integers(1, 9))
+        parents = np.array([-1] + [int(g.integers(0, i)) for i in range(1, T)], dtype=np.int32)
+        V = 2
+        draft = g.integers(0, V, T).astype(np.int32)
+        target = g.integers(0, V, T).astype(np.int32)
+        path, plen, acc, bonus = O.verify_tree(parents[None], draft[None], target)
+        d, x = _tree_brute(parents, draft, target)
+        assert acc[0] == d and path[0, plen[0] - 1] == x and bonus[0] == target[x]
+        assert path[0, 0] == 0 and plen[0] == d + 1
+
+
+def test_verify_tree_chain_equals_greedy():
+    g = S.rng(62)
+    T = 17
+    parents = np.arange(-1, T - 1, dtype=np.int32)           # chain: node i's parent is i-1
+    for L in range(0, 17):
+        target = g.integers(0, 50, T).astype(np.int32)
+        drafts = S.plant_block_drafts(target, 1, T - 1, T, np.array([L]), 50, tag=L)
+        tdraft = np.concatenate([[0], drafts[0]]).astype(np.int32)
+        _, _, acc, bonus = O.verify_tree(parents[None], tdraft[None], target)
+        gacc, gbonus = O.verify_greedy(drafts, target, T)
+        assert acc[0] == gacc[0] == L and bonus[0] == gbonus[0]
+
+
+def test_verify_tree_star_binary_and_duplicates():
+    # Star: root with 5 children, the 4th matches.
+    parents = np.array([-1, 0, 0, 0, 0, 0], dtype=np.int32)
+    target = np.array([7, 1, 1, 1, 1, 1], dtype=np.int32)
+    draft = np.array([0, 3, 4, 5, 7, 8], dtype=np.int32)
+    path, plen, acc, bonus = O.verify_tree(parents[None], draft[None], target)
+    assert acc[0] == 1 and list(path[0, :2]) == [0, 4] and bonus[0] == 1
+    # Duplicate sibling tokens: two accepted depth-1 nodes; the deeper branch wins,
+    # and among equal depth the lowest index wins.
+    parents = np.array([-1, 0, 0, 1, 2], dtype=np.int32)
+    target = np.array([9, 5, 6, 0, 0], dtype=np.int32)
+    draft = np.array([0, 9, 9, 4, 6], dtype=np.int32)       # nodes 1 and 2 both accepted; 4 under 2 accepted
+    path, plen, acc, bonus = O.verify_tree(parents[None], draft[None], target)
+    assert acc[0] == 2 and list(path[0, :3]) == [0, 2, 4]
+    draft2 = np.array([0, 9, 9, 1, 1], dtype=np.int32)      # only depth 1; tie between 1 and 2
+    path, plen, acc, bonus = O.verify_tree(parents[None], draft2[None], target)
+    assert acc[0] == 1 and path[0, 1] == 1 and bonus[0] == 5
+    # Full binary tree of depth 5 (63 nodes): accept along the right-most path to depth 5.
+    T = 63
+    parents = np.array([-1] + [(i - 1) // 2 for i in range(1, T)], dtype=np.int32)
+    target = np.arange(T, dtype=np.int32) + 1000
+    draft = np.zeros(T, dtype=np.int32)
+    x = 0
+    while 2 * x + 2 < T:
+        draft[2 * x + 2] = target[x]
+        x = 2 * x + 2
+    path, plen, acc, bonus = O.verify_tree(parents[None], draft[None], target)
+    assert acc[0] == 5 and path[0, 5] == x and bonus[0] == target[x]
+
+
+@pytest.mark.parametrize("D", [0, 5, 12])
+def test_verify_tree_planted_depth(D):
+    g = S.rng(70 + D)
+    parents = S.random_tree(64, g=g)
+    assert O.check_tree(parents) and S.tree_depths(parents).max() == 12
+    target = g.integers(0, 1000, 64).astype(np.int32)
+    draft, node = S.plant_tree_drafts(parents, target, D, 1000, g)
+    path, plen, acc, bonus = O.verify_tree(parents[None], draft[None], target)
+    assert acc[0] == D and path[0, D] == node
+
+
+def test_check_tree_rejects_invalid():
+    assert not O.check_tree(np.array([0, 0]))
+    assert not O.check_tree(np.array([-1, 1]))
+    assert not O.check_tree(np.array([-1, 0, 3, 1]))
+    with pytest.raises(ValueError):
+        O.verify_tree(np.array([[-1, 2, 0]]), np.zeros((1, 3), np.int32), np.zeros(3, np.int32))
+
+
+def test_oracle_gap_pin_math():
+    # math.nextafter-based near tie: the gap is the exact difference.
+    a = 1.0
+    b = math.nextafter(1.0, 0.0)
+    idx, gap = O.argmax_rows(np.array([[b, a, b]]))
+    assert idx[0] == 1 and gap[0] == a - b
