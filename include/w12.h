@@ -1,0 +1,201 @@
+/*
+ * w12.h -- C ABI of the GB300-native W12 speculative-decoding verify path.
+ *
+ * The verify pass of a speculative decoder reads every target weight to score
+ * a small block (or tree) of drafted tokens per request (SpecPilot paper
+ * digest, summary paragraph). Weights are stored in W12, a lossless 12-bit
+ * layout: BF16 is split into three 4-bit planes that the GEMM restores
+ * bitwise in registers (SpecPilot digest, "Reasons" bullet 2). Acceptance is
+ * greedy: a drafted token is kept iff it equals the target's argmax at the
+ * preceding position (SpecPilot digest, "Risks" bullet 3); draft trees are
+ * causal, each token conditioned on its root-to-node path (JetSpec article,
+ * "Technical architecture").
+ *
+ * W12 layout used by this library (the pages fix only "three 4-bit planes,
+ * restored bitwise"; the mapping below is this library's definition):
+ *   - rows n of W[N, K] (out x in, bf16) are cut into groups of 128 K values;
+ *   - per group, ebase = max(emax - 15, 0), emax = the largest biased exponent
+ *     among the group's finite nonzero normal values (0 if none);
+ *   - a normal finite value with exponent e > ebase is coded as
+ *     code12 = s<<11 | (e-ebase)<<7 | m; anything else (zeros, subnormals,
+ *     magnitudes below the 15-binade window, Inf, NaN) is coded 0 and listed
+ *     in the exception CSR with its exact 16 bits;
+ *   - plane p (p = 0, 1, 2) stores nibble p of code12, bytes [N, K/2]; in each
+ *     row the elements 8q..8q+7 fill bytes 4q..4q+3: byte 4q+i holds element
+ *     8q+i in its low nibble and element 8q+4+i in its high nibble;
+ *   - ebase is a byte array [K/128, N] (group-major);
+ *   - exceptions: blocks of 128 rows x 128 columns, u = (n/128)*(K/128)+k/128;
+ *     exc_off[u] .. exc_off[u+1] index exc_ent; an entry is
+ *     (n%128)<<23 | (k%128)<<16 | bf16 bits, ascending within a block.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in the argument lists are DEVICE pointers into memory the
+ *     caller owns (e.g. allocated by PyTorch), unless the comment says "host".
+ *     The library never allocates and never frees memory.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream). Entry points return once the work is
+ *     enqueued; only the *_query and w12_pack calls synchronise the stream.
+ *   - Return value: W12_OK or an error code; argument and shape errors are
+ *     detected on the host before anything is enqueued.
+ *   - `dev_status` (nullable device int32): kernels that detect an error at
+ *     run time (a bounded wait that expired, a malformed tree) store the first
+ *     such W12_ERR_* code there; the caller reads it after synchronising.
+ *     The word is never cleared by the library.
+ *   - `ws` / `ws_bytes`: caller-owned device workspace of at least the size
+ *     the matching *_ws_bytes function returns, ZERO-FILLED before its first
+ *     use; the library leaves it zeroed after every successful call, so it can
+ *     be reused. After an error status, zero it again. Calls that share one
+ *     workspace must not overlap in time (same stream, or synchronised).
+ *   - Shapes: N % 128 == 0, K % 128 == 0, 1 <= M <= 256 rows.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  W12_OK = 0,
+  W12_ERR_ARG = 1,        /* null pointer, bad enum, misaligned pointer      */
+  W12_ERR_SHAPE = 2,      /* K or N not a multiple of 128, M outside 1..256  */
+  W12_ERR_WORKSPACE = 3,  /* workspace or exception capacity too small       */
+  W12_ERR_BAD_TREE = 4,   /* parents[0] != -1 or parents[i] not in [0, i)    */
+  W12_ERR_CORRUPT = 5,    /* packed weights fail a consistency check         */
+  W12_ERR_TIMEOUT = 6,    /* a device-side bounded wait expired              */
+  W12_ERR_CUDA = 7,       /* a CUDA runtime call failed                      */
+  W12_ERR_UNSUPPORTED = 8 /* no sm_103a device, or the shape needs a feature
+                             this build does not have                        */
+};
+
+/* W12-packed weight matrix: plain data holding device pointers.
+ *   p0, p1, p2 : N*K/2 bytes each, 16-byte aligned
+ *   ebase      : (K/128)*N bytes
+ *   exc_off    : (N/128)*(K/128) + 1 uint32
+ *   exc_ent    : n_exc uint32 (capacity when passed to w12_pack) */
+typedef struct w12_weights {
+  int64_t N, K;
+  uint8_t* p0;
+  uint8_t* p1;
+  uint8_t* p2;
+  uint8_t* ebase;
+  uint32_t* exc_off;
+  uint32_t* exc_ent;
+  int64_t n_exc;
+} w12_weights;
+
+/* Byte sizes of the buffers of a packed N x K matrix (host struct). */
+typedef struct w12_sizes {
+  int64_t plane_bytes;    /* per plane: N*K/2                     */
+  int64_t ebase_bytes;    /* (K/128)*N                            */
+  int64_t exc_off_count;  /* (N/128)*(K/128) + 1                  */
+  int64_t n_exc;          /* exception entries of this matrix     */
+  int64_t total_bytes;    /* 1.5NK + NK/128 + 4*(U+1) + 4*n_exc   */
+} w12_sizes;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* w12_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int w12_version(void);
+
+/* --- W12 pack / unpack (SpecPilot digest, "Reasons" bullet 2) ----------- */
+
+/* Workspace for w12_pack_query: (N/128)*(K/128)+1 uint32 counters. */
+size_t w12_pack_ws_bytes(int64_t N, int64_t K);
+
+/* Count the exceptions of bf16 W[N, K] (row-major) and fill *out (host).
+ * Synchronises `stream`. */
+int w12_pack_query(const uint16_t* W, int64_t N, int64_t K, w12_sizes* out,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Pack bf16 W[N, K] into *dst (host struct; its buffers sized per
+ * w12_pack_query, dst->n_exc = capacity of dst->exc_ent). On success
+ * dst->n_exc is NOT modified; the exact count is exc_off[U]. Returns
+ * W12_ERR_WORKSPACE if the exceptions exceed the capacity. Synchronises. */
+int w12_pack(const uint16_t* W, int64_t N, int64_t K, const w12_weights* dst, void* stream);
+
+/* Restore bf16 W_out[N, K] bit-exactly from a packed matrix. */
+int w12_unpack(const w12_weights* src, uint16_t* W_out, void* stream);
+
+/* --- Verify GEMM (SpecPilot digest, summary; "Reasons" bullet 2) -------- */
+
+/* Workspace bytes for w12_gemm / w12_gemm_bf16_ref at this shape. */
+size_t w12_gemm_ws_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Y[M, N] (fp32, row-major) = X[M, K] (bf16, row-major) * W^T, W restored
+ * from its three planes inside the kernel. X must be 16-byte aligned. */
+int w12_gemm(const uint16_t* X, int64_t M, const w12_weights* W, float* Y,
+             void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Same product with W given as plain bf16 [N, K] (the in-tree BF16 baseline
+ * that shows what the 12/16 byte saving is worth). */
+int w12_gemm_bf16_ref(const uint16_t* X, int64_t M, const uint16_t* W, int64_t N, int64_t K,
+                      float* Y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* --- Greedy block verification (SpecPilot digest, "Risks" bullet 3) ----- */
+
+/* Workspace bytes for the verify entry points with M = B*rows verified rows
+ * over a vocabulary of V (V % 128 == 0 for the fused forms). */
+size_t w12_verify_ws_bytes(int64_t M, int64_t V);
+
+/* logits [B*T_rows, V] fp32. Row j of request b is the target's prediction
+ * for draft token j. accept_len[b] = longest L <= T with
+ * draft[b, j] == argmax(row b*T_rows + j) for all j < L; bonus[b] =
+ * argmax(row b*T_rows + L) if L < T_rows, else -1. Argmax ties resolve to the
+ * lowest index. T_rows is T or T+1. argmax_out [B*T_rows] is optional. */
+int w12_verify_greedy(const float* logits, int64_t V, const int32_t* draft, int B, int T, int T_rows,
+                      int32_t* accept_len, int32_t* bonus, int32_t* argmax_out,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Same, with the logits computed on the fly by the W12 LM head:
+ * H [B*T_rows, K] bf16 hidden states, head = W12 [V, K]. The logits are never
+ * written to memory; each 128-row vocabulary tile reduces to a per-row
+ * (max, index) pair inside the GEMM epilogue. */
+int w12_verify_greedy_fused(const uint16_t* H, const w12_weights* head, const int32_t* draft,
+                            int B, int T, int T_rows, int32_t* accept_len, int32_t* bonus,
+                            int32_t* argmax_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                            void* stream);
+
+/* --- Tree verification (JetSpec article, "Technical architecture";
+ *     SpecPilot digest, "Reasons" bullet 2) ------------------------------- */
+
+/* B trees of T nodes; node 0 of each tree is the committed anchor, parents
+ * [B, T] with parents[b, 0] = -1 and 0 <= parents[b, i] < i. Row b*T + p of
+ * logits [B*T, V] is the target's prediction after the path root..p. Node
+ * i > 0 is accepted iff its parent is accepted and draft[b, i] equals the
+ * argmax of its parent's row. Output per tree: the accepted node of greatest
+ * depth (lowest index among equals): path [B, T] root-first (-1 padded),
+ * path_len [B] = depth + 1, accept_len [B] = depth, bonus [B] = argmax of
+ * that node's row. A malformed tree sets W12_ERR_BAD_TREE in dev_status and
+ * -1 in its outputs. argmax_out [B*T] is optional. */
+int w12_verify_tree(const float* logits, int64_t V, const int32_t* parents, const int32_t* draft,
+                    int B, int T, int32_t* path, int32_t* path_len, int32_t* accept_len,
+                    int32_t* bonus, int32_t* argmax_out, void* ws, size_t ws_bytes,
+                    int32_t* dev_status, void* stream);
+
+/* Same, with the fused W12 LM head over H [B*T, K]. */
+int w12_verify_tree_fused(const uint16_t* H, const w12_weights* head, const int32_t* parents,
+                          const int32_t* draft, int B, int T, int32_t* path, int32_t* path_len,
+                          int32_t* accept_len, int32_t* bonus, int32_t* argmax_out, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* --- Diagnostics -------------------------------------------------------- */
+
+/* Launch a kernel that waits on a barrier nothing arrives at, with a bound of
+ * `limit_us` microseconds; it must store W12_ERR_TIMEOUT in dev_status and
+ * return (no fault, no hang). Used by the failure-detection tests. */
+int w12_selftest_timeout(int32_t* dev_status, int limit_us, void* stream);
+
+/* Bound (microseconds) used by every device-side wait of later launches;
+ * default 2000000. Values below 1 are rejected. */
+int w12_set_wait_limit_us(int64_t limit_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

@@ -1,0 +1,189 @@
+// Shared host code of libw12.so: status strings, device queries, tensor-map
+// encoding, workspace layout, the wait bound and the timeout self-test.
+#include <atomic>
+#include <mutex>
+
+#include "w12_dev.cuh"
+#include "w12_host.h"
+
+namespace w12 {
+
+static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool device_supported() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return major == 10 && minor == 3;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  return fn;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int gemm_shape(int64_t M, int64_t N, int64_t K, GemmShape* s) {
+  if (M < 1 || M > kMaxM || N < kGroup || K < kGroup || N % kGroup || K % kGroup) return W12_ERR_SHAPE;
+  if (N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return W12_ERR_SHAPE;
+  s->M = static_cast<int>(M);
+  s->Mpad = static_cast<int>(round_up(M, 16));
+  s->N = static_cast<int>(N);
+  s->K = static_cast<int>(K);
+  s->KB = static_cast<int>(K / kGroup);
+  s->tiles = static_cast<int>(N / kGroup);
+  s->units = int64_t(s->tiles) * s->KB;
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 256;  // sizing without a device: an upper bound
+  s->grid = static_cast<int>(s->units < sms ? s->units : sms);
+  return W12_OK;
+}
+
+WsLayout ws_layout(const GemmShape& s, int64_t partial_tiles) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += static_cast<size_t>(round_up(static_cast<int64_t>(bytes), 256));
+    return at;
+  };
+  L.counters = take(sizeof(int32_t) * s.tiles);
+  L.parts = take(sizeof(float) * size_t(2) * s.grid * s.Mpad * kGroup);
+  L.amax_val = take(sizeof(float) * size_t(partial_tiles) * s.Mpad);
+  L.amax_idx = take(sizeof(int32_t) * size_t(partial_tiles) * s.Mpad);
+  L.argmax = take(sizeof(int32_t) * s.Mpad);
+  L.done = take(sizeof(int32_t) * 4);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Timeout self-test: a barrier that nothing ever arrives at.
+// ---------------------------------------------------------------------------
+
+__global__ void selftest_timeout_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, limit_ns)) set_status(status, W12_ERR_TIMEOUT);
+  }
+  __syncthreads();
+}
+
+}  // namespace w12
+
+using namespace w12;
+
+extern "C" {
+
+const char* w12_status_string(int status) {
+  switch (status) {
+    case W12_OK: return "ok";
+    case W12_ERR_ARG: return "invalid argument";
+    case W12_ERR_SHAPE: return "unsupported shape (N, K multiples of 128; 1 <= M <= 256)";
+    case W12_ERR_WORKSPACE: return "workspace or exception capacity too small";
+    case W12_ERR_BAD_TREE: return "malformed draft tree (parents[0] != -1 or parents[i] not in [0, i))";
+    case W12_ERR_CORRUPT: return "packed weights failed a consistency check";
+    case W12_ERR_TIMEOUT: return "a device-side bounded wait expired";
+    case W12_ERR_CUDA: return "CUDA runtime error";
+    case W12_ERR_UNSUPPORTED: return "unsupported device or feature (needs an sm_103a GPU)";
+    default: return "unknown status";
+  }
+}
+
+int w12_version(void) { return 100; }
+
+int w12_set_wait_limit_us(int64_t limit_us) {
+  if (limit_us < 1) return W12_ERR_ARG;
+  g_wait_limit_ns.store(static_cast<uint64_t>(limit_us) * 1000ull, std::memory_order_relaxed);
+  return W12_OK;
+}
+
+int w12_selftest_timeout(int32_t* dev_status, int limit_us, void* stream) {
+  if (!dev_status || limit_us < 1) return W12_ERR_ARG;
+  if (!device_supported()) return W12_ERR_UNSUPPORTED;
+  selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_status,
+                                                                           uint64_t(limit_us) * 1000ull);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t w12_gemm_ws_bytes(int64_t M, int64_t N, int64_t K) {
+  GemmShape s;
+  if (gemm_shape(M, N, K, &s) != W12_OK) return 0;
+  return ws_layout(s, 0).total;
+}
+
+size_t w12_verify_ws_bytes(int64_t M, int64_t V) {
+  // The fused head needs the GEMM slots at K >= 128 and per-tile partials;
+  // the logits path needs per-chunk partials. Size for the larger of both.
+  GemmShape s;
+  int64_t Vr = round_up(V < kGroup ? kGroup : V, kGroup);
+  if (gemm_shape(M, Vr, kGroup, &s) != W12_OK) return 0;
+  int sms = device_sm_count();
+  s.grid = sms > 0 ? sms : 256;  // the fused head runs one CTA per SM
+  int64_t parts = s.tiles;
+  return ws_layout(s, parts).total;
+}
+
+}  // extern "C"

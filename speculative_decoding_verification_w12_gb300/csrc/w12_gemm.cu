@@ -1,0 +1,627 @@
+// W12 verify GEMM and the in-tree BF16 baseline on sm_103a.
+//
+// Y[M, N] = X[M, K] * W[N, K]^T with M (verified rows) small: the verify pass
+// streams every target weight to score a 16-token draft block (SpecPilot
+// paper digest, summary paragraph), so the kernel is bound by HBM reads of W.
+// W is stored in W12 and restored bitwise in registers before the tensor-core
+// contraction (SpecPilot digest, "Reasons" bullet 2).
+//
+// Design (one persistent CTA per SM, stream-K over 128x128 units of W):
+//   warp 0      TMA producer: three plane tiles (3 x 128x64 B, 64-byte
+//               swizzle), the 128 ebase bytes, and the X tile (2 boxes of
+//               Mpad x 64 bf16, 128-byte swizzle) per unit into a smem ring.
+//   warp 1      MMA issuer (one thread): swap-AB tcgen05.mma kind::f16,
+//               D[128 x Mpad] (TMEM, fp32) += A[128 x 16] (TMEM, decoded W)
+//               x B[16 x Mpad] (smem, X), 8 instructions per unit.
+//   warp 2      TMEM allocation / release.
+//   warp 3      stages the CTA's exception offsets and entries in smem.
+//   warps 4-11  decode: each thread restores half a row (64 values) of the
+//               unit from the planes (LDS.128), patches exceptions in
+//               registers, and writes bf16 pairs into TMEM (tcgen05.st).
+//   warps 12-15 epilogue: tcgen05.ld of the accumulator; unsplit tiles write
+//               Y directly; split tiles write partial slots and the last CTA
+//               to arrive sums them in a fixed order (deterministic).
+// The BF16 baseline uses the same skeleton with A loaded by TMA into smem.
+// In argmax mode (fused LM head) the epilogue reduces each 128-row vocab
+// tile to a per-row (max, index) pair instead of writing logits.
+#include "w12_dev.cuh"
+#include "w12_host.h"
+
+namespace w12 {
+
+constexpr int kNA = 4;                // TMEM A buffers (W12 mode)
+constexpr int kAColBase = 256;        // TMEM column of A buffer 0
+constexpr int kAColsPerBuf = 64;      // 128 K values = 64 columns of bf16 pairs
+constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
+constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
+constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
+
+struct GemmParams {
+  int M, Mpad, N, K, KB, tiles, grid, stages;
+  int64_t units;
+  const uint8_t* ebase;
+  const uint32_t* exc_off;
+  const uint32_t* exc_ent;
+  int64_t n_exc;
+  float* Y;
+  float* parts;
+  int32_t* counters;
+  float* amax_val;
+  int32_t* amax_idx;
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
+template <bool kW12>
+struct Cfg {
+  static constexpr int kDecWarps = kW12 ? 8 : 0;
+  static constexpr int kEpiWarp0 = 4 + kDecWarps;
+  static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+  static constexpr uint32_t kABytes = kW12 ? 3 * 8192 : 2 * 16384;  // A operand bytes per stage
+  static constexpr uint32_t kEbBytes = kW12 ? 1024 : 0;             // ebase (128 B used)
+  static constexpr uint32_t kTmemCols = kW12 ? 512 : 256;
+};
+
+// Shared memory carve-up (identical on host and device).
+struct SmemPlan {
+  uint32_t stage_bytes, x_off, eb_off, stages;
+  uint32_t scratch_off, red_off, soff_off, sent_off, bar_off, misc_off, total;
+};
+
+template <bool kW12>
+__host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
+  SmemPlan p;
+  p.eb_off = Cfg<kW12>::kABytes;
+  p.x_off = p.eb_off + Cfg<kW12>::kEbBytes;
+  p.stage_bytes = p.x_off + 2u * Mpad * 128u;
+  p.stages = stages;
+  uint32_t off = p.stage_bytes * stages;
+  p.scratch_off = off;
+  off += 16 * kScratchStride * 4;
+  p.red_off = off;
+  off += 4 * 16 * 8;
+  p.soff_off = off;
+  off += kW12 ? (kOffCap + 4) * 4 : 0;
+  p.sent_off = off;
+  off += kW12 ? kEntCap * 4 : 0;
+  off = (off + 15) & ~15u;
+  p.bar_off = off;
+  off += 64 * 8;
+  p.misc_off = off;
+  off += 64;
+  p.total = off + 1024;  // slack for 1024-byte alignment of the base
+  return p;
+}
+
+__device__ __forceinline__ int64_t unit_begin(int c, int64_t U, int G) { return int64_t(c) * U / G; }
+
+// CTA that owns unit u: the largest c with floor(c*U/G) <= u.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G) {
+  return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
+}
+
+struct Bars {
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* a_full;
+  uint64_t* a_empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* exc_ready;
+  uint64_t* drain;
+};
+
+template <bool kW12, bool kArgmax>
+__global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_x,
+                const GemmParams P) {
+  using C = Cfg<kW12>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SmemPlan plan = smem_plan<kW12>(P.Mpad, P.stages);
+  const int S = P.stages;
+  const int NACC = P.Mpad <= 128 ? 2 : 1;
+
+  uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
+  Bars B;
+  B.full = bar_base;
+  B.empty = bar_base + S;
+  B.a_full = bar_base + 2 * S;
+  B.a_empty = B.a_full + kNA;
+  B.acc_full = B.a_empty + kNA;
+  B.acc_empty = B.acc_full + 2;
+  B.exc_ready = B.acc_empty + 2;
+  B.drain = B.exc_ready + 1;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + plan.misc_off);
+  volatile uint32_t* tmem_slot = misc + 0;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 2);
+  volatile int* ent_in_smem = reinterpret_cast<volatile int*>(misc + 3);
+  volatile uint32_t* ent_base = misc + 4;
+  volatile uint32_t* ent_end = misc + 5;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int64_t U = P.units;
+  const int G = P.grid;
+  const int64_t ub = unit_begin(c, U, G), ue = unit_begin(c + 1, U, G);
+  const int KB = P.KB;
+  const uint64_t lim = P.limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&B.full[s], 1);
+      mbar_init(&B.empty[s], 1);
+    }
+    for (int a = 0; a < kNA; ++a) {
+      mbar_init(&B.a_full[a], C::kDecWarps * 32);
+      mbar_init(&B.a_empty[a], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&B.acc_full[a], 1);
+      mbar_init(&B.acc_empty[a], 128);
+    }
+    mbar_init(B.exc_ready, 1);
+    mbar_init(B.drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(const_cast<uint32_t*>(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&](int code) {
+    set_status(P.status, code);
+    *abort_flag = 1;
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < 0x80000000u; ++i) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 63u) == 63u) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > lim) {
+          fail(W12_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+    fail(W12_ERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      prefetch_tmap(&tm_x);
+      prefetch_tmap(&tm_a0);
+      if (kW12) {
+        prefetch_tmap(&tm_a1);
+        prefetch_tmap(&tm_a2);
+      }
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t xbox = uint32_t(P.Mpad) * 128u;
+      const uint32_t tx = C::kABytes + (kW12 ? 128u : 0u) + 2u * xbox;
+      int64_t issued = 0;
+      for (int64_t u = ub; u < ue; ++u, ++issued) {
+        const int64_t i = u - ub;
+        const int s = int(i % S);
+        const uint32_t ph = uint32_t(i / S) & 1u;
+        if (!wait(&B.empty[s], ph ^ 1u)) break;
+        const int t = int(u / KB), kb = int(u % KB);
+        uint8_t* st = smem + size_t(s) * plan.stage_bytes;
+        mbar_arrive_expect_tx(&B.full[s], tx);
+        if (kW12) {
+          tma_load_2d_hint(st, &tm_a0, kb * 64, t * 128, &B.full[s], pol_w);
+          tma_load_2d_hint(st + 8192, &tm_a1, kb * 64, t * 128, &B.full[s], pol_w);
+          tma_load_2d_hint(st + 16384, &tm_a2, kb * 64, t * 128, &B.full[s], pol_w);
+          bulk_load(st + plan.eb_off, P.ebase + int64_t(kb) * P.N + int64_t(t) * 128, 128u, &B.full[s]);
+        } else {
+          tma_load_2d_hint(st, &tm_a0, kb * 128, t * 128, &B.full[s], pol_w);
+          tma_load_2d_hint(st + 16384, &tm_a0, kb * 128 + 64, t * 128, &B.full[s], pol_w);
+        }
+        tma_load_2d_hint(st + plan.x_off, &tm_x, kb * 128, 0, &B.full[s], pol_x);
+        tma_load_2d_hint(st + plan.x_off + xbox, &tm_x, kb * 128 + 64, 0, &B.full[s], pol_x);
+      }
+      if (*abort_flag) {
+        // Let the copies already issued land before the CTA can exit.
+        const int64_t lo = issued > S ? issued - S : 0;
+        for (int64_t i = lo; i < issued; ++i)
+          mbar_wait(&B.full[int(i % S)], uint32_t(i / S) & 1u, lim);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, uint32_t(P.Mpad));
+      const uint32_t xbox = uint32_t(P.Mpad) * 128u;
+      int64_t seg = -1;
+      bool ok = true;
+      for (int64_t u = ub; u < ue && ok; ++u) {
+        const int64_t i = u - ub;
+        const bool first = (u == ub) || (u % KB == 0);
+        const bool last = (u + 1 == ue) || ((u + 1) % KB == 0);
+        if (first) {
+          ++seg;
+          if (!wait(&B.acc_empty[seg % NACC], (uint32_t(seg / NACC) & 1u) ^ 1u)) break;
+          tc_fence_after();
+        }
+        const int s = int(i % S);
+        if (!wait(&B.full[s], uint32_t(i / S) & 1u)) break;
+        const int ab = int(i % kNA);
+        if (kW12 && !wait(&B.a_full[ab], uint32_t(i / kNA) & 1u)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(seg % NACC) * uint32_t(P.Mpad);
+        const uint32_t st = smem_u32(smem + size_t(s) * plan.stage_bytes);
+        const uint32_t xs = st + plan.x_off;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bdesc = sdesc_k_sw128(xs + uint32_t(kk >> 2) * xbox + uint32_t(kk & 3) * 32u);
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+          if (kW12) {
+            mma_bf16_ts(d_tmem, tmem_base + kAColBase + uint32_t(ab * kAColsPerBuf + kk * 8), bdesc, idesc, acc);
+          } else {
+            const uint64_t adesc = sdesc_k_sw128(st + uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u);
+            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, acc);
+          }
+        }
+        tc_commit(&B.empty[s]);
+        if (kW12) tc_commit(&B.a_empty[ab]);
+        if (last) tc_commit(&B.acc_full[seg % NACC]);
+      }
+      // Make sure no MMA is in flight before TMEM is released.
+      tc_commit(B.drain);
+      mbar_wait(B.drain, 0, lim);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------- exception metadata (W12)
+    if (kW12) {
+      uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
+      uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
+      const int64_t nwin = ue - ub + 1;  // host guarantees nwin <= kOffCap
+      for (int64_t k = lane; k < nwin; k += 32) soff[k] = P.exc_off[ub + k];
+      __syncwarp();
+      const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
+      bool bad = e1 < e0 || int64_t(e1) > P.n_exc;
+      const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
+      if (fits) {
+        for (uint32_t k = lane; k < e1 - e0; k += 32) sent[k] = P.exc_ent[e0 + k];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (bad) set_status(P.status, W12_ERR_CORRUPT);
+        *ent_in_smem = fits ? 1 : 0;
+        *ent_base = e0;
+        *ent_end = bad ? e0 : e1;
+        mbar_arrive(B.exc_ready);
+      }
+    }
+  } else if (kW12 && warp >= 4 && warp < 4 + C::kDecWarps) {
+    // --------------------------------------------------------------- decode
+    const int dw = warp - 4;
+    const int q = warp & 3;          // TMEM lane quarter of this warp
+    const int h = dw >> 2;           // which 64-value half of the unit row
+    const int row = q * 32 + lane;   // W row within the unit
+    const uint32_t tm_lane = uint32_t(q * 32) << 16;
+    const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
+    const uint32_t* sent = reinterpret_cast<const uint32_t*>(smem + plan.sent_off);
+    bool ok = wait(B.exc_ready, 0);
+    const bool in_smem = ok && *ent_in_smem;
+    const uint32_t e_base = *ent_base;
+    const uint32_t e_end = *ent_end;
+    for (int64_t u = ub; u < ue && ok; ++u) {
+      const int64_t i = u - ub;
+      const int s = int(i % S);
+      const int ab = int(i % kNA);
+      if (!wait(&B.full[s], uint32_t(i / S) & 1u)) break;
+      if (!wait(&B.a_empty[ab], (uint32_t(i / kNA) & 1u) ^ 1u)) break;
+      tc_fence_after();
+      const uint8_t* st = smem + size_t(s) * plan.stage_bytes;
+      const uint32_t eb = st[plan.eb_off + row];
+      const uint32_t E2 = (eb << 7) * 0x00010001u;
+
+      // Exceptions of this unit that fall in this warp's rows and half.
+      uint32_t o0 = soff[i], o1 = soff[i + 1];
+      if (o1 < o0 || int64_t(o1) > P.n_exc || o0 < e_base || o1 > e_end) {
+        if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
+        o1 = o0;
+      }
+      const uint32_t nex = o1 - o0;
+      uint32_t ent = kInvalidEnt, m0 = 0, m1 = 0;
+      if (nex > 0) {
+        if (uint32_t(lane) < nex)
+          ent = in_smem ? sent[o0 - e_base + lane] : __ldg(P.exc_ent + o0 + lane);
+        const bool mine = ent != kInvalidEnt && ((ent >> 28) & 3u) == uint32_t(q);
+        const uint32_t ch = (ent >> 21) & 3u;
+        m0 = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(2 * h));
+        m1 = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(2 * h + 1));
+      }
+
+      const uint8_t* pl = st + row * 64;
+      const uint32_t swz = uint32_t(row >> 1) & 3u;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t lc = uint32_t(2 * h + cc);
+        const uint32_t off = ((lc ^ swz) << 4);
+        const uint4 a = *reinterpret_cast<const uint4*>(pl + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(pl + 8192 + off);
+        const uint4 g = *reinterpret_cast<const uint4*>(pl + 16384 + off);
+        uint32_t w[16];
+        decode8(a.x, b.x, g.x, E2, w + 0);
+        decode8(a.y, b.y, g.y, E2, w + 4);
+        decode8(a.z, b.z, g.z, E2, w + 8);
+        decode8(a.w, b.w, g.w, E2, w + 12);
+        uint32_t mk = cc ? m1 : m0;
+        while (mk) {
+          const int src = __ffs(mk) - 1;
+          mk &= mk - 1;
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, ent, src);
+          if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+        }
+        if (nex > 32) {
+          // Rare: more than 32 exceptions in the unit; walk the rest in batches.
+          for (uint32_t bst = o0 + 32; bst < o1; bst += 32) {
+            uint32_t e2 = kInvalidEnt;
+            if (bst + lane < o1) e2 = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
+            const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
+            uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
+            while (mk2) {
+              const int src = __ffs(mk2) - 1;
+              mk2 &= mk2 - 1;
+              const uint32_t e = __shfl_sync(0xFFFFFFFFu, e2, src);
+              if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+            }
+          }
+        }
+        tmem_st16(tmem_base + tm_lane + kAColBase + uint32_t(ab * kAColsPerBuf) + lc * 16u, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&B.a_full[ab]);
+    }
+  } else if (warp >= C::kEpiWarp0) {
+    // ------------------------------------------------------------- epilogue
+    const int ew = warp & 3;            // TMEM lane quarter
+    const int row = ew * 32 + lane;
+    const uint32_t tm_lane = uint32_t(ew * 32) << 16;
+    const int et = threadIdx.x - C::kEpiWarp0 * 32;  // 0..127
+    float* scratch = reinterpret_cast<float*>(smem + plan.scratch_off);
+    float* red_v = reinterpret_cast<float*>(smem + plan.red_off);
+    int32_t* red_i = reinterpret_cast<int32_t*>(smem + plan.red_off + 4 * 16 * 4);
+    const int first_tile = int(ub / KB);
+    const int nchunks = P.Mpad / 16;
+
+    // Tile argmax over a 16-column chunk: v[r] = logit of vocab row `row`
+    // for token mc*16 + r. Lowest vocab index wins ties.
+    auto argmax_chunk = [&](const float (&v)[16], int t, int mc) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) scratch[r * kScratchStride + row] = v[r];
+      named_bar_sync(kEpiBar, 128);
+      if (lane < 16) {
+        const float* col = scratch + lane * kScratchStride + ew * 32;
+        float best = col[0];
+        int bi = 0;
+        for (int k = 1; k < 32; ++k) {
+          const float x = col[k];
+          if (x > best) {
+            best = x;
+            bi = k;
+          }
+        }
+        red_v[ew * 16 + lane] = best;
+        red_i[ew * 16 + lane] = ew * 32 + bi;
+      }
+      named_bar_sync(kEpiBar, 128);
+      if (ew == 0 && lane < 16) {
+        float best = red_v[lane];
+        int bi = red_i[lane];
+        for (int w2 = 1; w2 < 4; ++w2) {
+          const float x = red_v[w2 * 16 + lane];
+          if (x > best) {
+            best = x;
+            bi = red_i[w2 * 16 + lane];
+          }
+        }
+        const int m = mc * 16 + lane;
+        P.amax_val[int64_t(t) * P.Mpad + m] = best;
+        P.amax_idx[int64_t(t) * P.Mpad + m] = t * 128 + bi;
+      }
+      named_bar_sync(kEpiBar, 128);
+    };
+    auto store_chunk = [&](const float (&v)[16], int t, int mc) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int m = mc * 16 + r;
+        if (m < P.M) P.Y[int64_t(m) * P.N + int64_t(t) * 128 + row] = v[r];
+      }
+    };
+
+    int64_t seg = 0;
+    for (int64_t u = ub; u < ue; ++seg) {
+      const int t = int(u / KB);
+      const int64_t seg_end = (int64_t(t) + 1) * KB < ue ? (int64_t(t) + 1) * KB : ue;
+      u = seg_end;
+      const int accb = int(seg % NACC);
+      if (!wait(&B.acc_full[accb], uint32_t(seg / NACC) & 1u)) break;
+      tc_fence_after();
+      const int c_first = unit_owner(int64_t(t) * KB, U, G);
+      const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
+      const int nsplit = c_last - c_first + 1;
+      const uint32_t d_tmem = tmem_base + tm_lane + uint32_t(accb) * uint32_t(P.Mpad);
+      if (nsplit == 1) {
+        for (int mc = 0; mc < nchunks; ++mc) {
+          uint32_t r[16];
+          tmem_ld16(d_tmem + uint32_t(mc * 16), r);
+          tmem_ld_wait(r);
+          float v[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+          if (kArgmax) argmax_chunk(v, t, mc);
+          else store_chunk(v, t, mc);
+        }
+        tc_fence_before();
+        mbar_arrive(&B.acc_empty[accb]);
+      } else {
+        const int slot = 2 * c + (t == first_tile ? 0 : 1);
+        float* my = P.parts + size_t(slot) * P.Mpad * 128;
+        for (int mc = 0; mc < nchunks; ++mc) {
+          uint32_t r[16];
+          tmem_ld16(d_tmem + uint32_t(mc * 16), r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) my[(mc * 16 + k) * 128 + row] = __uint_as_float(r[k]);
+        }
+        tc_fence_before();
+        mbar_arrive(&B.acc_empty[accb]);
+        __threadfence();
+        named_bar_sync(kEpiBar, 128);
+        if (et == 0) {
+          const int old = atomicAdd(&P.counters[t], 1);
+          *last_flag = (old == nsplit - 1) ? 1 : 0;
+        }
+        named_bar_sync(kEpiBar, 128);
+        if (*last_flag) {
+          __threadfence();
+          for (int mc = 0; mc < nchunks; ++mc) {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = 0.0f;
+            for (int sp = 0; sp < nsplit; ++sp) {
+              const int cc = c_first + sp;
+              const int ft = int(unit_begin(cc, U, G) / KB);
+              const int sl = 2 * cc + (t == ft ? 0 : 1);
+              const float* pp = P.parts + size_t(sl) * P.Mpad * 128;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) v[k] += __ldcg(pp + (mc * 16 + k) * 128 + row);
+            }
+            if (kArgmax) argmax_chunk(v, t, mc);
+            else store_chunk(v, t, mc);
+          }
+          if (et == 0) P.counters[t] = 0;
+        }
+        named_bar_sync(kEpiBar, 128);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <bool kW12, bool kArgmax>
+static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensorMap& a0, const CUtensorMap& a1,
+                       const CUtensorMap& a2, const CUtensorMap& x, cudaStream_t stream) {
+  GemmParams P = P0;
+  // Deepest ring that fits next to the fixed carve-up.
+  const int smem_max = 232448;
+  int stages = 8;
+  while (stages > 2 && smem_plan<kW12>(sh.Mpad, stages).total > uint32_t(smem_max)) --stages;
+  const SmemPlan plan = smem_plan<kW12>(sh.Mpad, stages);
+  if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
+  P.stages = stages;
+  auto kern = gemm_kernel<kW12, kArgmax>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
+    return W12_ERR_CUDA;
+  kern<<<P.grid, Cfg<kW12>::kThreads, plan.total, stream>>>(a0, a1, a2, x, P);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, const w12_weights* W,
+                const uint16_t* Wbf16, int64_t N, int64_t K, float* Y, float* amax_val, int32_t* amax_idx,
+                void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  GemmShape sh;
+  int st = gemm_shape(M, N, K, &sh);
+  if (st) return st;
+  if (!X || !aligned(X, 16) || !ws) return W12_ERR_ARG;
+  if (argmax_mode ? (!amax_val || !amax_idx) : !Y) return W12_ERR_ARG;
+  if (w12_mode) {
+    if (!W || !W->p0 || !W->p1 || !W->p2 || !W->ebase || !W->exc_off) return W12_ERR_ARG;
+    if (W->n_exc > 0 && !W->exc_ent) return W12_ERR_ARG;
+    if (!aligned(W->p0, 16) || !aligned(W->p1, 16) || !aligned(W->p2, 16) || !aligned(W->ebase, 16))
+      return W12_ERR_ARG;
+  } else {
+    if (!Wbf16 || !aligned(Wbf16, 16)) return W12_ERR_ARG;
+  }
+  if (!device_supported()) return W12_ERR_UNSUPPORTED;
+  if (w12_mode && (sh.units + sh.grid - 1) / sh.grid + 1 > kOffCap) return W12_ERR_SHAPE;
+  const WsLayout L = ws_layout(sh, 0);
+  if (ws_bytes < L.total) return W12_ERR_WORKSPACE;
+
+  GemmParams P{};
+  P.M = sh.M;
+  P.Mpad = sh.Mpad;
+  P.N = sh.N;
+  P.K = sh.K;
+  P.KB = sh.KB;
+  P.tiles = sh.tiles;
+  P.grid = sh.grid;
+  P.units = sh.units;
+  P.ebase = w12_mode ? W->ebase : nullptr;
+  P.exc_off = w12_mode ? W->exc_off : nullptr;
+  P.exc_ent = w12_mode ? W->exc_ent : nullptr;
+  P.n_exc = w12_mode ? W->n_exc : 0;
+  P.Y = Y;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  P.counters = reinterpret_cast<int32_t*>(wsb + L.counters);
+  P.parts = reinterpret_cast<float*>(wsb + L.parts);
+  P.amax_val = amax_val;
+  P.amax_idx = amax_idx;
+  P.status = dev_status;
+  P.limit_ns = wait_limit_ns();
+
+  CUtensorMap tx, t0, t1, t2;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(X), uint64_t(K), uint64_t(M),
+                      uint64_t(K) * 2, 64, uint32_t(sh.Mpad), CU_TENSOR_MAP_SWIZZLE_128B))
+    return W12_ERR_CUDA;
+  if (w12_mode) {
+    const uint64_t half = uint64_t(K) / 2;
+    if (!encode_tmap_2d(&t0, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p0, half, uint64_t(N), half, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_tmap_2d(&t1, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p1, half, uint64_t(N), half, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_tmap_2d(&t2, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p2, half, uint64_t(N), half, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_64B))
+      return W12_ERR_CUDA;
+    return argmax_mode ? launch_impl<true, true>(sh, P, t0, t1, t2, tx, stream)
+                       : launch_impl<true, false>(sh, P, t0, t1, t2, tx, stream);
+  }
+  if (!encode_tmap_2d(&t0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(Wbf16), uint64_t(K),
+                      uint64_t(N), uint64_t(K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return W12_ERR_CUDA;
+  if (argmax_mode) return W12_ERR_UNSUPPORTED;
+  return launch_impl<false, false>(sh, P, t0, t0, t0, tx, stream);
+}
+
+}  // namespace w12
+
+using namespace w12;
+
+extern "C" {
+
+int w12_gemm(const uint16_t* X, int64_t M, const w12_weights* W, float* Y, void* ws, size_t ws_bytes,
+             int32_t* dev_status, void* stream) {
+  if (!W) return W12_ERR_ARG;
+  return launch_gemm(true, false, X, M, W, nullptr, W->N, W->K, Y, nullptr, nullptr, ws, ws_bytes, dev_status,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int w12_gemm_bf16_ref(const uint16_t* X, int64_t M, const uint16_t* W, int64_t N, int64_t K, float* Y, void* ws,
+                      size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return launch_gemm(false, false, X, M, nullptr, W, N, K, Y, nullptr, nullptr, ws, ws_bytes, dev_status,
+                     static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

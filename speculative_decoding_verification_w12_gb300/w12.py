@@ -1,0 +1,282 @@
+"""Thin ctypes binding of libw12.so (the C ABI declared in include/w12.h).
+
+Argument marshalling only: every step of the verify path runs in the
+library's CUDA kernels. PyTorch supplies device memory and the current
+stream. There is no fallback: if the library is missing or was built for a
+different GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libw12.so")
+
+W12_OK = 0
+ERRORS = {1: "ARG", 2: "SHAPE", 3: "WORKSPACE", 4: "BAD_TREE", 5: "CORRUPT", 6: "TIMEOUT", 7: "CUDA",
+          8: "UNSUPPORTED"}
+
+EXPORTS = [
+    "w12_status_string", "w12_version", "w12_pack_ws_bytes", "w12_pack_query", "w12_pack", "w12_unpack",
+    "w12_gemm_ws_bytes", "w12_gemm", "w12_gemm_bf16_ref", "w12_verify_ws_bytes", "w12_verify_greedy",
+    "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
+    "w12_set_wait_limit_us",
+]
+
+
+class W12Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: W12_ERR_{ERRORS.get(code, code)} ({status_string(code)})")
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("p0", ctypes.c_void_p), ("p1", ctypes.c_void_p),
+                ("p2", ctypes.c_void_p), ("ebase", ctypes.c_void_p), ("exc_off", ctypes.c_void_p),
+                ("exc_ent", ctypes.c_void_p), ("n_exc", ctypes.c_int64)]
+
+
+class _Sizes(ctypes.Structure):
+    _fields_ = [("plane_bytes", ctypes.c_int64), ("ebase_bytes", ctypes.c_int64),
+                ("exc_off_count", ctypes.c_int64), ("n_exc", ctypes.c_int64), ("total_bytes", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libw12.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "or python -m speculative_decoding_verification_w12_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "w12_status_string": (ctypes.c_char_p, [i32]),
+            "w12_version": (i32, []),
+            "w12_pack_ws_bytes": (sz, [i64, i64]),
+            "w12_pack_query": (i32, [vp, i64, i64, ctypes.POINTER(_Sizes), vp, sz, vp]),
+            "w12_pack": (i32, [vp, i64, i64, ctypes.POINTER(_Weights), vp]),
+            "w12_unpack": (i32, [ctypes.POINTER(_Weights), vp, vp]),
+            "w12_gemm_ws_bytes": (sz, [i64, i64, i64]),
+            "w12_gemm": (i32, [vp, i64, ctypes.POINTER(_Weights), vp, vp, sz, vp, vp]),
+            "w12_gemm_bf16_ref": (i32, [vp, i64, vp, i64, i64, vp, vp, sz, vp, vp]),
+            "w12_verify_ws_bytes": (sz, [i64, i64]),
+            "w12_verify_greedy": (i32, [vp, i64, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
+            "w12_verify_greedy_fused": (i32, [vp, ctypes.POINTER(_Weights), vp, i32, i32, i32, vp, vp, vp, vp, sz,
+                                              vp, vp]),
+            "w12_verify_tree": (i32, [vp, i64, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
+            "w12_verify_tree_fused": (i32, [vp, ctypes.POINTER(_Weights), vp, vp, i32, i32, vp, vp, vp, vp, vp, vp,
+                                            sz, vp, vp]),
+            "w12_selftest_timeout": (i32, [vp, i32, vp]),
+            "w12_set_wait_limit_us": (i32, [i64]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().w12_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != W12_OK:
+        raise W12Error(code, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bits16(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("bf16 data must be a bfloat16 (or 16-bit integer bit-pattern) tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled device workspace (the library leaves it zeroed after each call)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class W12Weights:
+    """A W12-packed [N, K] matrix held in torch device tensors."""
+    N: int
+    K: int
+    p0: torch.Tensor
+    p1: torch.Tensor
+    p2: torch.Tensor
+    ebase: torch.Tensor
+    exc_off: torch.Tensor
+    exc_ent: torch.Tensor
+    n_exc: int
+
+    def struct(self) -> _Weights:
+        return _Weights(self.N, self.K, self.p0.data_ptr(), self.p1.data_ptr(), self.p2.data_ptr(),
+                        self.ebase.data_ptr(), self.exc_off.data_ptr(),
+                        self.exc_ent.data_ptr() if self.exc_ent.numel() else None, self.n_exc)
+
+    @property
+    def nbytes(self) -> int:
+        """Bytes a GEMM streams: the three planes and the group offsets."""
+        return 3 * self.N * self.K // 2 + self.N * self.K // 128
+
+    @property
+    def total_bytes(self) -> int:
+        return self.nbytes + 4 * self.exc_off.numel() + 4 * self.n_exc
+
+
+def pack(W: torch.Tensor, stream=None) -> W12Weights:
+    """Pack a bf16 [N, K] device matrix into W12 (bit-exact, synchronises)."""
+    W = _bits16(W)
+    N, K = W.shape
+    dev = W.device
+    ws = torch.zeros(max(int(lib().w12_pack_ws_bytes(N, K)), 4), dtype=torch.uint8, device=dev)
+    sizes = _Sizes()
+    _check(lib().w12_pack_query(W.data_ptr(), N, K, ctypes.byref(sizes), ws.data_ptr(), ws.numel(),
+                                _stream(stream)), "w12_pack_query")
+    n_exc = int(sizes.n_exc)
+    U = (N // 128) * (K // 128)
+    out = W12Weights(
+        N=N, K=K,
+        p0=torch.empty((N, K // 2), dtype=torch.uint8, device=dev),
+        p1=torch.empty((N, K // 2), dtype=torch.uint8, device=dev),
+        p2=torch.empty((N, K // 2), dtype=torch.uint8, device=dev),
+        ebase=torch.empty((K // 128, N), dtype=torch.uint8, device=dev),
+        exc_off=torch.empty(U + 1, dtype=torch.int32, device=dev),
+        exc_ent=torch.empty(max(n_exc, 1), dtype=torch.int32, device=dev),
+        n_exc=n_exc)
+    _check(lib().w12_pack(W.data_ptr(), N, K, ctypes.byref(out.struct()), _stream(stream)), "w12_pack")
+    return out
+
+
+def unpack(w: W12Weights, stream=None) -> torch.Tensor:
+    out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=w.p0.device)
+    _check(lib().w12_unpack(ctypes.byref(w.struct()), out.data_ptr(), _stream(stream)), "w12_unpack")
+    return out
+
+
+def gemm_ws_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().w12_gemm_ws_bytes(M, N, K))
+
+
+def verify_ws_bytes(M: int, V: int) -> int:
+    return int(lib().w12_verify_ws_bytes(M, V))
+
+
+def gemm(X: torch.Tensor, w: W12Weights, Y: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+         status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[M, N] fp32 = X[M, K] (bf16) * W^T with W in W12."""
+    X = _bits16(X)
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, w.N), dtype=torch.float32, device=X.device)
+    if ws is None:
+        ws = workspace(gemm_ws_bytes(M, w.N, w.K), X.device)
+    _check(lib().w12_gemm(X.data_ptr(), M, ctypes.byref(w.struct()), Y.data_ptr(), ws.data_ptr(), ws.numel(),
+                          _ptr(status), _stream(stream)), "w12_gemm")
+    return Y
+
+
+def gemm_bf16_ref(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                  status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[M, N] fp32 = X[M, K] * W[N, K]^T with plain bf16 W (in-tree baseline kernel)."""
+    X, W = _bits16(X), _bits16(W)
+    M = X.shape[0]
+    N, K = W.shape
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    if ws is None:
+        ws = workspace(gemm_ws_bytes(M, N, K), X.device)
+    _check(lib().w12_gemm_bf16_ref(X.data_ptr(), M, W.data_ptr(), N, K, Y.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   _ptr(status), _stream(stream)), "w12_gemm_bf16_ref")
+    return Y
+
+
+def _i32(n, device):
+    return torch.empty(n, dtype=torch.int32, device=device)
+
+
+def verify_greedy(logits: torch.Tensor, draft: torch.Tensor, T_rows: int, ws=None, status=None, stream=None):
+    """(accept_len[B], bonus[B], argmax[B*T_rows]) from fp32 logits [B*T_rows, V]."""
+    B, T = draft.shape
+    V = logits.shape[1]
+    dev = logits.device
+    acc, bonus, am = _i32(B, dev), _i32(B, dev), _i32(B * T_rows, dev)
+    if ws is None:
+        ws = workspace(verify_ws_bytes(B * T_rows, V), dev)
+    _check(lib().w12_verify_greedy(logits.data_ptr(), V, draft.data_ptr(), B, T, T_rows, acc.data_ptr(),
+                                   bonus.data_ptr(), am.data_ptr(), ws.data_ptr(), ws.numel(), _ptr(status),
+                                   _stream(stream)), "w12_verify_greedy")
+    return acc, bonus, am
+
+
+def verify_greedy_fused(H: torch.Tensor, head: W12Weights, draft: torch.Tensor, T_rows: int, ws=None, status=None,
+                        stream=None, out=None):
+    """Fused W12 LM head + row argmax + greedy acceptance."""
+    H = _bits16(H)
+    B, T = draft.shape
+    dev = H.device
+    acc, bonus, am = out if out is not None else (_i32(B, dev), _i32(B, dev), _i32(B * T_rows, dev))
+    if ws is None:
+        ws = workspace(verify_ws_bytes(B * T_rows, head.N), dev)
+    _check(lib().w12_verify_greedy_fused(H.data_ptr(), ctypes.byref(head.struct()), draft.data_ptr(), B, T, T_rows,
+                                         acc.data_ptr(), bonus.data_ptr(), _ptr(am), ws.data_ptr(), ws.numel(),
+                                         _ptr(status), _stream(stream)), "w12_verify_greedy_fused")
+    return acc, bonus, am
+
+
+def verify_tree(logits: torch.Tensor, parents: torch.Tensor, draft: torch.Tensor, ws=None, status=None, stream=None):
+    """(path[B,T], path_len[B], accept_len[B], bonus[B], argmax[B*T]) from logits [B*T, V]."""
+    B, T = parents.shape
+    V = logits.shape[1]
+    dev = logits.device
+    path, plen, acc, bonus, am = _i32((B, T), dev), _i32(B, dev), _i32(B, dev), _i32(B, dev), _i32(B * T, dev)
+    if ws is None:
+        ws = workspace(verify_ws_bytes(B * T, V), dev)
+    _check(lib().w12_verify_tree(logits.data_ptr(), V, parents.data_ptr(), draft.data_ptr(), B, T, path.data_ptr(),
+                                 plen.data_ptr(), acc.data_ptr(), bonus.data_ptr(), am.data_ptr(), ws.data_ptr(),
+                                 ws.numel(), _ptr(status), _stream(stream)), "w12_verify_tree")
+    return path, plen, acc, bonus, am
+
+
+def verify_tree_fused(H: torch.Tensor, head: W12Weights, parents: torch.Tensor, draft: torch.Tensor, ws=None,
+                      status=None, stream=None):
+    """Fused W12 LM head + row argmax + tree acceptance over H [B*T, K]."""
+    H = _bits16(H)
+    B, T = parents.shape
+    dev = H.device
+    path, plen, acc, bonus, am = _i32((B, T), dev), _i32(B, dev), _i32(B, dev), _i32(B, dev), _i32(B * T, dev)
+    if ws is None:
+        ws = workspace(verify_ws_bytes(B * T, head.N), dev)
+    _check(lib().w12_verify_tree_fused(H.data_ptr(), ctypes.byref(head.struct()), parents.data_ptr(),
+                                       draft.data_ptr(), B, T, path.data_ptr(), plen.data_ptr(), acc.data_ptr(),
+                                       bonus.data_ptr(), am.data_ptr(), ws.data_ptr(), ws.numel(), _ptr(status),
+                                       _stream(stream)), "w12_verify_tree_fused")
+    return path, plen, acc, bonus, am
+
+
+def selftest_timeout(limit_us: int, status: torch.Tensor, stream=None):
+    _check(lib().w12_selftest_timeout(status.data_ptr(), int(limit_us), _stream(stream)), "w12_selftest_timeout")
+
+
+def set_wait_limit_us(limit_us: int):
+    _check(lib().w12_set_wait_limit_us(int(limit_us)), "w12_set_wait_limit_us")

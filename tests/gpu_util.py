@@ -1,0 +1,51 @@
+"""Helpers shared by the GPU parity tests (device transfer and tolerances)."""
+import numpy as np
+import torch
+
+# GEMM agreement with the float64 oracle (fp32 accumulation in any order).
+REL_FRO = 1e-3
+MAX_ABS_OVER_RMS = 1e-2
+NEAR_TIE = 1e-3
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev()).view(torch.bfloat16)
+
+
+def to_dev_i32(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev())
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def packed_to_numpy(pk) -> dict:
+    torch.cuda.synchronize()
+    return dict(p0=pk.p0.cpu().numpy(), p1=pk.p1.cpu().numpy(), p2=pk.p2.cpu().numpy(),
+                ebase=pk.ebase.cpu().numpy(), exc_off=pk.exc_off.cpu().numpy().view(np.uint32),
+                exc_ent=pk.exc_ent.cpu().numpy().view(np.uint32)[:pk.n_exc], n_exc=pk.n_exc)
+
+
+def assert_gemm_close(Y: np.ndarray, Y64: np.ndarray, what=""):
+    Y = np.asarray(Y, dtype=np.float64)
+    err = Y - Y64
+    rel = np.linalg.norm(err) / max(np.linalg.norm(Y64), 1e-300)
+    rms = np.sqrt(np.mean(Y64 ** 2))
+    mx = np.abs(err).max()
+    assert rel <= REL_FRO, f"{what}: rel Frobenius {rel:.3e}"
+    assert mx <= MAX_ABS_OVER_RMS * rms, f"{what}: max abs {mx:.3e} vs rms {rms:.3e}"
+    return rel, mx / rms
+
+
+def new_status():
+    return torch.zeros(1, dtype=torch.int32, device=dev())
+
+
+def status_value(st):
+    torch.cuda.synchronize()
+    return int(st.item())

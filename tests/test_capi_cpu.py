@@ -1,0 +1,78 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+function include/w12.h declares, and validates arguments on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_w12_gb300 import build as B
+from speculative_decoding_verification_w12_gb300 import w12
+
+HEADER = os.path.join(B.ROOT, "include", "w12.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return w12.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(w12_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("w12_pack", "w12_unpack", "w12_gemm", "w12_gemm_bf16_ref", "w12_verify_greedy",
+                     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused"):
+        assert required in names
+    assert set(names) == set(w12.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert L.w12_version() == 100
+    for code in range(0, 9):
+        assert len(w12.status_string(code)) > 0
+    assert w12.status_string(6).startswith("a device-side bounded wait")
+
+
+def test_workspace_sizes(L):
+    assert L.w12_gemm_ws_bytes(16, 7168, 5120) > 0
+    assert L.w12_gemm_ws_bytes(0, 7168, 5120) == 0
+    assert L.w12_gemm_ws_bytes(257, 7168, 5120) == 0
+    assert L.w12_gemm_ws_bytes(16, 7100, 5120) == 0
+    assert L.w12_pack_ws_bytes(1024, 512) == 4 * (8 * 4 + 1)
+    assert L.w12_verify_ws_bytes(256, 151936) > L.w12_verify_ws_bytes(16, 151936)
+
+
+def test_host_validation_without_gpu(L):
+    null = None
+    # Null pointers and bad shapes are rejected before any device call.
+    assert L.w12_gemm(null, 16, null, null, null, 0, null, null) == 1
+    ws = (ctypes.c_uint8 * 64)()
+    wt = w12._Weights(1024, 500, 16, 16, 16, 16, 16, 16, 0)
+    assert L.w12_gemm(ctypes.addressof(ws), 16, ctypes.byref(wt), 16, ctypes.addressof(ws), 64, null,
+                      null) == 2
+    assert L.w12_verify_greedy(16, 4096, 16, 1, 16, 18, 16, 16, null, 16, 64, null, null) == 1
+    assert L.w12_verify_tree(16, 4096, 16, 16, 4, 300, 16, 16, 16, 16, null, 16, 64, null, null) == 1
+    assert L.w12_set_wait_limit_us(0) == 1
+    assert L.w12_set_wait_limit_us(2000000) == 0
+
+
+def test_no_gpu_means_unsupported_not_fallback(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    buf = (ctypes.c_uint8 * 4096)()
+    a = ctypes.addressof(buf)
+    a16 = (a + 15) // 16 * 16
+    sizes = w12._Sizes()
+    assert L.w12_pack_query(a16, 128, 128, ctypes.byref(sizes), a16, 1024, None) == 8
