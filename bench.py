@@ -1,0 +1,424 @@
+"""Benchmark of the W12 verify path on GB300.
+
+One step = one verify pass at batch 1 x 16-token draft block (M = 16 rows):
+the four W12 GEMMs of a 27B-class dense decoder layer (qkv 5120->7168,
+o 5120->5120, gate_up 5120->34816, down 17408->5120) followed by the fused
+W12 LM head (5120->151936) with row argmax and greedy block acceptance.
+Metric: achieved HBM GB/s on the packed W12 weight bytes the step streams
+(plus verified tokens/s). Inputs are seeded synthetic data (weights
+N(0, 0.02) bf16 packed to W12, activations N(0, 1)); the weight working set
+(1.67 GB) is larger than L2, so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_w12_gb300 import synthetic as S  # noqa: E402
+
+METRIC = "W12 verify-GEMM achieved HBM GB/s (fraction of peak) at M=16; verified tokens/s"
+UNIT = "GB/s"
+LAYER = [("qkv", 7168, 5120), ("o", 5120, 5120), ("gate_up", 34816, 5120), ("down", 5120, 17408)]
+HEAD = ("head", 151936, 5120)
+M_ROWS, T_BLOCK = 16, 16
+WORKLOAD = "27B-class dense layer W12 verify GEMMs + fused W12 LM head (V=151936) + greedy accept, M=16"
+
+
+def packed_stream_bytes(N, K):
+    """Bytes a GEMM must stream per call: three 4-bit planes + one ebase byte per 128 values."""
+    return 3 * N * K // 2 + N * K // 128
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (reported baseline; the oracle as it stands)
+# ---------------------------------------------------------------------------
+
+def oracle_sample():
+    """Bounded sample of the step for the CPU oracle: 512 weight rows of each
+    layer GEMM and 1024 vocabulary rows of the head, the same M=16 inputs."""
+    from oracle import w12_oracle as O
+    rows_layer, rows_head = 512, 1024
+    items = []
+    for i, (name, N, K) in enumerate(LAYER):
+        W = S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i, row_blocks=range(rows_layer // 128))
+        items.append((name, O.pack(W), S.activations_bf16(M_ROWS, K, tag=i)))
+    N, K = HEAD[1], HEAD[2]
+    Wh = S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + 10, row_blocks=range(rows_head // 128))
+    items.append(("head", O.pack(Wh), S.activations_bf16(M_ROWS, K, tag=10)))
+    nbytes = sum(packed_stream_bytes(pk["N"], pk["K"]) for _, pk, _ in items)
+    desc = (f"oracle unpack + float64 GEMM on {rows_layer} rows of each layer weight and {rows_head} "
+            f"head rows (argmax + greedy accept on the head sample), M=16; "
+            f"{nbytes / 1e6:.1f} MB packed per sample step")
+    return items, nbytes, desc
+
+
+def oracle_step(items):
+    from oracle import w12_oracle as O
+    out = None
+    for name, pk, X in items:
+        Y = O.gemm(X, pk)
+        if name == "head":
+            am, _ = O.argmax_rows(Y)
+            draft = np.asarray(am[:T_BLOCK], dtype=np.int32).reshape(1, T_BLOCK)
+            out = O.verify_greedy(draft, am, T_BLOCK)
+    return out
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    items, nbytes, desc = oracle_sample()
+    for _ in range(args.warmup):
+        oracle_step(items)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(items)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T_BLOCK, "parallelism": "replicas",
+                       "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+def to_dev_bf16(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    dev = torch.device("cuda", local)
+    w12.lib()
+    stream = torch.cuda.current_stream(dev)
+
+    # Weights: seeded, packed once on the device (offline step, not timed).
+    layer = []
+    for i, (name, N, K) in enumerate(LAYER):
+        pk = w12.pack(to_dev_bf16(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i), dev))
+        X = to_dev_bf16(S.activations_bf16(M_ROWS, K, tag=i), dev)
+        Y = torch.empty((M_ROWS, N), dtype=torch.float32, device=dev)
+        ws = w12.workspace(w12.gemm_ws_bytes(M_ROWS, N, K), dev)
+        layer.append(dict(name=name, N=N, K=K, pk=pk, X=X, Y=Y, ws=ws))
+    Wh_bits = S.weights_bf16(HEAD[1], HEAD[2], seed=S.SEED_WEIGHTS + 10)
+    head = w12.pack(to_dev_bf16(Wh_bits, dev))
+    Wh_bf16 = to_dev_bf16(Wh_bits, dev) if args.bf16_baseline else None
+    del Wh_bits
+    H = to_dev_bf16(S.activations_bf16(M_ROWS, HEAD[2], tag=10), dev)
+    hws = w12.workspace(w12.verify_ws_bytes(M_ROWS, HEAD[1]), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    bonus = torch.empty(1, dtype=torch.int32, device=dev)
+    am = torch.empty(M_ROWS, dtype=torch.int32, device=dev)
+
+    # Plant the draft block against the target's own argmax (from an untimed pass).
+    draft = torch.zeros((1, T_BLOCK), dtype=torch.int32, device=dev)
+    w12.verify_greedy_fused(H, head, draft, T_BLOCK, ws=hws, status=status, out=(acc, bonus, am))
+    torch.cuda.synchronize(dev)
+    L = S.accept_lengths_uniform(1, T_BLOCK, tag=3)
+    draft_np = S.plant_block_drafts(am.cpu().numpy(), 1, T_BLOCK, T_BLOCK, L, HEAD[1])
+    draft.copy_(torch.from_numpy(draft_np))
+
+    layer_bytes = sum(packed_stream_bytes(g["N"], g["K"]) for g in layer)
+    head_bytes = packed_stream_bytes(HEAD[1], HEAD[2])
+    step_bytes = layer_bytes + head_bytes
+    # Algorithmic bytes of the fused head launch: packed weights incl. exception CSR + H + partials.
+    head_alg = (head_bytes + 4 * head.exc_off.numel() + 4 * head.n_exc + M_ROWS * HEAD[2] * 2
+                + (HEAD[1] // 128) * 16 * 8)
+
+    nk = 6  # kernel launches per step: 4 layer GEMMs, fused head GEMM, reduce+accept
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+
+    def step(events=None):
+        if events:
+            events[0].record(stream)
+        for j, g in enumerate(layer):
+            w12.gemm(g["X"], g["pk"], Y=g["Y"], ws=g["ws"], status=status)
+            if events:
+                events[j + 1].record(stream)
+        w12.verify_greedy_fused(H, head, draft, T_BLOCK, ws=hws, status=status, out=(acc, bonus, am))
+        if events:
+            events[nk].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(ev[k])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms, world)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    per = {g["name"]: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j, g in enumerate(layer)}
+    per["head+accept"] = statistics.median(e[4].elapsed_time(e[nk]) for e in ev)
+    layer_ms = statistics.median(e[0].elapsed_time(e[4]) for e in ev)
+
+    # Fused-head kernel alone, timed with events on its stream (for the roofline).
+    hk = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for g in layer:  # evict the head's tail from L2 with other weight traffic
+            w12.gemm(g["X"], g["pk"], Y=g["Y"], ws=g["ws"])
+        a.record(stream)
+        w12.lib().w12_verify_greedy_fused  # noqa: B018 (binding resolved before timing)
+        w12.verify_greedy_fused(H, head, draft, T_BLOCK, ws=hws, status=status, out=(acc, bonus, am))
+        b.record(stream)
+        hk.append((a, b))
+    torch.cuda.synchronize(dev)
+    head_ms = statistics.median(a.elapsed_time(b) for a, b in hk)
+
+    hbm_peak, tc_peak, peak_src = peaks()
+    value = world * step_bytes / (ms * 1e-3) / 1e9
+    accepted = int(acc.item())
+    verified_tokens = accepted + (1 if int(bonus.item()) >= 0 else 0)
+
+    # End to end: host (pinned) inputs -> C-ABI calls -> host results, every step.
+    hx = [g["X"].cpu().pin_memory() for g in layer]
+    hH = H.cpu().pin_memory()
+    hdraft = draft.cpu().pin_memory()
+    hout = torch.empty(2 + M_ROWS, dtype=torch.int32).pin_memory()
+    outbuf = torch.empty(2 + M_ROWS, dtype=torch.int32, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in hx) + hH.numel() * 2 + hdraft.numel() * 4
+    d2h = hout.numel() * 4
+
+    def e2e_step():
+        for g, h in zip(layer, hx):
+            g["X"].copy_(h, non_blocking=True)
+        H.copy_(hH, non_blocking=True)
+        draft.copy_(hdraft, non_blocking=True)
+        step()
+        outbuf[0:1].copy_(acc)
+        outbuf[1:2].copy_(bonus)
+        outbuf[2:].copy_(am)
+        hout.copy_(outbuf, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    bf16_detail = None
+    if args.bf16_baseline:
+        # In-tree BF16 kernel on the same layer shapes (bytes x 16/12).
+        bdet = {}
+        for i, g in enumerate(layer):
+            Wb = to_dev_bf16(S.weights_bf16(g["N"], g["K"], seed=S.SEED_WEIGHTS + i), dev)
+            ts = []
+            for _ in range(args.steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                w12.gemm_bf16_ref(g["X"], Wb, Y=g["Y"], ws=g["ws"])
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize(dev)
+            bdet[g["name"]] = statistics.median(a.elapsed_time(b) for a, b in ts)
+            del Wb
+        bf16_detail = {"ms": bdet, "layer_ms": sum(bdet.values()),
+                       "w12_layer_ms": sum(per[g["name"]] for g in layer)}
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        items, nbytes, desc = oracle_sample()
+        oracle_step(items)
+        reps = 3
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle_step(items)
+        dt = (time.perf_counter() - t0) / reps
+        cpu = {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+
+    achieved = head_alg / (head_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T_BLOCK, "parallelism": f"replicas{world}",
+                   "l2": "no flush: 1.67 GB of weights streamed per step > 129 MB L2",
+                   "packed_bytes_per_step": step_bytes},
+        "fraction_of_peak": value / world / hbm_peak,
+        "verified_tokens_per_s": world * verified_tokens / (ms * 1e-3),
+        "accept_len": accepted,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "gemm_kernel<W12, argmax> (fused LM head)", "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": head_alg, "launch_ms": head_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": nk * args.steps,
+        "clocks": clk.summary(),
+        "detail": {"kernel_ms": per, "layer_ms": layer_ms, "layer_gbs": layer_bytes / (layer_ms * 1e-3) / 1e9,
+                   "layer_frac": layer_bytes / (layer_ms * 1e-3) / 1e9 / hbm_peak, "head_ms": head_ms,
+                   "bf16_baseline": bf16_detail},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16-baseline", action="store_true", default=True)
+    ap.add_argument("--no-bf16-baseline", dest="bf16_baseline", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -155,9 +155,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       mbar_init(&B.full[s], 1);
       mbar_init(&B.empty[s], 1);
     }
-    for (int a = 0; a < kNA; ++a) {
-      mbar_init(&B.a_full[a], C::kDecWarps * 32);
-      mbar_init(&B.a_empty[a], 1);
+    if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
+      for (int a = 0; a < kNA; ++a) {
+        mbar_init(&B.a_full[a], C::kDecWarps > 0 ? C::kDecWarps * 32 : 1);
+        mbar_init(&B.a_empty[a], 1);
+      }
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&B.acc_full[a], 1);
