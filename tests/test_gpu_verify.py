@@ -36,14 +36,14 @@ def test_verify_greedy_logits(B, T_rows, V):
 
 
 def test_verify_greedy_ties_take_lowest_index():
-    M, V = 16, 9000
+    M, V = 16, 12000
     logits = np.zeros((M, V), dtype=np.float32)
     for m in range(M):
-        cols = [m * 500 + 7, m * 500 + 4100, 8999 - m]
+        cols = [m * 500 + 7, m * 500 + 4100, V - 1 - m]   # ties inside and across 4096-column chunks
         logits[m, cols] = 3.0
     draft = np.array([[m * 500 + 7 for m in range(16)]], dtype=np.int32)
     acc, bonus, am = w12.verify_greedy(f32_dev(logits), to_dev_i32(draft), 16)
-    np.testing.assert_array_equal(am.cpu().numpy(), [min(m * 500 + 7, 8999 - m) for m in range(M)])
+    np.testing.assert_array_equal(am.cpu().numpy(), [m * 500 + 7 for m in range(M)])
     assert int(acc.item()) == 16 and int(bonus.item()) == -1
 
 
