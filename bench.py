@@ -210,6 +210,7 @@ def to_dev_bf16(bits, dev):
 def run_ours(args, world, rank, local):
     import torch
     from speculative_decoding_verification_w12_gb300 import w12
+    from speculative_decoding_verification_w12_gb300.engine import VerifyStep
 
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
@@ -218,55 +219,34 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     # Weights: seeded, packed once on the device (offline step, not timed).
-    layer = []
+    packs = []
     for i, (name, N, K) in enumerate(LAYER):
-        pk = w12.pack(to_dev_bf16(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i), dev))
-        X = to_dev_bf16(S.activations_bf16(M_ROWS, K, tag=i), dev)
-        Y = torch.empty((M_ROWS, N), dtype=torch.float32, device=dev)
-        ws = w12.workspace(w12.gemm_ws_bytes(M_ROWS, N, K), dev)
-        layer.append(dict(name=name, N=N, K=K, pk=pk, X=X, Y=Y, ws=ws))
-    Wh_bits = S.weights_bf16(HEAD[1], HEAD[2], seed=S.SEED_WEIGHTS + 10)
-    head = w12.pack(to_dev_bf16(Wh_bits, dev))
-    Wh_bf16 = to_dev_bf16(Wh_bits, dev) if args.bf16_baseline else None
-    del Wh_bits
-    H = to_dev_bf16(S.activations_bf16(M_ROWS, HEAD[2], tag=10), dev)
-    hws = w12.workspace(w12.verify_ws_bytes(M_ROWS, HEAD[1]), dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    acc = torch.empty(1, dtype=torch.int32, device=dev)
-    bonus = torch.empty(1, dtype=torch.int32, device=dev)
-    am = torch.empty(M_ROWS, dtype=torch.int32, device=dev)
+        packs.append(w12.pack(to_dev_bf16(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i), dev)))
+    head = w12.pack(to_dev_bf16(S.weights_bf16(HEAD[1], HEAD[2], seed=S.SEED_WEIGHTS + 10), dev))
+    torch.cuda.empty_cache()
+    st = VerifyStep(packs, head, B=1, T=T_BLOCK, device=dev)
+    for i, (x, (_, N, K)) in enumerate(zip(st.X, LAYER)):
+        x.copy_(to_dev_bf16(S.activations_bf16(M_ROWS, K, tag=i), dev))
+    st.H.copy_(to_dev_bf16(S.activations_bf16(M_ROWS, HEAD[2], tag=10), dev))
 
     # Plant the draft block against the target's own argmax (from an untimed pass).
-    draft = torch.zeros((1, T_BLOCK), dtype=torch.int32, device=dev)
-    w12.verify_greedy_fused(H, head, draft, T_BLOCK, ws=hws, status=status, out=(acc, bonus, am))
+    st.run()
     torch.cuda.synchronize(dev)
     L = S.accept_lengths_uniform(1, T_BLOCK, tag=3)
-    draft_np = S.plant_block_drafts(am.cpu().numpy(), 1, T_BLOCK, T_BLOCK, L, HEAD[1])
-    draft.copy_(torch.from_numpy(draft_np))
+    st.draft.copy_(torch.from_numpy(S.plant_block_drafts(st.argmax.cpu().numpy(), 1, T_BLOCK, T_BLOCK, L,
+                                                         HEAD[1])))
+    st.capture()
 
-    layer_bytes = sum(packed_stream_bytes(g["N"], g["K"]) for g in layer)
-    head_bytes = packed_stream_bytes(HEAD[1], HEAD[2])
-    step_bytes = layer_bytes + head_bytes
+    layer_bytes = sum(w.nbytes for w in packs)
+    head_bytes = head.nbytes
+    step_bytes = st.packed_bytes
     # Algorithmic bytes of the fused head launch: packed weights incl. exception CSR + H + partials.
     head_alg = (head_bytes + 4 * head.exc_off.numel() + 4 * head.n_exc + M_ROWS * HEAD[2] * 2
                 + (HEAD[1] // 128) * 16 * 8)
-
-    nk = 6  # kernel launches per step: 4 layer GEMMs, fused head GEMM, reduce+accept
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
-
-    def step(events=None):
-        if events:
-            events[0].record(stream)
-        for j, g in enumerate(layer):
-            w12.gemm(g["X"], g["pk"], Y=g["Y"], ws=g["ws"], status=status)
-            if events:
-                events[j + 1].record(stream)
-        w12.verify_greedy_fused(H, head, draft, T_BLOCK, ws=hws, status=status, out=(acc, bonus, am))
-        if events:
-            events[nk].record(stream)
+    nk = st.launches
 
     for _ in range(args.warmup):
-        step()
+        st.replay()
     torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -274,87 +254,74 @@ def run_ours(args, world, rank, local):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for k in range(args.steps):
-            step(ev[k])
+        for _ in range(args.steps):
+            st.replay()
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
-    ms = t_start.elapsed_time(t_end) / args.steps
-    ms = max_over_ranks(ms, world)
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    per = {g["name"]: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j, g in enumerate(layer)}
-    per["head+accept"] = statistics.median(e[4].elapsed_time(e[nk]) for e in ev)
-    layer_ms = statistics.median(e[0].elapsed_time(e[4]) for e in ev)
+    ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world)
+    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
+    accepted = int(st.accept_len.item())
+    verified_tokens = accepted + (1 if int(st.bonus.item()) >= 0 else 0)
 
-    # Fused-head kernel alone, timed with events on its stream (for the roofline).
-    hk = []
+    # Per-kernel breakdown from eager launches with events on the launching stream.
+    ev = []
     for _ in range(args.steps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for g in layer:  # evict the head's tail from L2 with other weight traffic
-            w12.gemm(g["X"], g["pk"], Y=g["Y"], ws=g["ws"])
-        a.record(stream)
-        w12.lib().w12_verify_greedy_fused  # noqa: B018 (binding resolved before timing)
-        w12.verify_greedy_fused(H, head, draft, T_BLOCK, ws=hws, status=status, out=(acc, bonus, am))
-        b.record(stream)
-        hk.append((a, b))
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(len(packs) + 2)]
+        e[0].record(stream)
+        for j, (x, w, y, ws) in enumerate(zip(st.X, st.layers, st.Y, st.ws)):
+            w12.gemm(x, w, Y=y, ws=ws, status=st.status)
+            e[j + 1].record(stream)
+        w12.verify_greedy_fused(st.H, head, st.draft, T_BLOCK, ws=st.hws, status=st.status,
+                                out=(st.accept_len, st.bonus, st.argmax))
+        e[-1].record(stream)
+        ev.append(e)
     torch.cuda.synchronize(dev)
-    head_ms = statistics.median(a.elapsed_time(b) for a, b in hk)
+    per = {name: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev) for j, (name, _, _) in enumerate(LAYER)}
+    head_ms = statistics.median(e[len(packs)].elapsed_time(e[-1]) for e in ev)
+    per["head+accept"] = head_ms
+    layer_ms = statistics.median(e[0].elapsed_time(e[len(packs)]) for e in ev)
 
     hbm_peak, tc_peak, peak_src = peaks()
     value = world * step_bytes / (ms * 1e-3) / 1e9
-    accepted = int(acc.item())
-    verified_tokens = accepted + (1 if int(bonus.item()) >= 0 else 0)
 
-    # End to end: host (pinned) inputs -> C-ABI calls -> host results, every step.
-    hx = [g["X"].cpu().pin_memory() for g in layer]
-    hH = H.cpu().pin_memory()
-    hdraft = draft.cpu().pin_memory()
-    hout = torch.empty(2 + M_ROWS, dtype=torch.int32).pin_memory()
-    outbuf = torch.empty(2 + M_ROWS, dtype=torch.int32, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in hx) + hH.numel() * 2 + hdraft.numel() * 4
-    d2h = hout.numel() * 4
-
-    def e2e_step():
-        for g, h in zip(layer, hx):
-            g["X"].copy_(h, non_blocking=True)
-        H.copy_(hH, non_blocking=True)
-        draft.copy_(hdraft, non_blocking=True)
-        step()
-        outbuf[0:1].copy_(acc)
-        outbuf[1:2].copy_(bonus)
-        outbuf[2:].copy_(am)
-        hout.copy_(outbuf, non_blocking=True)
-
+    # End to end: pinned host inputs -> copies + step (public VerifyStep API) -> host results, every step.
+    hx = [x.cpu().pin_memory() for x in st.X]
+    hH = st.H.cpu().pin_memory()
+    hdraft = st.draft.cpu().pin_memory()
     for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+        st.run_host(hx, hH, hdraft)
+        torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        e2e_step()
+        acc_h, _, _ = st.run_host(hx, hH, hdraft)
+        stream.synchronize()                      # the host reads the step's result
+        assert int(acc_h[0]) == accepted
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
     bf16_detail = None
     if args.bf16_baseline:
-        # In-tree BF16 kernel on the same layer shapes (bytes x 16/12).
+        # In-tree BF16 kernel on the same layer shapes (16 bytes per 12 streamed).
         bdet = {}
-        for i, g in enumerate(layer):
-            Wb = to_dev_bf16(S.weights_bf16(g["N"], g["K"], seed=S.SEED_WEIGHTS + i), dev)
+        for i, ((name, N, K), x, y, ws) in enumerate(zip(LAYER, st.X, st.Y, st.ws)):
+            Wb = to_dev_bf16(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i), dev)
+            w12.gemm_bf16_ref(x, Wb, Y=y, ws=ws)
             ts = []
             for _ in range(args.steps):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                w12.gemm_bf16_ref(g["X"], Wb, Y=g["Y"], ws=g["ws"])
+                w12.gemm_bf16_ref(x, Wb, Y=y, ws=ws)
                 b.record(stream)
                 ts.append((a, b))
             torch.cuda.synchronize(dev)
-            bdet[g["name"]] = statistics.median(a.elapsed_time(b) for a, b in ts)
+            bdet[name] = statistics.median(a.elapsed_time(b) for a, b in ts)
             del Wb
         bf16_detail = {"ms": bdet, "layer_ms": sum(bdet.values()),
-                       "w12_layer_ms": sum(per[g["name"]] for g in layer)}
+                       "w12_layer_ms": sum(per[n] for n, _, _ in LAYER)}
 
     if rank != 0:
         return 0
@@ -376,22 +343,22 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T_BLOCK, "parallelism": f"replicas{world}",
                    "l2": "no flush: 1.67 GB of weights streamed per step > 129 MB L2",
-                   "packed_bytes_per_step": step_bytes},
+                   "packed_bytes_per_step": step_bytes, "launch": "CUDA graph of the step's 6 kernels"},
         "fraction_of_peak": value / world / hbm_peak,
         "verified_tokens_per_s": world * verified_tokens / (ms * 1e-3),
         "accept_len": accepted,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
-                     "kernel": "gemm_kernel<W12, argmax> (fused LM head)", "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": head_alg, "launch_ms": head_ms},
+                     "kernel": "fused W12 LM head: gemm_kernel<W12, argmax> + reduce_accept_kernel",
+                     "peak_source": peak_src, "algorithmic_bytes_per_launch": head_alg, "launch_ms": head_ms},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(), "ms_per_step": e2e_ms},
         "gpu_launches": nk * args.steps,
         "clocks": clk.summary(),
-        "detail": {"kernel_ms": per, "layer_ms": layer_ms, "layer_gbs": layer_bytes / (layer_ms * 1e-3) / 1e9,
-                   "layer_frac": layer_bytes / (layer_ms * 1e-3) / 1e9 / hbm_peak, "head_ms": head_ms,
-                   "bf16_baseline": bf16_detail},
+        "detail": {"kernel_ms_eager": per, "layer_ms_eager": layer_ms,
+                   "layer_gbs_eager": layer_bytes / (layer_ms * 1e-3) / 1e9,
+                   "head_ms": head_ms, "bf16_baseline": bf16_detail},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -409,10 +376,11 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        # The oracle leg needs no GPU and no collective: rank 0 runs it, others exit.
+        return run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
     world, rank, local = dist_setup()
     try:
-        if args.impl == "reference":
-            return run_reference(args, world, rank)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

@@ -33,17 +33,21 @@ int device_sm_count() {
 }
 
 bool device_supported() {
+  static int cache[64] = {0};  // 0 unknown, 1 yes, 2 no
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  return major == 10 && minor == 3;
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -67,8 +71,37 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// A tensor map depends only on these fields (the address, not the data), so
+// encoded maps are cached: repeated calls on the same buffers skip the driver.
+struct TmapKey {
+  int dtype, swizzle;
+  void* base;
+  uint64_t inner, outer, stride;
+  uint32_t box_inner, box_outer;
+  bool operator==(const TmapKey& o) const {
+    return dtype == o.dtype && swizzle == o.swizzle && base == o.base && inner == o.inner && outer == o.outer &&
+           stride == o.stride && box_inner == o.box_inner && box_outer == o.box_outer;
+  }
+};
+
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  constexpr int kSlots = 512;
+  static std::mutex mu;
+  static TmapKey keys[kSlots];
+  static CUtensorMap maps[kSlots];
+  static bool used[kSlots] = {false};
+  const TmapKey key{int(dtype), int(swizzle), base, inner, outer, row_stride_bytes, box_inner, box_outer};
+  const uint64_t h = (reinterpret_cast<uint64_t>(base) >> 8) ^ (inner * 0x9E3779B97F4A7C15ull) ^ (outer << 7) ^
+                     (uint64_t(box_outer) << 17) ^ uint64_t(dtype) ^ (uint64_t(swizzle) << 3);
+  const int slot = int(h % kSlots);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (used[slot] && keys[slot] == key) {
+      *map = maps[slot];
+      return true;
+    }
+  }
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -77,7 +110,12 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uin
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  keys[slot] = key;
+  maps[slot] = *map;
+  used[slot] = true;
+  return true;
 }
 
 int gemm_shape(int64_t M, int64_t N, int64_t K, GemmShape* s) {

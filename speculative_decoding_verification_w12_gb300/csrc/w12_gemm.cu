@@ -214,14 +214,16 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint64_t pol_x = policy_evict_last();
       const uint32_t xbox = uint32_t(P.Mpad) * 128u;
       const uint32_t tx = C::kABytes + (kW12 ? 128u : 0u) + 2u * xbox;
-      int64_t issued = 0;
-      for (int64_t u = ub; u < ue; ++u, ++issued) {
-        const int64_t i = u - ub;
-        const int s = int(i % S);
-        const uint32_t ph = uint32_t(i / S) & 1u;
+      // Per-unit state kept incrementally in 32-bit registers (no 64-bit
+      // division in this single-thread loop).
+      int t = int(ub / KB), kb = int(ub % KB);
+      const int n_units = int(ue - ub);
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      for (; issued < n_units; ++issued) {
         if (!wait(&B.empty[s], ph ^ 1u)) break;
-        const int t = int(u / KB), kb = int(u % KB);
-        uint8_t* st = smem + size_t(s) * plan.stage_bytes;
+        uint8_t* st = smem + s * plan.stage_bytes;
         mbar_arrive_expect_tx(&B.full[s], tx);
         if (kW12) {
           tma_load_2d_hint(st, &tm_a0, kb * 64, t * 128, &B.full[s], pol_w);
@@ -234,12 +236,19 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
         tma_load_2d_hint(st + plan.x_off, &tm_x, kb * 128, 0, &B.full[s], pol_x);
         tma_load_2d_hint(st + plan.x_off + xbox, &tm_x, kb * 128 + 64, 0, &B.full[s], pol_x);
+        if (++kb == KB) {
+          kb = 0;
+          ++t;
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (*abort_flag) {
         // Let the copies already issued land before the CTA can exit.
-        const int64_t lo = issued > S ? issued - S : 0;
-        for (int64_t i = lo; i < issued; ++i)
-          mbar_wait(&B.full[int(i % S)], uint32_t(i / S) & 1u, lim);
+        for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+          mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, lim);
       }
     }
   } else if (warp == 1) {
@@ -247,39 +256,59 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, uint32_t(P.Mpad));
       const uint32_t xbox = uint32_t(P.Mpad) * 128u;
-      int64_t seg = -1;
-      bool ok = true;
-      for (int64_t u = ub; u < ue && ok; ++u) {
-        const int64_t i = u - ub;
-        const bool first = (u == ub) || (u % KB == 0);
-        const bool last = (u + 1 == ue) || ((u + 1) % KB == 0);
+      // Descriptors of stage 0; other stages and K steps add (byte offset >> 4)
+      // to the 14-bit start-address field, which cannot overflow (smem < 256 KB).
+      const uint32_t st0 = smem_u32(smem);
+      const uint64_t bdesc0 = sdesc_k_sw128(st0 + plan.x_off);
+      const uint64_t adesc0 = sdesc_k_sw128(st0);
+      const uint32_t a_tmem0 = tmem_base + kAColBase;
+      const int n_units = int(ue - ub);
+      int kb = int(ub % KB);
+      int s = 0, ab = 0, accb = 0;
+      uint32_t ph = 0, aph = 0, accph = 0;
+      for (int i = 0; i < n_units; ++i) {
+        const bool first = (i == 0) || (kb == 0);
+        const bool last = (i + 1 == n_units) || (kb + 1 == KB);
         if (first) {
-          ++seg;
-          if (!wait(&B.acc_empty[seg % NACC], (uint32_t(seg / NACC) & 1u) ^ 1u)) break;
+          if (!wait(&B.acc_empty[accb], accph ^ 1u)) break;
           tc_fence_after();
         }
-        const int s = int(i % S);
-        if (!wait(&B.full[s], uint32_t(i / S) & 1u)) break;
-        const int ab = int(i % kNA);
-        if (kW12 && !wait(&B.a_full[ab], uint32_t(i / kNA) & 1u)) break;
+        if (!wait(&B.full[s], ph)) break;
+        if (kW12 && !wait(&B.a_full[ab], aph)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(seg % NACC) * uint32_t(P.Mpad);
-        const uint32_t st = smem_u32(smem + size_t(s) * plan.stage_bytes);
-        const uint32_t xs = st + plan.x_off;
+        const uint32_t d_tmem = tmem_base + uint32_t(accb) * uint32_t(P.Mpad);
+        const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
+        const uint32_t a_tmem = a_tmem0 + uint32_t(ab * kAColsPerBuf);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bdesc = sdesc_k_sw128(xs + uint32_t(kk >> 2) * xbox + uint32_t(kk & 3) * 32u);
+          const uint64_t koff = uint64_t(((uint32_t(kk >> 2) * xbox) + uint32_t(kk & 3) * 32u) >> 4);
+          const uint64_t bdesc = bdesc0 + soff16 + koff;
           const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
           if (kW12) {
-            mma_bf16_ts(d_tmem, tmem_base + kAColBase + uint32_t(ab * kAColsPerBuf + kk * 8), bdesc, idesc, acc);
+            mma_bf16_ts(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
           } else {
-            const uint64_t adesc = sdesc_k_sw128(st + uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u);
-            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, acc);
+            const uint64_t aoff = uint64_t((uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u) >> 4);
+            mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
           }
         }
         tc_commit(&B.empty[s]);
         if (kW12) tc_commit(&B.a_empty[ab]);
-        if (last) tc_commit(&B.acc_full[seg % NACC]);
+        if (last) {
+          tc_commit(&B.acc_full[accb]);
+          if (++accb == NACC) {
+            accb = 0;
+            accph ^= 1u;
+          }
+        }
+        if (++kb == KB) kb = 0;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++ab == kNA) {
+          ab = 0;
+          aph ^= 1u;
+        }
       }
       // Make sure no MMA is in flight before TMEM is released.
       tc_commit(B.drain);
@@ -321,14 +350,14 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const bool in_smem = ok && *ent_in_smem;
     const uint32_t e_base = *ent_base;
     const uint32_t e_end = *ent_end;
-    for (int64_t u = ub; u < ue && ok; ++u) {
-      const int64_t i = u - ub;
-      const int s = int(i % S);
-      const int ab = int(i % kNA);
-      if (!wait(&B.full[s], uint32_t(i / S) & 1u)) break;
-      if (!wait(&B.a_empty[ab], (uint32_t(i / kNA) & 1u) ^ 1u)) break;
+    const int n_units = int(ue - ub);
+    int s = 0, ab = 0;
+    uint32_t ph = 0, aph = 0;
+    for (int i = 0; i < n_units && ok; ++i) {
+      if (!wait(&B.full[s], ph)) break;
+      if (!wait(&B.a_empty[ab], aph ^ 1u)) break;
       tc_fence_after();
-      const uint8_t* st = smem + size_t(s) * plan.stage_bytes;
+      const uint8_t* st = smem + s * plan.stage_bytes;
       const uint32_t eb = st[plan.eb_off + row];
       const uint32_t E2 = (eb << 7) * 0x00010001u;
 
@@ -390,6 +419,14 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&B.a_full[ab]);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+      if (++ab == kNA) {
+        ab = 0;
+        aph ^= 1u;
+      }
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------- epilogue
@@ -448,18 +485,24 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
     };
 
-    int64_t seg = 0;
-    for (int64_t u = ub; u < ue; ++seg) {
-      const int t = int(u / KB);
+    int accb = 0;
+    uint32_t accph = 0;
+    int t = first_tile;
+    for (int64_t u = ub; u < ue; ++t) {
       const int64_t seg_end = (int64_t(t) + 1) * KB < ue ? (int64_t(t) + 1) * KB : ue;
       u = seg_end;
-      const int accb = int(seg % NACC);
-      if (!wait(&B.acc_full[accb], uint32_t(seg / NACC) & 1u)) break;
+      const int cur = accb;
+      const uint32_t cur_ph = accph;
+      if (++accb == NACC) {
+        accb = 0;
+        accph ^= 1u;
+      }
+      if (!wait(&B.acc_full[cur], cur_ph)) break;
       tc_fence_after();
       const int c_first = unit_owner(int64_t(t) * KB, U, G);
       const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
       const int nsplit = c_last - c_first + 1;
-      const uint32_t d_tmem = tmem_base + tm_lane + uint32_t(accb) * uint32_t(P.Mpad);
+      const uint32_t d_tmem = tmem_base + tm_lane + uint32_t(cur) * uint32_t(P.Mpad);
       if (nsplit == 1) {
         for (int mc = 0; mc < nchunks; ++mc) {
           uint32_t r[16];
@@ -472,7 +515,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           else store_chunk(v, t, mc);
         }
         tc_fence_before();
-        mbar_arrive(&B.acc_empty[accb]);
+        mbar_arrive(&B.acc_empty[cur]);
       } else {
         const int slot = 2 * c + (t == first_tile ? 0 : 1);
         float* my = P.parts + size_t(slot) * P.Mpad * 128;
@@ -484,7 +527,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           for (int k = 0; k < 16; ++k) my[(mc * 16 + k) * 128 + row] = __uint_as_float(r[k]);
         }
         tc_fence_before();
-        mbar_arrive(&B.acc_empty[accb]);
+        mbar_arrive(&B.acc_empty[cur]);
         __threadfence();
         named_bar_sync(kEpiBar, 128);
         if (et == 0) {
@@ -535,8 +578,14 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
   auto kern = gemm_kernel<kW12, kArgmax>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
-    return W12_ERR_CUDA;
+  static bool attr_set[64] = {false};  // per device; setting it twice is harmless
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
+      return W12_ERR_CUDA;
+    attr_set[dev] = true;
+  }
   kern<<<P.grid, Cfg<kW12>::kThreads, plan.total, stream>>>(a0, a1, a2, x, P);
   return cuda_status(cudaGetLastError());
 }

@@ -1,0 +1,66 @@
+"""Run one verify-path kernel on a seeded workload a few times (for ncu).
+
+  python -m speculative_decoding_verification_w12_gb300.profile_case --op w12 --shape gate_up --M 16 --iters 3
+
+--op w12 | bf16 | head (fused LM head + greedy accept); --shape one of the
+27B-class layer GEMMs (qkv, o, gate_up, down) or head (5120 -> 151936).
+Prints the mean CUDA-event time per launch.
+"""
+import argparse
+
+import numpy as np
+import torch
+
+from . import synthetic as S
+from . import w12
+
+SHAPES = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (34816, 5120), "down": (5120, 17408),
+          "head": (151936, 5120)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head"])
+    ap.add_argument("--shape", default="gate_up", choices=sorted(SHAPES))
+    ap.add_argument("--M", type=int, default=16)
+    ap.add_argument("--iters", type=int, default=3)
+    a = ap.parse_args()
+    N, K = SHAPES[a.shape]
+    dev = torch.device("cuda")
+
+    def d(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    Wb = d(S.weights_bf16(N, K))
+    X = d(S.activations_bf16(a.M, K))
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if a.op == "bf16":
+        ws = w12.workspace(w12.gemm_ws_bytes(a.M, N, K))
+        Y = torch.empty((a.M, N), dtype=torch.float32, device=dev)
+        fn = lambda: w12.gemm_bf16_ref(X, Wb, Y=Y, ws=ws, status=st)  # noqa: E731
+    else:
+        pk = w12.pack(Wb)
+        del Wb
+        if a.op == "w12":
+            ws = w12.workspace(w12.gemm_ws_bytes(a.M, N, K))
+            Y = torch.empty((a.M, N), dtype=torch.float32, device=dev)
+            fn = lambda: w12.gemm(X, pk, Y=Y, ws=ws, status=st)  # noqa: E731
+        else:
+            B = max(1, a.M // 16)
+            draft = torch.zeros((B, 16), dtype=torch.int32, device=dev)
+            ws = w12.workspace(w12.verify_ws_bytes(B * 16, N))
+            fn = lambda: w12.verify_greedy_fused(X[:B * 16], pk, draft, 16, ws=ws, status=st)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    print(f"{a.op} {a.shape} M={a.M}: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/launch")
+
+
+if __name__ == "__main__":
+    main()

@@ -130,9 +130,13 @@ class W12Weights:
     n_exc: int
 
     def struct(self) -> _Weights:
-        return _Weights(self.N, self.K, self.p0.data_ptr(), self.p1.data_ptr(), self.p2.data_ptr(),
-                        self.ebase.data_ptr(), self.exc_off.data_ptr(),
-                        self.exc_ent.data_ptr() if self.exc_ent.numel() else None, self.n_exc)
+        s = self.__dict__.get("_struct")
+        if s is None:  # the packed buffers never move, so the descriptor is built once
+            s = _Weights(self.N, self.K, self.p0.data_ptr(), self.p1.data_ptr(), self.p2.data_ptr(),
+                         self.ebase.data_ptr(), self.exc_off.data_ptr(),
+                         self.exc_ent.data_ptr() if self.exc_ent.numel() else None, self.n_exc)
+            self.__dict__["_struct"] = s
+        return s
 
     @property
     def nbytes(self) -> int:
