@@ -194,6 +194,16 @@ int w12_selftest_timeout(int32_t* dev_status, int limit_us, void* stream);
  * default 2000000. Values below 1 are rejected. */
 int w12_set_wait_limit_us(int64_t limit_us);
 
+/* Launch overlap (programmatic dependent launch), on by default: a GEMM or
+ * verify launch may start while the previous kernel on its stream is still
+ * running. Before that kernel completes it only reads the packed weights
+ * (planes, ebase, exception CSR); it reads X/H/logits/drafts and writes any
+ * output or workspace only after waiting for it. So packed weights must not
+ * be written by the kernel launched immediately before on the same stream
+ * (a copy-engine transfer or an event in between is fine). Pass 0 to launch
+ * with ordinary stream ordering. Returns W12_OK. */
+int w12_set_overlap(int enable);
+
 #ifdef __cplusplus
 }
 #endif

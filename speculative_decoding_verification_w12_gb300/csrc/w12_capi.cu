@@ -12,6 +12,10 @@ static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+static std::atomic<int> g_overlap{1};
+
+bool overlap_enabled() { return g_overlap.load(std::memory_order_relaxed) != 0; }
+
 int device_sm_count() {
   static std::mutex mu;
   static int cache[64] = {0};
@@ -195,6 +199,11 @@ int w12_version(void) { return 100; }
 int w12_set_wait_limit_us(int64_t limit_us) {
   if (limit_us < 1) return W12_ERR_ARG;
   g_wait_limit_ns.store(static_cast<uint64_t>(limit_us) * 1000ull, std::memory_order_relaxed);
+  return W12_OK;
+}
+
+int w12_set_overlap(int enable) {
+  g_overlap.store(enable ? 1 : 0, std::memory_order_relaxed);
   return W12_OK;
 }
 

@@ -233,6 +233,12 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[16]) {
                : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends on
+// have completed and their writes are visible (returns at once for an
+// ordinary launch), and allow the next grid on the stream to start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -15,10 +15,10 @@
 //               x B[16 x Mpad] (smem, X), 8 instructions per unit.
 //   warp 2      TMEM allocation / release.
 //   warp 3      stages the CTA's exception offsets and entries in smem.
-//   warps 4-11  decode: each thread restores half a row (64 values) of the
-//               unit from the planes (LDS.128), patches exceptions in
+//   warps 4-19  decode: each thread restores a quarter row (32 values) of
+//               the unit from the planes (LDS.128), patches exceptions in
 //               registers, and writes bf16 pairs into TMEM (tcgen05.st).
-//   warps 12-15 epilogue: tcgen05.ld of the accumulator; unsplit tiles write
+//   warps 20-23 epilogue: tcgen05.ld of the accumulator; unsplit tiles write
 //               Y directly; split tiles write partial slots and the last CTA
 //               to arrive sums them in a fixed order (deterministic).
 // The BF16 baseline uses the same skeleton with A loaded by TMA into smem.
@@ -29,8 +29,15 @@
 
 namespace w12 {
 
-constexpr int kNA = 4;                // TMEM A buffers (W12 mode)
-constexpr int kAColBase = 256;        // TMEM column of A buffer 0
+// Decode warps per CTA (multiple of 4: each TMEM lane quarter gets the same
+// number); each decodes 128/(W12_DEC_WARPS/4) values of its row per unit.
+#ifndef W12_DEC_WARPS
+#define W12_DEC_WARPS 8
+#endif
+static_assert(W12_DEC_WARPS == 8 || W12_DEC_WARPS == 16, "decode warps: 8 or 16");
+
+constexpr int kChunksPerThread = 16 / W12_DEC_WARPS;  // 32-value chunks each decode thread restores per unit
+constexpr int kMaxStages = 8;         // smem ring depth limit (one TMEM A buffer per stage)
 constexpr int kAColsPerBuf = 64;      // 128 K values = 64 columns of bf16 pairs
 constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
 constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
@@ -54,7 +61,7 @@ struct GemmParams {
 
 template <bool kW12>
 struct Cfg {
-  static constexpr int kDecWarps = kW12 ? 8 : 0;
+  static constexpr int kDecWarps = kW12 ? W12_DEC_WARPS : 0;
   static constexpr int kEpiWarp0 = 4 + kDecWarps;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr uint32_t kABytes = kW12 ? 3 * 8192 : 2 * 16384;  // A operand bytes per stage
@@ -104,7 +111,6 @@ struct Bars {
   uint64_t* full;
   uint64_t* empty;
   uint64_t* a_full;
-  uint64_t* a_empty;
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* exc_ready;
@@ -128,8 +134,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   B.full = bar_base;
   B.empty = bar_base + S;
   B.a_full = bar_base + 2 * S;
-  B.a_empty = B.a_full + kNA;
-  B.acc_full = B.a_empty + kNA;
+  B.acc_full = B.a_full + S;
   B.acc_empty = B.acc_full + 2;
   B.exc_ready = B.acc_empty + 2;
   B.drain = B.exc_ready + 1;
@@ -156,10 +161,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       mbar_init(&B.empty[s], 1);
     }
     if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
-      for (int a = 0; a < kNA; ++a) {
-        mbar_init(&B.a_full[a], C::kDecWarps > 0 ? C::kDecWarps * 32 : 1);
-        mbar_init(&B.a_empty[a], 1);
-      }
+      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], C::kDecWarps > 0 ? C::kDecWarps * 32 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&B.acc_full[a], 1);
@@ -179,6 +181,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // TMEM columns: accumulators [0, NACC*Mpad), then one 64-column A buffer per stage.
+  const uint32_t a_col0 = uint32_t((NACC * P.Mpad + 63) & ~63);
 
   auto fail = [&](int code) {
     set_status(P.status, code);
@@ -218,21 +222,48 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // division in this single-thread loop).
       int t = int(ub / KB), kb = int(ub % KB);
       const int n_units = int(ue - ub);
+      // The first ring-full of weight tiles is requested before waiting for
+      // the previous kernel on the stream (launch overlap); X is loaded, and
+      // anything else is read or written, only after that wait.
+      const int prefill = n_units < S ? n_units : S;
+      {
+        int t0 = t, kb0 = kb;
+        for (int i = 0; i < prefill; ++i) {
+          uint8_t* st = smem + i * plan.stage_bytes;
+          mbar_arrive_expect_tx(&B.full[i], tx);
+          if (kW12) {
+            tma_load_2d_hint(st, &tm_a0, kb0 * 64, t0 * 128, &B.full[i], pol_w);
+            tma_load_2d_hint(st + 8192, &tm_a1, kb0 * 64, t0 * 128, &B.full[i], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a2, kb0 * 64, t0 * 128, &B.full[i], pol_w);
+            bulk_load(st + plan.eb_off, P.ebase + int64_t(kb0) * P.N + int64_t(t0) * 128, 128u, &B.full[i]);
+          } else {
+            tma_load_2d_hint(st, &tm_a0, kb0 * 128, t0 * 128, &B.full[i], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a0, kb0 * 128 + 64, t0 * 128, &B.full[i], pol_w);
+          }
+          if (++kb0 == KB) {
+            kb0 = 0;
+            ++t0;
+          }
+        }
+      }
+      grid_dep_wait();
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;
       for (; issued < n_units; ++issued) {
-        if (!wait(&B.empty[s], ph ^ 1u)) break;
         uint8_t* st = smem + s * plan.stage_bytes;
-        mbar_arrive_expect_tx(&B.full[s], tx);
-        if (kW12) {
-          tma_load_2d_hint(st, &tm_a0, kb * 64, t * 128, &B.full[s], pol_w);
-          tma_load_2d_hint(st + 8192, &tm_a1, kb * 64, t * 128, &B.full[s], pol_w);
-          tma_load_2d_hint(st + 16384, &tm_a2, kb * 64, t * 128, &B.full[s], pol_w);
-          bulk_load(st + plan.eb_off, P.ebase + int64_t(kb) * P.N + int64_t(t) * 128, 128u, &B.full[s]);
-        } else {
-          tma_load_2d_hint(st, &tm_a0, kb * 128, t * 128, &B.full[s], pol_w);
-          tma_load_2d_hint(st + 16384, &tm_a0, kb * 128 + 64, t * 128, &B.full[s], pol_w);
+        if (issued >= prefill) {
+          if (!wait(&B.empty[s], ph ^ 1u)) break;
+          mbar_arrive_expect_tx(&B.full[s], tx);
+          if (kW12) {
+            tma_load_2d_hint(st, &tm_a0, kb * 64, t * 128, &B.full[s], pol_w);
+            tma_load_2d_hint(st + 8192, &tm_a1, kb * 64, t * 128, &B.full[s], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a2, kb * 64, t * 128, &B.full[s], pol_w);
+            bulk_load(st + plan.eb_off, P.ebase + int64_t(kb) * P.N + int64_t(t) * 128, 128u, &B.full[s]);
+          } else {
+            tma_load_2d_hint(st, &tm_a0, kb * 128, t * 128, &B.full[s], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a0, kb * 128 + 64, t * 128, &B.full[s], pol_w);
+          }
         }
         tma_load_2d_hint(st + plan.x_off, &tm_x, kb * 128, 0, &B.full[s], pol_x);
         tma_load_2d_hint(st + plan.x_off + xbox, &tm_x, kb * 128 + 64, 0, &B.full[s], pol_x);
@@ -245,6 +276,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           ph ^= 1u;
         }
       }
+      grid_dep_launch();
       if (*abort_flag) {
         // Let the copies already issued land before the CTA can exit.
         for (int i = issued > S ? issued - S : 0; i < issued; ++i)
@@ -261,11 +293,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint32_t st0 = smem_u32(smem);
       const uint64_t bdesc0 = sdesc_k_sw128(st0 + plan.x_off);
       const uint64_t adesc0 = sdesc_k_sw128(st0);
-      const uint32_t a_tmem0 = tmem_base + kAColBase;
+      const uint32_t a_tmem0 = tmem_base + a_col0;
       const int n_units = int(ue - ub);
       int kb = int(ub % KB);
-      int s = 0, ab = 0, accb = 0;
-      uint32_t ph = 0, aph = 0, accph = 0;
+      int s = 0, accb = 0;
+      uint32_t ph = 0, accph = 0;
       for (int i = 0; i < n_units; ++i) {
         const bool first = (i == 0) || (kb == 0);
         const bool last = (i + 1 == n_units) || (kb + 1 == KB);
@@ -273,12 +305,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           if (!wait(&B.acc_empty[accb], accph ^ 1u)) break;
           tc_fence_after();
         }
-        if (!wait(&B.full[s], ph)) break;
-        if (kW12 && !wait(&B.a_full[ab], aph)) break;
+        // W12: the decoders waited for the stage's copies before arriving on
+        // a_full, so "decoded" implies "landed" for X as well.
+        if (kW12 ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(accb) * uint32_t(P.Mpad);
         const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
-        const uint32_t a_tmem = a_tmem0 + uint32_t(ab * kAColsPerBuf);
+        const uint32_t a_tmem = a_tmem0 + uint32_t(s * kAColsPerBuf);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t koff = uint64_t(((uint32_t(kk >> 2) * xbox) + uint32_t(kk & 3) * 32u) >> 4);
@@ -291,8 +324,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
           }
         }
-        tc_commit(&B.empty[s]);
-        if (kW12) tc_commit(&B.a_empty[ab]);
+        tc_commit(&B.empty[s]);  // frees the smem stage and its TMEM A buffer
         if (last) {
           tc_commit(&B.acc_full[accb]);
           if (++accb == NACC) {
@@ -304,10 +336,6 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         if (++s == S) {
           s = 0;
           ph ^= 1u;
-        }
-        if (++ab == kNA) {
-          ab = 0;
-          aph ^= 1u;
         }
       }
       // Make sure no MMA is in flight before TMEM is released.
@@ -341,7 +369,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     // --------------------------------------------------------------- decode
     const int dw = warp - 4;
     const int q = warp & 3;          // TMEM lane quarter of this warp
-    const int h = dw >> 2;           // which 64-value half of the unit row
+    const int h = dw >> 2;           // which slice of the unit row (kChunksPerThread chunks of 32 values)
     const int row = q * 32 + lane;   // W row within the unit
     const uint32_t tm_lane = uint32_t(q * 32) << 16;
     const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
@@ -351,11 +379,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const uint32_t e_base = *ent_base;
     const uint32_t e_end = *ent_end;
     const int n_units = int(ue - ub);
-    int s = 0, ab = 0;
-    uint32_t ph = 0, aph = 0;
+    int s = 0;
+    uint32_t ph = 0;
     for (int i = 0; i < n_units && ok; ++i) {
+      // Stage s's copies can only have landed after the MMA that last read
+      // its TMEM A buffer committed, so the buffer is free once this returns.
       if (!wait(&B.full[s], ph)) break;
-      if (!wait(&B.a_empty[ab], aph ^ 1u)) break;
       tc_fence_after();
       const uint8_t* st = smem + s * plan.stage_bytes;
       const uint32_t eb = st[plan.eb_off + row];
@@ -368,21 +397,25 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         o1 = o0;
       }
       const uint32_t nex = o1 - o0;
-      uint32_t ent = kInvalidEnt, m0 = 0, m1 = 0;
+      uint32_t ent = kInvalidEnt;
+      uint32_t mchunk[kChunksPerThread];
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc) mchunk[cc] = 0;
       if (nex > 0) {
         if (uint32_t(lane) < nex)
           ent = in_smem ? sent[o0 - e_base + lane] : __ldg(P.exc_ent + o0 + lane);
         const bool mine = ent != kInvalidEnt && ((ent >> 28) & 3u) == uint32_t(q);
         const uint32_t ch = (ent >> 21) & 3u;
-        m0 = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(2 * h));
-        m1 = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(2 * h + 1));
+#pragma unroll
+        for (int cc = 0; cc < kChunksPerThread; ++cc)
+          mchunk[cc] = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(h * kChunksPerThread + cc));
       }
 
       const uint8_t* pl = st + row * 64;
       const uint32_t swz = uint32_t(row >> 1) & 3u;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t lc = uint32_t(2 * h + cc);
+      for (int cc = 0; cc < kChunksPerThread; ++cc) {
+        const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
         const uint32_t off = ((lc ^ swz) << 4);
         const uint4 a = *reinterpret_cast<const uint4*>(pl + off);
         const uint4 b = *reinterpret_cast<const uint4*>(pl + 8192 + off);
@@ -392,7 +425,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         decode8(a.y, b.y, g.y, E2, w + 4);
         decode8(a.z, b.z, g.z, E2, w + 8);
         decode8(a.w, b.w, g.w, E2, w + 12);
-        uint32_t mk = cc ? m1 : m0;
+        uint32_t mk = mchunk[cc];
         while (mk) {
           const int src = __ffs(mk) - 1;
           mk &= mk - 1;
@@ -414,18 +447,14 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             }
           }
         }
-        tmem_st16(tmem_base + tm_lane + kAColBase + uint32_t(ab * kAColsPerBuf) + lc * 16u, w);
+        tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&B.a_full[ab]);
+      mbar_arrive(&B.a_full[s]);
       if (++s == S) {
         s = 0;
         ph ^= 1u;
-      }
-      if (++ab == kNA) {
-        ab = 0;
-        aph ^= 1u;
       }
     }
   } else if (warp >= C::kEpiWarp0) {
@@ -485,6 +514,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
     };
 
+    grid_dep_wait();
     int accb = 0;
     uint32_t accph = 0;
     int t = first_tile;
@@ -572,8 +602,13 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
   GemmParams P = P0;
   // Deepest ring that fits next to the fixed carve-up.
   const int smem_max = 232448;
-  int stages = 8;
-  while (stages > 2 && smem_plan<kW12>(sh.Mpad, stages).total > uint32_t(smem_max)) --stages;
+  const int nacc = sh.Mpad <= 128 ? 2 : 1;
+  const int a_col0 = (nacc * sh.Mpad + 63) & ~63;
+  int stages = kMaxStages;
+  while (stages > 2 && (smem_plan<kW12>(sh.Mpad, stages).total > uint32_t(smem_max) ||
+                        (kW12 && a_col0 + stages * kAColsPerBuf > 512)))
+    --stages;
+  if (kW12 && a_col0 + stages * kAColsPerBuf > 512) return W12_ERR_UNSUPPORTED;
   const SmemPlan plan = smem_plan<kW12>(sh.Mpad, stages);
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
@@ -586,8 +621,17 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
       return W12_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<P.grid, Cfg<kW12>::kThreads, plan.total, stream>>>(a0, a1, a2, x, P);
-  return cuda_status(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(P.grid));
+  cfg.blockDim = dim3(unsigned(Cfg<kW12>::kThreads));
+  cfg.dynamicSmemBytes = plan.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, a0, a1, a2, x, P));
 }
 
 int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, const w12_weights* W,

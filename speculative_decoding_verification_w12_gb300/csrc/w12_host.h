@@ -18,6 +18,10 @@ constexpr int kTreeMax = 256;          // nodes per draft tree
 // Wall-time bound for every device-side wait (nanoseconds).
 uint64_t wait_limit_ns();
 
+// Whether launches may overlap the previous kernel on the stream
+// (programmatic dependent launch); on by default.
+bool overlap_enabled();
+
 // Number of SMs of the current device (cached per device); 0 if no device.
 int device_sm_count();
 

@@ -61,6 +61,7 @@ __device__ __forceinline__ void block_argmax(float& bv, int& bi) {
 __global__ void __launch_bounds__(256) logits_partials_kernel(const float* __restrict__ logits, int64_t V,
                                                               int Mstride, int chunk, float* __restrict__ pv,
                                                               int32_t* __restrict__ pi) {
+  grid_dep_wait();
   const int m = blockIdx.y, cidx = blockIdx.x;
   const int64_t beg = int64_t(cidx) * chunk;
   const int64_t end = beg + chunk < V ? beg + chunk : V;
@@ -193,6 +194,8 @@ __global__ void __launch_bounds__(256) reduce_accept_kernel(
     int32_t* __restrict__ path_len, int32_t* argmax_ws, int32_t* argmax_out, int32_t* done, int32_t* status) {
   __shared__ int is_last;
   __shared__ int tree_scratch[8][3][kTreeMax];
+  grid_dep_wait();
+  grid_dep_launch();
   const int m = blockIdx.x;
   float bv = -INFINITY;
   int bi = 0x7FFFFFFF;
@@ -223,19 +226,34 @@ __global__ void __launch_bounds__(256) reduce_accept_kernel(
 int launch_logits_partials(const float* logits, int64_t V, int M, int Mstride, int chunk, float* pv, int32_t* pi,
                            cudaStream_t stream) {
   const int64_t nparts = (V + chunk - 1) / chunk;
-  dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(M));
-  logits_partials_kernel<<<grid, 256, 0, stream>>>(logits, V, Mstride, chunk, pv, pi);
-  return cuda_status(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nparts), static_cast<unsigned>(M));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, logits_partials_kernel, logits, V, Mstride, chunk, pv, pi));
 }
 
 int launch_reduce_accept(const float* pv, const int32_t* pi, int nparts, int Mstride, int M, int mode, int B, int T,
                          int T_rows, const int32_t* draft, const int32_t* parents, int32_t* accept_len, int32_t* bonus,
                          int32_t* path, int32_t* path_len, int32_t* argmax_ws, int32_t* argmax_out, int32_t* done,
                          int32_t* dev_status, cudaStream_t stream) {
-  reduce_accept_kernel<<<M, 256, 0, stream>>>(pv, pi, nparts, Mstride, M, mode, B, T, T_rows, draft, parents,
-                                              accept_len, bonus, path, path_len, argmax_ws, argmax_out, done,
-                                              dev_status);
-  return cuda_status(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(M));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, reduce_accept_kernel, pv, pi, nparts, Mstride, M, mode, B, T, T_rows,
+                                        draft, parents, accept_len, bonus, path, path_len, argmax_ws, argmax_out, done,
+                                        dev_status));
 }
 
 static int check_greedy(int B, int T, int T_rows) {

@@ -24,7 +24,7 @@ EXPORTS = [
     "w12_status_string", "w12_version", "w12_pack_ws_bytes", "w12_pack_query", "w12_pack", "w12_unpack",
     "w12_gemm_ws_bytes", "w12_gemm", "w12_gemm_bf16_ref", "w12_verify_ws_bytes", "w12_verify_greedy",
     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
-    "w12_set_wait_limit_us",
+    "w12_set_wait_limit_us", "w12_set_overlap",
 ]
 
 
@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
                                             sz, vp, vp]),
             "w12_selftest_timeout": (i32, [vp, i32, vp]),
             "w12_set_wait_limit_us": (i32, [i64]),
+            "w12_set_overlap": (i32, [i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -284,3 +285,8 @@ def selftest_timeout(limit_us: int, status: torch.Tensor, stream=None):
 
 def set_wait_limit_us(limit_us: int):
     _check(lib().w12_set_wait_limit_us(int(limit_us)), "w12_set_wait_limit_us")
+
+
+def set_overlap(enable: bool):
+    """Enable/disable launch overlap with the previous kernel on the stream."""
+    _check(lib().w12_set_overlap(1 if enable else 0), "w12_set_overlap")
