@@ -379,6 +379,36 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const uint32_t e_base = *ent_base;
     const uint32_t e_end = *ent_end;
     const int n_units = int(ue - ub);
+
+    // Exceptions of unit i that fall in this warp's rows: the lane-held entry
+    // (first 32 of the unit) and one ballot mask per 32-value chunk. Prepared
+    // one unit ahead so this bookkeeping overlaps the previous unit's stores.
+    struct Exc {
+      uint32_t o0, o1, ent, mask[kChunksPerThread];
+    };
+    auto prep = [&](int i, Exc& x) {
+      x.o0 = soff[i];
+      x.o1 = soff[i + 1];
+      if (x.o1 < x.o0 || int64_t(x.o1) > P.n_exc || x.o0 < e_base || x.o1 > e_end) {
+        if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
+        x.o1 = x.o0;
+      }
+      const uint32_t nex = x.o1 - x.o0;
+      x.ent = kInvalidEnt;
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc) x.mask[cc] = 0;
+      if (nex > 0) {
+        if (uint32_t(lane) < nex) x.ent = in_smem ? sent[x.o0 - e_base + lane] : __ldg(P.exc_ent + x.o0 + lane);
+        const bool mine = x.ent != kInvalidEnt && ((x.ent >> 28) & 3u) == uint32_t(q);
+        const uint32_t ch = (x.ent >> 21) & 3u;
+#pragma unroll
+        for (int cc = 0; cc < kChunksPerThread; ++cc)
+          x.mask[cc] = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(h * kChunksPerThread + cc));
+      }
+    };
+    Exc cur;
+    if (ok && n_units > 0) prep(0, cur);
+
     int s = 0;
     uint32_t ph = 0;
     for (int i = 0; i < n_units && ok; ++i) {
@@ -387,56 +417,39 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       if (!wait(&B.full[s], ph)) break;
       tc_fence_after();
       const uint8_t* st = smem + s * plan.stage_bytes;
+      const uint8_t* pl = st + row * 64;
+      const uint32_t swz = uint32_t(row >> 1) & 3u;
+      uint4 a[kChunksPerThread], b[kChunksPerThread], g[kChunksPerThread];
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc) {
+        const uint32_t off = ((uint32_t(h * kChunksPerThread + cc) ^ swz) << 4);
+        a[cc] = *reinterpret_cast<const uint4*>(pl + off);
+        b[cc] = *reinterpret_cast<const uint4*>(pl + 8192 + off);
+        g[cc] = *reinterpret_cast<const uint4*>(pl + 16384 + off);
+      }
       const uint32_t eb = st[plan.eb_off + row];
       const uint32_t E2 = (eb << 7) * 0x00010001u;
 
-      // Exceptions of this unit that fall in this warp's rows and half.
-      uint32_t o0 = soff[i], o1 = soff[i + 1];
-      if (o1 < o0 || int64_t(o1) > P.n_exc || o0 < e_base || o1 > e_end) {
-        if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
-        o1 = o0;
-      }
-      const uint32_t nex = o1 - o0;
-      uint32_t ent = kInvalidEnt;
-      uint32_t mchunk[kChunksPerThread];
-#pragma unroll
-      for (int cc = 0; cc < kChunksPerThread; ++cc) mchunk[cc] = 0;
-      if (nex > 0) {
-        if (uint32_t(lane) < nex)
-          ent = in_smem ? sent[o0 - e_base + lane] : __ldg(P.exc_ent + o0 + lane);
-        const bool mine = ent != kInvalidEnt && ((ent >> 28) & 3u) == uint32_t(q);
-        const uint32_t ch = (ent >> 21) & 3u;
-#pragma unroll
-        for (int cc = 0; cc < kChunksPerThread; ++cc)
-          mchunk[cc] = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(h * kChunksPerThread + cc));
-      }
-
-      const uint8_t* pl = st + row * 64;
-      const uint32_t swz = uint32_t(row >> 1) & 3u;
 #pragma unroll
       for (int cc = 0; cc < kChunksPerThread; ++cc) {
         const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
-        const uint32_t off = ((lc ^ swz) << 4);
-        const uint4 a = *reinterpret_cast<const uint4*>(pl + off);
-        const uint4 b = *reinterpret_cast<const uint4*>(pl + 8192 + off);
-        const uint4 g = *reinterpret_cast<const uint4*>(pl + 16384 + off);
         uint32_t w[16];
-        decode8(a.x, b.x, g.x, E2, w + 0);
-        decode8(a.y, b.y, g.y, E2, w + 4);
-        decode8(a.z, b.z, g.z, E2, w + 8);
-        decode8(a.w, b.w, g.w, E2, w + 12);
-        uint32_t mk = mchunk[cc];
+        decode8(a[cc].x, b[cc].x, g[cc].x, E2, w + 0);
+        decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
+        decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
+        decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
+        uint32_t mk = cur.mask[cc];
         while (mk) {
           const int src = __ffs(mk) - 1;
           mk &= mk - 1;
-          const uint32_t e = __shfl_sync(0xFFFFFFFFu, ent, src);
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
           if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
         }
-        if (nex > 32) {
+        if (cur.o1 - cur.o0 > 32) {
           // Rare: more than 32 exceptions in the unit; walk the rest in batches.
-          for (uint32_t bst = o0 + 32; bst < o1; bst += 32) {
+          for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
             uint32_t e2 = kInvalidEnt;
-            if (bst + lane < o1) e2 = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
+            if (bst + lane < cur.o1) e2 = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
             const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
             uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
             while (mk2) {
@@ -449,6 +462,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
         tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
       }
+      if (i + 1 < n_units) prep(i + 1, cur);  // overlaps the stores in flight
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&B.a_full[s]);

@@ -116,3 +116,23 @@ def test_layer_shapes_sampled_columns(name, N, K):
     cols = np.unique(np.concatenate([np.arange(0, N, 97), [N - 1]]))
     Y64 = O.gemm_rows(X, W[cols])
     assert_gemm_close(Y[:, cols], Y64, name)
+
+
+def test_extreme_group_offsets_both_restore_paths():
+    """Rows with offsets above 127 (|w| >= 2^16) use the integer restore, the
+    rest the power-of-two multiply; rows below 2^-112 have offset 0. Checked
+    per row group so small rows are not hidden by large ones."""
+    W = S.weights_bf16(512, 1024, seed=14)
+    Wf = S.bf16_bits_to_f32(W).copy()
+    Wf[0:64] *= np.float32(2.0 ** 30)        # offsets ~138
+    Wf[64:96] *= np.float32(2.0 ** -110)     # offsets 0 (emax < 15)
+    Wf[200:210] *= np.float32(2.0 ** 100)    # offsets ~208
+    Wf[300, 5] = np.float32(1.0e37)          # near the top of the exponent range (offset 235)
+    W = S.f32_to_bf16_bits(Wf)
+    X = S.activations_bf16(16, 1024, seed=15)
+    pk = O.pack(W)
+    Y64 = O.gemm(X, pk)
+    Y, Yr = run_both(X, W)
+    for lo, hi in [(0, 64), (64, 96), (96, 200), (200, 210), (210, 300), (300, 301), (301, 512)]:
+        assert_gemm_close(Y[:, lo:hi], Y64[:, lo:hi], f"w12 rows {lo}:{hi}")
+        assert_gemm_close(Yr[:, lo:hi], Y64[:, lo:hi], f"bf16 rows {lo}:{hi}")
