@@ -15,10 +15,11 @@
 //               x B[16 x Mpad] (smem, X), 8 instructions per unit.
 //   warp 2      TMEM allocation / release.
 //   warp 3      stages the CTA's exception offsets and entries in smem.
-//   warps 4-19  decode: each thread restores a quarter row (32 values) of
-//               the unit from the planes (LDS.128), patches exceptions in
-//               registers, and writes bf16 pairs into TMEM (tcgen05.st).
-//   warps 20-23 epilogue: tcgen05.ld of the accumulator; unsplit tiles write
+//   decode warps (4 + 4*groups*split of them): each thread restores its
+//               row's share of the unit from the planes (LDS.128), patches
+//               exceptions in registers, and writes bf16 pairs into TMEM
+//               (tcgen05.st); decode groups take units in turn.
+//   last 4 warps epilogue: tcgen05.ld of the accumulator; unsplit tiles write
 //               Y directly; split tiles write partial slots and the last CTA
 //               to arrive sums them in a fixed order (deterministic).
 // The BF16 baseline uses the same skeleton with A loaded by TMA into smem.
@@ -29,14 +30,21 @@
 
 namespace w12 {
 
-// Decode warps per CTA (multiple of 4: each TMEM lane quarter gets the same
-// number); each decodes 128/(W12_DEC_WARPS/4) values of its row per unit.
-#ifndef W12_DEC_WARPS
-#define W12_DEC_WARPS 8
+// Decode warps: W12_DEC_GROUPS groups of 4 x W12_DEC_SPLIT warps. Each warp
+// serves one TMEM lane quarter (32 rows); the W12_DEC_SPLIT warps of a
+// quarter in a group split the unit's 4 chunks of 32 values; groups take
+// units in turn (unit i goes to group i % W12_DEC_GROUPS).
+#ifndef W12_DEC_GROUPS
+#define W12_DEC_GROUPS 2
 #endif
-static_assert(W12_DEC_WARPS == 8 || W12_DEC_WARPS == 16, "decode warps: 8 or 16");
-
-constexpr int kChunksPerThread = 16 / W12_DEC_WARPS;  // 32-value chunks each decode thread restores per unit
+#ifndef W12_DEC_SPLIT
+#define W12_DEC_SPLIT 1
+#endif
+static_assert(W12_DEC_GROUPS >= 1 && W12_DEC_GROUPS <= 3, "decode groups: 1..3");
+static_assert(W12_DEC_SPLIT == 1 || W12_DEC_SPLIT == 2 || W12_DEC_SPLIT == 4, "decode split: 1, 2 or 4");
+constexpr int kDecGroups = W12_DEC_GROUPS;
+constexpr int kDecSplit = W12_DEC_SPLIT;
+constexpr int kChunksPerThread = 4 / kDecSplit;  // 32-value chunks each decode thread restores per unit
 constexpr int kMaxStages = 8;         // smem ring depth limit (one TMEM A buffer per stage)
 constexpr int kAColsPerBuf = 64;      // 128 K values = 64 columns of bf16 pairs
 constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
@@ -61,7 +69,7 @@ struct GemmParams {
 
 template <bool kW12>
 struct Cfg {
-  static constexpr int kDecWarps = kW12 ? W12_DEC_WARPS : 0;
+  static constexpr int kDecWarps = kW12 ? 4 * kDecGroups * kDecSplit : 0;
   static constexpr int kEpiWarp0 = 4 + kDecWarps;
   static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
   static constexpr uint32_t kABytes = kW12 ? 3 * 8192 : 2 * 16384;  // A operand bytes per stage
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       mbar_init(&B.empty[s], 1);
     }
     if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
-      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], C::kDecWarps > 0 ? C::kDecWarps * 32 : 1);
+      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * kDecSplit);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&B.acc_full[a], 1);
@@ -369,7 +377,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     // --------------------------------------------------------------- decode
     const int dw = warp - 4;
     const int q = warp & 3;          // TMEM lane quarter of this warp
-    const int h = dw >> 2;           // which slice of the unit row (kChunksPerThread chunks of 32 values)
+    const int grp = (dw >> 2) / kDecSplit;  // decode group: units grp, grp + kDecGroups, ...
+    const int h = (dw >> 2) % kDecSplit;    // slice of the unit row (kChunksPerThread chunks of 32 values)
     const int row = q * 32 + lane;   // W row within the unit
     const uint32_t tm_lane = uint32_t(q * 32) << 16;
     const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
@@ -407,11 +416,16 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
     };
     Exc cur;
-    if (ok && n_units > 0) prep(0, cur);
+    if (ok && grp < n_units) prep(grp, cur);
 
     int s = 0;
     uint32_t ph = 0;
-    for (int i = 0; i < n_units && ok; ++i) {
+    for (int k = 0; k < grp; ++k)
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    for (int i = grp; i < n_units && ok; i += kDecGroups) {
       // Stage s's copies can only have landed after the MMA that last read
       // its TMEM A buffer committed, so the buffer is free once this returns.
       if (!wait(&B.full[s], ph)) break;
@@ -462,14 +476,15 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
         tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
       }
-      if (i + 1 < n_units) prep(i + 1, cur);  // overlaps the stores in flight
+      if (i + kDecGroups < n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&B.a_full[s]);
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
+      for (int k = 0; k < kDecGroups; ++k)
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------- epilogue
