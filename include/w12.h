@@ -131,6 +131,24 @@ size_t w12_gemm_ws_bytes(int64_t M, int64_t N, int64_t K);
 int w12_gemm(const uint16_t* X, int64_t M, const w12_weights* W, float* Y,
              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* Same product as w12_gemm without a caller workspace, for callers that
+ * cannot allocate device memory: code embedded in a host application that
+ * owns every device allocation and exposes no allocator, and latency-critical
+ * loops that may not call cudaMalloc/cudaFree (or a framework allocator)
+ * while they run. The pages have no counterpart to this entry point.
+ * The split-K scratch is a fixed array of 3,162,112 bytes that the library
+ * holds in device memory on every GPU where it is loaded, until the process
+ * exits. It serves M <= 16 rows, N <= 524288 (4096 tiles of 128), and GPUs
+ * with up to 192 SMs; larger shapes return W12_ERR_WORKSPACE (use w12_gemm).
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. Every
+ * call clears the tile counters it uses and allocates nothing. All calls
+ * share the one array: calls that overlap on the GPU (other streams, or
+ * several host threads) race and corrupt each other's results; serialise
+ * them. X, Y, dev_status and stream are as for w12_gemm. */
+int w12_gemm_noalloc(const uint16_t* X, int64_t M, const w12_weights* W, float* Y,
+                     int32_t* dev_status, void* stream);
+
 /* Same product with W given as plain bf16 [N, K] (the in-tree BF16 baseline
  * that shows what the 12/16 byte saving is worth). */
 int w12_gemm_bf16_ref(const uint16_t* X, int64_t M, const uint16_t* W, int64_t N, int64_t K,

@@ -24,7 +24,7 @@ EXPORTS = [
     "w12_status_string", "w12_version", "w12_pack_ws_bytes", "w12_pack_query", "w12_pack", "w12_unpack",
     "w12_gemm_ws_bytes", "w12_gemm", "w12_gemm_bf16_ref", "w12_verify_ws_bytes", "w12_verify_greedy",
     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
-    "w12_set_wait_limit_us", "w12_set_overlap",
+    "w12_set_wait_limit_us", "w12_set_overlap", "w12_gemm_noalloc",
 ]
 
 
@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
             "w12_selftest_timeout": (i32, [vp, i32, vp]),
             "w12_set_wait_limit_us": (i32, [i64]),
             "w12_set_overlap": (i32, [i32]),
+            "w12_gemm_noalloc": (i32, [vp, i64, ctypes.POINTER(_Weights), vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -198,6 +199,22 @@ def gemm(X: torch.Tensor, w: W12Weights, Y: torch.Tensor | None = None, ws: torc
         ws = workspace(gemm_ws_bytes(M, w.N, w.K), X.device)
     _check(lib().w12_gemm(X.data_ptr(), M, ctypes.byref(w.struct()), Y.data_ptr(), ws.data_ptr(), ws.numel(),
                           _ptr(status), _stream(stream)), "w12_gemm")
+    return Y
+
+
+def gemm_noalloc(X: torch.Tensor, w: W12Weights, Y: torch.Tensor, status: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Y[M, N] = X * W^T through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory (code inside a host
+    application that owns all allocations, or loops that must not allocate
+    while they run): the library serves the split-K scratch from a fixed
+    array it holds itself (M <= 16). The caller supplies X and the output Y.
+    Calls that overlap on the GPU share that array and race.
+    """
+    X = _bits16(X)
+    _check(lib().w12_gemm_noalloc(X.data_ptr(), X.shape[0], ctypes.byref(w.struct()), Y.data_ptr(), _ptr(status),
+                                  _stream(stream)), "w12_gemm_noalloc")
     return Y
 
 
