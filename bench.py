@@ -42,6 +42,26 @@ def packed_stream_bytes(N, K):
     return 3 * N * K // 2 + N * K // 128
 
 
+def profiled_traffic():
+    """DRAM bytes per launch of the fused-head GEMM from the committed ncu
+    summary, or None if the kernel sources changed since that capture."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "fused_head_m16.md")
+    srcs = [os.path.join(ROOT, "speculative_decoding_verification_w12_gb300", "csrc", f)
+            for f in ("w12_gemm.cu", "w12_dev.cuh")]
+    if not os.path.exists(prof) or not all(os.path.exists(f) for f in srcs):
+        return None
+    fields = {}
+    for line in open(prof):
+        if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_launch", "kernel_source_sha256"):
+            k, v = line.split(":", 1)
+            fields[k] = v.strip()
+    h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()
+    if fields.get("kernel_source_sha256") != h or "traffic_bytes_per_launch" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -348,7 +368,7 @@ def run_ours(args, world, rank, local):
         "verified_tokens_per_s": world * verified_tokens / (ms * 1e-3),
         "accept_len": accepted,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
                      "kernel": "fused W12 LM head: gemm_kernel<W12, argmax> + reduce_accept_kernel",
                      "peak_source": peak_src, "algorithmic_bytes_per_launch": head_alg, "launch_ms": head_ms},
         "cpu_baseline": cpu,
