@@ -52,7 +52,7 @@ constexpr int kScratchStride = 129;   // floats per column in the argmax transpo
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
 
 struct GemmParams {
-  int M, Mpad, N, K, KB, tiles, grid, stages;
+  int M, Mpad, N, K, KB, tiles, grid, stages, issuers;
   int64_t units;
   const uint8_t* ebase;
   const uint32_t* exc_off;
@@ -172,11 +172,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * kDecSplit);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&B.acc_full[a], 1);
+      mbar_init(&B.acc_full[a], P.issuers);  // one commit per MMA issuer per segment
       mbar_init(&B.acc_empty[a], 128);
     }
     mbar_init(B.exc_ready, 1);
-    mbar_init(B.drain, 1);
+    mbar_init(B.drain, P.issuers);
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -189,8 +189,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // TMEM columns: accumulators [0, NACC*Mpad), then one 64-column A buffer per stage.
-  const uint32_t a_col0 = uint32_t((NACC * P.Mpad + 63) & ~63);
+  // TMEM columns: accumulators [0, NACC*issuers*Mpad) (buffer b, issuer k at
+  // column (b*issuers + k)*Mpad), then one 64-column A buffer per stage.
+  const int NISS = P.issuers;
+  const uint32_t a_col0 = uint32_t((NACC * NISS * P.Mpad + 63) & ~63);
 
   auto fail = [&](int code) {
     set_status(P.status, code);
@@ -291,9 +293,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, lim);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // Issuer k (warp 1 + k, one thread) takes the units i with i % issuers == k
+    // into its own accumulator: one thread can only issue a kind::f16 MMA
+    // every few tens of cycles, so two issuers double the issue rate.
+    const int k = warp - 1;
+    if (lane == 0 && k < NISS) {
       const uint32_t idesc = idesc_bf16(128, uint32_t(P.Mpad));
       const uint32_t xbox = uint32_t(P.Mpad) * 128u;
       // Descriptors of stage 0; other stages and K steps add (byte offset >> 4)
@@ -306,35 +312,40 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       int kb = int(ub % KB);
       int s = 0, accb = 0;
       uint32_t ph = 0, accph = 0;
+      bool started = false;  // this issuer has written its accumulator in the current segment
       for (int i = 0; i < n_units; ++i) {
         const bool first = (i == 0) || (kb == 0);
         const bool last = (i + 1 == n_units) || (kb + 1 == KB);
         if (first) {
           if (!wait(&B.acc_empty[accb], accph ^ 1u)) break;
           tc_fence_after();
+          started = false;
         }
-        // W12: the decoders waited for the stage's copies before arriving on
-        // a_full, so "decoded" implies "landed" for X as well.
-        if (kW12 ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(accb) * uint32_t(P.Mpad);
-        const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
-        const uint32_t a_tmem = a_tmem0 + uint32_t(s * kAColsPerBuf);
+        if (i % NISS == k) {
+          // W12: the decoders waited for the stage's copies before arriving on
+          // a_full, so "decoded" implies "landed" for X as well.
+          if (kW12 ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + uint32_t(accb * NISS + k) * uint32_t(P.Mpad);
+          const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
+          const uint32_t a_tmem = a_tmem0 + uint32_t(s * kAColsPerBuf);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t koff = uint64_t(((uint32_t(kk >> 2) * xbox) + uint32_t(kk & 3) * 32u) >> 4);
-          const uint64_t bdesc = bdesc0 + soff16 + koff;
-          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-          if (kW12) {
-            mma_bf16_ts(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
-          } else {
-            const uint64_t aoff = uint64_t((uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u) >> 4);
-            mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t koff = uint64_t(((uint32_t(kk >> 2) * xbox) + uint32_t(kk & 3) * 32u) >> 4);
+            const uint64_t bdesc = bdesc0 + soff16 + koff;
+            const uint32_t acc = (started || kk > 0) ? 1u : 0u;
+            if (kW12) {
+              mma_bf16_ts(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
+            } else {
+              const uint64_t aoff = uint64_t((uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u) >> 4);
+              mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
+            }
           }
+          started = true;
+          tc_commit(&B.empty[s]);  // frees the smem stage and its TMEM A buffer
         }
-        tc_commit(&B.empty[s]);  // frees the smem stage and its TMEM A buffer
         if (last) {
-          tc_commit(&B.acc_full[accb]);
+          tc_commit(&B.acc_full[accb]);  // every issuer arrives once per segment
           if (++accb == NACC) {
             accb = 0;
             accph ^= 1u;
@@ -548,6 +559,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     uint32_t accph = 0;
     int t = first_tile;
     for (int64_t u = ub; u < ue; ++t) {
+      const int64_t seg_begin = u;
       const int64_t seg_end = (int64_t(t) + 1) * KB < ue ? (int64_t(t) + 1) * KB : ue;
       u = seg_end;
       const int cur = accb;
@@ -561,15 +573,26 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const int c_first = unit_owner(int64_t(t) * KB, U, G);
       const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
       const int nsplit = c_last - c_first + 1;
-      const uint32_t d_tmem = tmem_base + tm_lane + uint32_t(cur) * uint32_t(P.Mpad);
+      // Issuer k wrote accumulator (cur, k) iff the segment holds a unit i
+      // (counted from the CTA's first unit) with i % issuers == k.
+      const int ia = int(seg_begin - ub), nseg = int(seg_end - seg_begin);
+      const uint32_t d_tmem = tmem_base + tm_lane + uint32_t(cur * NISS) * uint32_t(P.Mpad);
+      auto load_acc = [&](int mc, float (&v)[16]) {
+        bool have = false;
+        for (int kq = 0; kq < NISS; ++kq) {
+          if (!(nseg >= NISS || (ia % NISS) == kq)) continue;
+          uint32_t r[16];
+          tmem_ld16(d_tmem + uint32_t(kq * P.Mpad + mc * 16), r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] = have ? v[x] + __uint_as_float(r[x]) : __uint_as_float(r[x]);
+          have = true;
+        }
+      };
       if (nsplit == 1) {
         for (int mc = 0; mc < nchunks; ++mc) {
-          uint32_t r[16];
-          tmem_ld16(d_tmem + uint32_t(mc * 16), r);
-          tmem_ld_wait(r);
           float v[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+          load_acc(mc, v);
           if (kArgmax) argmax_chunk(v, t, mc);
           else store_chunk(v, t, mc);
         }
@@ -579,11 +602,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         const int slot = 2 * c + (t == first_tile ? 0 : 1);
         float* my = P.parts + size_t(slot) * P.Mpad * 128;
         for (int mc = 0; mc < nchunks; ++mc) {
-          uint32_t r[16];
-          tmem_ld16(d_tmem + uint32_t(mc * 16), r);
-          tmem_ld_wait(r);
+          float v[16];
+          load_acc(mc, v);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) my[(mc * 16 + k) * 128 + row] = __uint_as_float(r[k]);
+          for (int k = 0; k < 16; ++k) my[(mc * 16 + k) * 128 + row] = v[k];
         }
         tc_fence_before();
         mbar_arrive(&B.acc_empty[cur]);
@@ -632,7 +654,9 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
   // Deepest ring that fits next to the fixed carve-up.
   const int smem_max = 232448;
   const int nacc = sh.Mpad <= 128 ? 2 : 1;
-  const int a_col0 = (nacc * sh.Mpad + 63) & ~63;
+  // Two MMA issuers when their accumulators fit in half of TMEM (Mpad <= 64).
+  const int issuers = nacc * 2 * sh.Mpad <= 256 ? 2 : 1;
+  const int a_col0 = (nacc * issuers * sh.Mpad + 63) & ~63;
   int stages = kMaxStages;
   while (stages > 2 && (smem_plan<kW12>(sh.Mpad, stages).total > uint32_t(smem_max) ||
                         (kW12 && a_col0 + stages * kAColsPerBuf > 512)))
@@ -641,6 +665,7 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
   const SmemPlan plan = smem_plan<kW12>(sh.Mpad, stages);
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
+  P.issuers = issuers;
   auto kern = gemm_kernel<kW12, kArgmax>;
   static bool attr_set[64] = {false};  // per device; setting it twice is harmless
   int dev = 0;
