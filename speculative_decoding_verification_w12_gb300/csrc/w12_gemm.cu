@@ -600,35 +600,59 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         mbar_arrive(&B.acc_empty[cur]);
       } else {
         const int slot = 2 * c + (t == first_tile ? 0 : 1);
-        float* my = P.parts + size_t(slot) * P.Mpad * 128;
+        // Partial slots are laid out [chunk][row][16] floats: each thread's 16
+        // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
+        float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
         for (int mc = 0; mc < nchunks; ++mc) {
           float v[16];
           load_acc(mc, v);
+          float4* dst = my + (size_t(mc) * 128 + row) * 4;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) my[(mc * 16 + k) * 128 + row] = v[k];
+          for (int x = 0; x < 4; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
         }
         tc_fence_before();
         mbar_arrive(&B.acc_empty[cur]);
-        __threadfence();
+        // The barrier orders every epilogue thread's partial stores before the
+        // single release-acquire increment; the last contributor's readers are
+        // ordered after that increment by the second barrier.
         named_bar_sync(kEpiBar, 128);
         if (et == 0) {
-          const int old = atomicAdd(&P.counters[t], 1);
+          const int old = atomic_add_acq_rel_gpu(&P.counters[t], 1);
           *last_flag = (old == nsplit - 1) ? 1 : 0;
         }
         named_bar_sync(kEpiBar, 128);
         if (*last_flag) {
-          __threadfence();
           for (int mc = 0; mc < nchunks; ++mc) {
             float v[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) v[k] = 0.0f;
-            for (int sp = 0; sp < nsplit; ++sp) {
-              const int cc = c_first + sp;
-              const int ft = int(unit_begin(cc, U, G) / KB);
-              const int sl = 2 * cc + (t == ft ? 0 : 1);
-              const float* pp = P.parts + size_t(sl) * P.Mpad * 128;
+            // Two slots per round trip, summed in slot order (deterministic).
+            for (int sp0 = 0; sp0 < nsplit; sp0 += 2) {
+              float4 tmp[2][4];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) v[k] += __ldcg(pp + (mc * 16 + k) * 128 + row);
+              for (int j = 0; j < 2; ++j) {
+                if (sp0 + j < nsplit) {
+                  const int cc = c_first + sp0 + j;
+                  const int ft = int(unit_begin(cc, U, G) / KB);
+                  const int sl = 2 * cc + (t == ft ? 0 : 1);
+                  const float4* src =
+                      reinterpret_cast<const float4*>(P.parts + size_t(sl) * P.Mpad * 128) + (size_t(mc) * 128 + row) * 4;
+#pragma unroll
+                  for (int x = 0; x < 4; ++x) tmp[j][x] = __ldcg(src + x);
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                if (sp0 + j < nsplit) {
+#pragma unroll
+                  for (int x = 0; x < 4; ++x) {
+                    v[4 * x] += tmp[j][x].x;
+                    v[4 * x + 1] += tmp[j][x].y;
+                    v[4 * x + 2] += tmp[j][x].z;
+                    v[4 * x + 3] += tmp[j][x].w;
+                  }
+                }
+              }
             }
             if (kArgmax) argmax_chunk(v, t, mc);
             else store_chunk(v, t, mc);
