@@ -323,25 +323,32 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
 
-    bf16_detail = None
-    if args.bf16_baseline:
-        # In-tree BF16 kernel on the same layer shapes (16 bytes per 12 streamed).
-        bdet = {}
-        for i, ((name, N, K), x, y, ws) in enumerate(zip(LAYER, st.X, st.Y, st.ws)):
+    # Per-GEMM kernel time, W12 vs the in-tree BF16 kernel: R back-to-back
+    # launches of the same GEMM (launch overlap on), CUDA events around the run.
+    def per_launch_ms(fn, reps=20):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    kern = {}
+    for i, ((name, N, K), x, y, ws, pk) in enumerate(zip(LAYER, st.X, st.Y, st.ws, packs)):
+        w_ms = per_launch_ms(lambda: w12.gemm(x, pk, Y=y, ws=ws))
+        b_ms = None
+        if args.bf16_baseline:
             Wb = to_dev_bf16(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i), dev)
-            w12.gemm_bf16_ref(x, Wb, Y=y, ws=ws)
-            ts = []
-            for _ in range(args.steps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                w12.gemm_bf16_ref(x, Wb, Y=y, ws=ws)
-                b.record(stream)
-                ts.append((a, b))
-            torch.cuda.synchronize(dev)
-            bdet[name] = statistics.median(a.elapsed_time(b) for a, b in ts)
+            b_ms = per_launch_ms(lambda: w12.gemm_bf16_ref(x, Wb, Y=y, ws=ws))
             del Wb
-        bf16_detail = {"ms": bdet, "layer_ms": sum(bdet.values()),
-                       "w12_layer_ms": sum(per[n] for n, _, _ in LAYER)}
+        kern[name] = {"w12_ms": w_ms, "bf16_ms": b_ms, "w12_gbs": pk.nbytes / (w_ms * 1e-3) / 1e9,
+                      "bf16_gbs": (N * K * 2 / (b_ms * 1e-3) / 1e9) if b_ms else None}
+    bf16_detail = {"per_gemm_back_to_back": kern,
+                   "layer_w12_ms": sum(v["w12_ms"] for v in kern.values()),
+                   "layer_bf16_ms": (sum(v["bf16_ms"] for v in kern.values()) if args.bf16_baseline else None)}
 
     if rank != 0:
         return 0
@@ -378,7 +385,7 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
         "detail": {"kernel_ms_eager": per, "layer_ms_eager": layer_ms,
                    "layer_gbs_eager": layer_bytes / (layer_ms * 1e-3) / 1e9,
-                   "head_ms": head_ms, "bf16_baseline": bf16_detail},
+                   "head_ms": head_ms, "gemm_kernels": bf16_detail},
     }
     print(json.dumps(line), flush=True)
     return 0
