@@ -391,6 +391,103 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_sweep(args, local):
+    """The other workloads: batched layer GEMMs (M = 16, 128, 256) against the
+    BF16 kernel (HBM vs tensor-pipe crossover), the fused head + greedy verify
+    at M = 16, 64, 128, and the fused head + tree verify (4 trees x 64 nodes).
+    Prints one JSON object (not the contract line)."""
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, _, _ = peaks()
+    tc_peak = 1929.0
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        tc_peak = float(json.load(open(pk_path))["bf16_tflops"])
+
+    def per_launch_ms(fn, reps=10):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    out = {"layer": {}, "head_greedy": {}, "head_tree": {}, "hbm_peak_gbs": hbm_peak, "bf16_tflops_peak": tc_peak}
+    for i, (name, N, K) in enumerate(LAYER):
+        Wbits = S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i)
+        Wb = to_dev_bf16(Wbits, dev)
+        pk = w12.pack(Wb)
+        for M in (16, 128, 256):
+            X = to_dev_bf16(S.activations_bf16(M, K, tag=i), dev)
+            Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            ws = w12.workspace(w12.gemm_ws_bytes(M, N, K), dev)
+            tw = per_launch_ms(lambda: w12.gemm(X, pk, Y=Y, ws=ws))
+            tb = per_launch_ms(lambda: w12.gemm_bf16_ref(X, Wb, Y=Y, ws=ws))
+            fl = 2.0 * M * N * K
+            out["layer"][f"{name}_M{M}"] = {
+                "w12_us": tw * 1e3, "bf16_us": tb * 1e3, "w12_gbs": pk.nbytes / (tw * 1e-3) / 1e9,
+                "w12_frac_hbm": pk.nbytes / (tw * 1e-3) / 1e9 / hbm_peak,
+                "w12_tflops": fl / (tw * 1e-3) / 1e12, "w12_frac_tensor": fl / (tw * 1e-3) / 1e12 / tc_peak,
+                "bf16_gbs": N * K * 2 / (tb * 1e-3) / 1e9, "bf16_tflops": fl / (tb * 1e-3) / 1e12}
+        del Wb, pk
+        torch.cuda.empty_cache()
+    V, K = HEAD[1], HEAD[2]
+    head = w12.pack(to_dev_bf16(S.weights_bf16(V, K, seed=S.SEED_WEIGHTS + 10), dev))
+    torch.cuda.empty_cache()
+    for B in (1, 4, 8):
+        M = 16 * B
+        H = to_dev_bf16(S.activations_bf16(M, K, tag=20 + B), dev)
+        ws = w12.workspace(w12.verify_ws_bytes(M, V), dev)
+        draft = torch.zeros((B, 16), dtype=torch.int32, device=dev)
+        acc, bonus, am = w12.verify_greedy_fused(H, head, draft, 16, ws=ws)
+        torch.cuda.synchronize(dev)
+        L = S.accept_lengths_uniform(B, 16, tag=30 + B)
+        draft.copy_(torch.from_numpy(S.plant_block_drafts(am.cpu().numpy(), B, 16, 16, L, V)))
+        t = per_launch_ms(lambda: w12.verify_greedy_fused(H, head, draft, 16, ws=ws, out=(acc, bonus, am)))
+        accepted = int(acc.sum().item()) + int((bonus >= 0).sum().item())
+        out["head_greedy"][f"M{M}"] = {"us": t * 1e3, "gbs": head.nbytes / (t * 1e-3) / 1e9,
+                                       "frac_hbm": head.nbytes / (t * 1e-3) / 1e9 / hbm_peak,
+                                       "verified_tokens_per_s": accepted / (t * 1e-3),
+                                       "accept_len": acc.cpu().tolist(), "planted": L.tolist()}
+    B, T = 4, 64
+    g = S.rng(S.SEED_TREE, 5)
+    parents = np.stack([S.random_tree(T, g=g) for _ in range(B)])
+    H = to_dev_bf16(S.activations_bf16(B * T, K, tag=40), dev)
+    ws = w12.workspace(w12.verify_ws_bytes(B * T, V), dev)
+    par = torch.from_numpy(parents).to(dev)
+    draft = torch.zeros((B, T), dtype=torch.int32, device=dev)
+    _, _, _, _, am = w12.verify_tree_fused(H, head, par, draft, ws=ws)
+    torch.cuda.synchronize(dev)
+    amn = am.cpu().numpy()
+    dr = np.zeros((B, T), dtype=np.int32)
+    Ds = []
+    for b in range(B):
+        D = int(g.integers(0, 13))
+        Ds.append(D)
+        dr[b], _ = S.plant_tree_drafts(parents[b], amn[b * T:(b + 1) * T], D, V, g)
+    draft.copy_(torch.from_numpy(dr))
+    res = {}
+
+    def tree():
+        res["r"] = w12.verify_tree_fused(H, head, par, draft, ws=ws)
+
+    t = per_launch_ms(tree)
+    _, plen, acc, bonus, _ = res["r"]
+    fl = 2.0 * B * T * V * K
+    out["head_tree"] = {"us": t * 1e3, "gbs": head.nbytes / (t * 1e-3) / 1e9,
+                        "frac_hbm": head.nbytes / (t * 1e-3) / 1e9 / hbm_peak,
+                        "tflops": fl / (t * 1e-3) / 1e12, "frac_tensor": fl / (t * 1e-3) / 1e12 / tc_peak,
+                        "accept_len": acc.cpu().tolist(), "planted": Ds}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -400,6 +497,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bf16-baseline", action="store_true", default=True)
     ap.add_argument("--no-bf16-baseline", dest="bf16_baseline", action="store_false")
+    ap.add_argument("--sweep", action="store_true", help="time the batched, head and tree workloads instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -408,6 +506,8 @@ def main(argv=None):
         return run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
     world, rank, local = dist_setup()
     try:
+        if args.sweep:
+            return run_sweep(args, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

@@ -136,3 +136,17 @@ def test_extreme_group_offsets_both_restore_paths():
     for lo, hi in [(0, 64), (64, 96), (96, 200), (200, 210), (210, 300), (300, 301), (301, 512)]:
         assert_gemm_close(Y[:, lo:hi], Y64[:, lo:hi], f"w12 rows {lo}:{hi}")
         assert_gemm_close(Yr[:, lo:hi], Y64[:, lo:hi], f"bf16 rows {lo}:{hi}")
+
+
+@pytest.mark.parametrize("M", [128, 256])
+@pytest.mark.parametrize("name,N,K", [("qkv", 7168, 5120), ("gate_up", 34816, 5120), ("down", 5120, 17408)])
+def test_batched_layer_shapes_sampled_columns(M, name, N, K):
+    """Batched verify (8 or 16 requests x 16-token blocks) on the layer shapes; sampled outputs vs the oracle."""
+    W = S.weights_bf16(N, K)
+    X = S.activations_bf16(M, K, seed=M)
+    pk = w12.pack(to_dev_bf16(W))
+    st = new_status()
+    Y = w12.gemm(to_dev_bf16(X), pk, status=st).cpu().numpy()
+    assert status_value(st) == 0
+    cols = np.unique(np.concatenate([np.arange(0, N, 131), [N - 1]]))
+    assert_gemm_close(Y[:, cols], O.gemm_rows(X, W[cols]), f"{name} M={M}")

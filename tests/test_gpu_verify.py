@@ -191,3 +191,35 @@ def test_argument_errors_raise():
         w12.gemm_bf16_ref(to_dev_bf16(np.zeros((300, 128), np.uint16)), to_dev_bf16(np.zeros((128, 128), np.uint16)))
     with pytest.raises(w12.W12Error):
         w12.verify_greedy(f32_dev(np.zeros((16, 10))), to_dev_i32(np.zeros((1, 16))), 18)
+
+
+@pytest.mark.parametrize("B", [1, 4, 8])
+def test_fused_greedy_full_head_accept_sweep(B):
+    """Fused W12 LM head 5120 -> 151936 with greedy verify at M = 16*B; planted
+    accept lengths sweep 0..16 across requests and repeated draft sets."""
+    K, V, T = 5120, 151936, 16
+    M = B * T
+    Wh = S.weights_bf16(V, K, seed=88)
+    H = S.activations_bf16(M, K, seed=89 + B)
+    target, gap = _oracle_head_argmax(H, Wh)
+    near = gap < NEAR_TIE
+    head = w12.pack(to_dev_bf16(Wh))
+    hd = to_dev_bf16(H)
+    ws = w12.workspace(w12.verify_ws_bytes(M, V))
+    am_gpu = None
+    for rep, L0 in enumerate(range(0, 17, B if B > 1 else 4)):
+        L = np.array([(L0 + b) % 17 for b in range(B)], dtype=np.int32)
+        draft = S.plant_block_drafts(target, B, T, T, L, V, tag=rep)
+        st = new_status()
+        acc, bonus, am = w12.verify_greedy_fused(hd, head, to_dev_i32(draft), T, ws=ws, status=st)
+        assert status_value(st) == 0
+        am = am.cpu().numpy()
+        assert np.all((am == target) | near)
+        if am_gpu is not None:
+            np.testing.assert_array_equal(am, am_gpu)       # deterministic across calls
+        am_gpu = am
+        ea, eb = O.verify_greedy(draft, am, T)               # GPU argmax through the oracle walk: exact
+        np.testing.assert_array_equal(acc.cpu().numpy(), ea)
+        np.testing.assert_array_equal(bonus.cpu().numpy(), eb)
+        if not near.any():
+            np.testing.assert_array_equal(acc.cpu().numpy(), L)
