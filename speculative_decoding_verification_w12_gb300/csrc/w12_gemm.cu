@@ -123,6 +123,7 @@ struct Bars {
   uint64_t* acc_empty;
   uint64_t* exc_ready;
   uint64_t* drain;
+  uint64_t* gather;
 };
 
 template <bool kW12, bool kArgmax>
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   B.acc_empty = B.acc_full + 2;
   B.exc_ready = B.acc_empty + 2;
   B.drain = B.exc_ready + 1;
+  B.gather = B.drain + 1;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + plan.misc_off);
   volatile uint32_t* tmem_slot = misc + 0;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -153,6 +155,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   volatile int* ent_in_smem = reinterpret_cast<volatile int*>(misc + 3);
   volatile uint32_t* ent_base = misc + 4;
   volatile uint32_t* ent_end = misc + 5;
+  volatile int* pref_flag = reinterpret_cast<volatile int*>(misc + 6);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -177,6 +180,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     }
     mbar_init(B.exc_ready, 1);
     mbar_init(B.drain, P.issuers);
+    mbar_init(B.gather, 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -366,14 +370,35 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     if (kW12) {
       uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
       uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
-      const int64_t nwin = ue - ub + 1;  // host guarantees nwin <= kOffCap
-      for (int64_t k = lane; k < nwin; k += 32) soff[k] = P.exc_off[ub + k];
+      // Every load of a batch is issued before the batch's first store, so the
+      // window costs one memory round trip per batch rather than one per 32
+      // values: the decoders cannot start before this warp arrives.
+      const int nwin = int(ue - ub) + 1;  // host guarantees nwin <= kOffCap
+      {
+        uint32_t v[kOffCap / 32];
+#pragma unroll
+        for (int j = 0; j < kOffCap / 32; ++j)
+          if (lane + 32 * j < nwin) v[j] = P.exc_off[ub + lane + 32 * j];
+#pragma unroll
+        for (int j = 0; j < kOffCap / 32; ++j)
+          if (lane + 32 * j < nwin) soff[lane + 32 * j] = v[j];
+      }
       __syncwarp();
       const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
       bool bad = e1 < e0 || int64_t(e1) > P.n_exc;
       const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
       if (fits) {
-        for (uint32_t k = lane; k < e1 - e0; k += 32) sent[k] = P.exc_ent[e0 + k];
+        constexpr int kBatch = 16;  // entries per lane in flight
+        const uint32_t n = e1 - e0;
+        for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
+          uint32_t v[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            if (b0 + lane + 32 * j < n) v[j] = P.exc_ent[e0 + b0 + lane + 32 * j];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            if (b0 + lane + 32 * j < n) sent[b0 + lane + 32 * j] = v[j];
+        }
       }
       __syncwarp();
       if (lane == 0) {
@@ -568,11 +593,59 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         accb = 0;
         accph ^= 1u;
       }
-      if (!wait(&B.acc_full[cur], cur_ph)) break;
-      tc_fence_after();
       const int c_first = unit_owner(int64_t(t) * KB, U, G);
       const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
       const int nsplit = c_last - c_first + 1;
+      // Partial slots are laid out [chunk][row][16] floats: each thread's 16
+      // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
+      auto slot_of = [&](int cc) {
+        const int ft = int(unit_begin(cc, U, G) / KB);
+        return 2 * cc + (t == ft ? 0 : 1);
+      };
+      // The CTA's final segment ends the kernel. When its tile has one other
+      // piece and that piece is already done (it was the first piece its CTA
+      // processed, so it usually is), its partial is fetched while this
+      // segment's last units are still in flight, and the tile is finished
+      // here without writing a partial or taking a counter round trip.
+      const int me = c - c_first;
+      int pref = 0;
+      if (seg_end == ue && nsplit == 2 && nchunks == 1) {
+        if (et == 0) {
+          int done = 0;
+          const uint64_t t0 = globaltimer_ns();
+          for (;;) {
+            if (ld_acquire_gpu(&P.counters[t]) == nsplit - 1) {
+              done = 1;
+              break;
+            }
+            if (mbar_try_wait(&B.acc_full[cur], cur_ph)) {
+              done = ld_acquire_gpu(&P.counters[t]) == nsplit - 1;
+              break;
+            }
+            if (*abort_flag || globaltimer_ns() - t0 > lim) break;  // the wait below reports it
+          }
+          *pref_flag = done;
+        }
+        named_bar_sync(kEpiBar, 128);
+        pref = *pref_flag;
+        if (pref) {
+          const float4* s0 =
+              reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + 1 - me)) * P.Mpad * 128) + size_t(row) * 4;
+          // Parked in this thread's own column of the transpose buffer (free
+          // until this segment's epilogue writes the same places).
+          float* sc = scratch + row;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float4 f = __ldcg(s0 + x);
+            sc[(4 * x) * kScratchStride] = f.x;
+            sc[(4 * x + 1) * kScratchStride] = f.y;
+            sc[(4 * x + 2) * kScratchStride] = f.z;
+            sc[(4 * x + 3) * kScratchStride] = f.w;
+          }
+        }
+      }
+      if (!wait(&B.acc_full[cur], cur_ph)) break;
+      tc_fence_after();
       // Issuer k wrote accumulator (cur, k) iff the segment holds a unit i
       // (counted from the CTA's first unit) with i % issuers == k.
       const int ia = int(seg_begin - ub), nseg = int(seg_end - seg_begin);
@@ -589,19 +662,29 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           have = true;
         }
       };
-      if (nsplit == 1) {
+      if (nsplit == 1 || pref) {
         for (int mc = 0; mc < nchunks; ++mc) {
           float v[16];
           load_acc(mc, v);
+          if (pref) {
+            // Same slot-order sum as the fixup below (own piece at position me).
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const float o = scratch[x * kScratchStride + row];
+              float acc = 0.0f;
+              acc += me == 0 ? v[x] : o;
+              acc += me == 0 ? o : v[x];
+              v[x] = acc;
+            }
+          }
           if (kArgmax) argmax_chunk(v, t, mc);
           else store_chunk(v, t, mc);
         }
         tc_fence_before();
         mbar_arrive(&B.acc_empty[cur]);
+        if (pref && et == 0) P.counters[t] = 0;  // every other contributor has already counted
       } else {
         const int slot = 2 * c + (t == first_tile ? 0 : 1);
-        // Partial slots are laid out [chunk][row][16] floats: each thread's 16
-        // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
         float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
         for (int mc = 0; mc < nchunks; ++mc) {
           float v[16];
@@ -621,44 +704,57 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           *last_flag = (old == nsplit - 1) ? 1 : 0;
         }
         named_bar_sync(kEpiBar, 128);
-        if (*last_flag) {
-          for (int mc = 0; mc < nchunks; ++mc) {
-            float v[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = 0.0f;
-            // Two slots per round trip, summed in slot order (deterministic).
-            for (int sp0 = 0; sp0 < nsplit; sp0 += 2) {
-              float4 tmp[2][4];
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                if (sp0 + j < nsplit) {
-                  const int cc = c_first + sp0 + j;
-                  const int ft = int(unit_begin(cc, U, G) / KB);
-                  const int sl = 2 * cc + (t == ft ? 0 : 1);
-                  const float4* src =
-                      reinterpret_cast<const float4*>(P.parts + size_t(sl) * P.Mpad * 128) + (size_t(mc) * 128 + row) * 4;
-#pragma unroll
-                  for (int x = 0; x < 4; ++x) tmp[j][x] = __ldcg(src + x);
-                }
-              }
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                if (sp0 + j < nsplit) {
-#pragma unroll
-                  for (int x = 0; x < 4; ++x) {
-                    v[4 * x] += tmp[j][x].x;
-                    v[4 * x + 1] += tmp[j][x].y;
-                    v[4 * x + 2] += tmp[j][x].z;
-                    v[4 * x + 3] += tmp[j][x].w;
-                  }
-                }
-              }
+        // In the final segment every stage of the ring has been consumed (the
+        // segment's MMAs completed), so the other pieces' partials can all be
+        // brought in with bulk copies at once: one round trip, not one per
+        // pair of slots. This CTA's own piece is then taken from TMEM.
+        const uint32_t gather_bytes = uint32_t(nsplit - 1) * uint32_t(nchunks) * 8192u;
+        const bool gather = seg_end == ue && gather_bytes <= uint32_t(S) * plan.stage_bytes;
+        bool have = *last_flag != 0;
+        if (have && gather) {
+          if (et == 0) {
+            mbar_arrive_expect_tx(B.gather, gather_bytes);
+            int j = 0;
+            for (int sp = 0; sp < nsplit; ++sp) {
+              if (sp == me) continue;
+              const float* src = P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128;
+              for (int mc = 0; mc < nchunks; ++mc)
+                bulk_load(smem + uint32_t(j * nchunks + mc) * 8192u, src + size_t(mc) * 128 * 16, 8192u, B.gather);
+              ++j;
             }
-            if (kArgmax) argmax_chunk(v, t, mc);
-            else store_chunk(v, t, mc);
           }
-          if (et == 0) P.counters[t] = 0;
+          have = wait(B.gather, 0);
         }
+        if (have) {
+          for (int mc = 0; mc < nchunks; ++mc) {
+            float r[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = 0.0f;
+            // Slot order, so the sum does not depend on which CTA finishes
+            // the tile or by which path.
+            for (int sp = 0, j = 0; sp < nsplit; ++sp) {
+              float q[16];
+              if (gather && sp == me) {
+                load_acc(mc, q);
+              } else {
+                const float4* src =
+                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nchunks + mc) * 8192u) + row * 4
+                           : reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128) +
+                                 (size_t(mc) * 128 + row) * 4;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                  const float4 f = gather ? src[x] : __ldcg(src + x);
+                  q[4 * x] = f.x, q[4 * x + 1] = f.y, q[4 * x + 2] = f.z, q[4 * x + 3] = f.w;
+                }
+              }
+#pragma unroll
+              for (int x = 0; x < 16; ++x) r[x] += q[x];
+            }
+            if (kArgmax) argmax_chunk(r, t, mc);
+            else store_chunk(r, t, mc);
+          }
+        }
+        if (*last_flag && et == 0) P.counters[t] = 0;
         named_bar_sync(kEpiBar, 128);
       }
     }
@@ -718,7 +814,7 @@ int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, c
   GemmShape sh;
   int st = gemm_shape(M, N, K, &sh);
   if (st) return st;
-  if (!X || !aligned(X, 16) || !ws) return W12_ERR_ARG;
+  if (!X || !aligned(X, 16) || !ws || !aligned(ws, 16)) return W12_ERR_ARG;
   if (argmax_mode ? (!amax_val || !amax_idx) : !Y) return W12_ERR_ARG;
   if (w12_mode) {
     if (!W || !W->p0 || !W->p1 || !W->p2 || !W->ebase || !W->exc_off) return W12_ERR_ARG;
