@@ -6,6 +6,12 @@ activation rows and finishes with the fused W12 LM head, row argmax and
 greedy acceptance. Capturing the launches removes per-call host overhead
 (Python, ctypes, argument checks), which otherwise dominates the short
 layer GEMMs at M = 16.
+
+Inputs (activations X, hidden states H, draft block) live in one device
+buffer mirrored by one pinned host buffer, and the results (accept_len,
+bonus, argmax) in one device buffer mirrored by one pinned host buffer, so
+the host path is one graph: a single host-to-device copy, the step, and a
+single device-to-host copy.
 """
 from __future__ import annotations
 
@@ -24,18 +30,31 @@ class VerifyStep:
         self.layers = layers
         self.head = head
         M = self.M
-        self.X = [torch.zeros((M, w.K), dtype=torch.bfloat16, device=self.dev) for w in layers]
+        # Input layout (byte offsets, 256-aligned): X[0..L), H, draft.
+        shapes = [((M, w.K), torch.bfloat16) for w in layers] + [((M, head.K), torch.bfloat16), ((B, T), torch.int32)]
+        offs, off = [], 0
+        for shp, dt in shapes:
+            offs.append(off)
+            off += -(-shp[0] * shp[1] * (2 if dt == torch.bfloat16 else 4) // 256) * 256
+        self._in_dev = torch.zeros(off, dtype=torch.uint8, device=self.dev)
+        self._in_host = torch.zeros(off, dtype=torch.uint8).pin_memory()
+
+        def carve(buf):
+            return [buf[o:o + shp[0] * shp[1] * (2 if dt == torch.bfloat16 else 4)].view(dt).view(shp)
+                    for o, (shp, dt) in zip(offs, shapes)]
+
+        *self.X, self.H, self.draft = carve(self._in_dev)
+        *self._X_host, self._H_host, self._draft_host = carve(self._in_host)
         self.Y = [torch.empty((M, w.N), dtype=torch.float32, device=self.dev) for w in layers]
         self.ws = [w12.workspace(w12.gemm_ws_bytes(M, w.N, w.K), self.dev) for w in layers]
-        self.H = torch.zeros((M, head.K), dtype=torch.bfloat16, device=self.dev)
-        self.draft = torch.zeros((B, T), dtype=torch.int32, device=self.dev)
         self.hws = w12.workspace(w12.verify_ws_bytes(M, head.N), self.dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.dev)
-        self.accept_len = torch.empty(B, dtype=torch.int32, device=self.dev)
-        self.bonus = torch.empty(B, dtype=torch.int32, device=self.dev)
-        self.argmax = torch.empty(M, dtype=torch.int32, device=self.dev)
+        # Results: [accept_len (B) | bonus (B) | argmax (M)] int32.
+        self._out_dev = torch.zeros(2 * B + M, dtype=torch.int32, device=self.dev)
+        self._out_host = torch.zeros(2 * B + M, dtype=torch.int32).pin_memory()
+        self.accept_len, self.bonus, self.argmax = self._out_dev[:B], self._out_dev[B:2 * B], self._out_dev[2 * B:]
         self.graph = None
-        self._host = None
+        self.graph_host = None
 
     @property
     def packed_bytes(self) -> int:
@@ -69,32 +88,51 @@ class VerifyStep:
             self.capture()
         self.graph.replay()
 
-    def run_host(self, xs_host, H_host, draft_host):
+    def host_inputs(self):
+        """Pinned host views (X list, H, draft) that run_host copies in.
+
+        Writing the next step's inputs here saves run_host a host-side copy.
+        """
+        return self._X_host, self._H_host, self._draft_host
+
+    def capture_host(self):
+        """Record copy-in, step and copy-out into one CUDA graph."""
+        self.run()
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._in_dev.copy_(self._in_host, non_blocking=True)
+            self.run()
+            self._out_host.copy_(self._out_dev, non_blocking=True)
+        torch.cuda.synchronize(self.dev)
+        self.graph_host = g
+        return self
+
+    def run_host(self, xs_host=None, H_host=None, draft_host=None):
         """One end-to-end step from pinned host inputs to host results.
 
-        Copies the activations, hidden states and draft block in, replays the
-        captured step, and copies (accept_len, bonus, argmax) back; returns
-        host tensors (valid after the current stream synchronises).
+        Inputs given here are first copied into the pinned staging buffer
+        (host_inputs(); pass None for any already written there). One graph
+        then copies the staging buffer to the device, runs the step and copies
+        (accept_len, bonus, argmax) back. Returns host tensors, valid after
+        the current stream synchronises; the next run_host overwrites them.
         """
-        if self._host is None:
-            n = 2 * self.B + self.M
-            self._host = (torch.empty(n, dtype=torch.int32).pin_memory(),
-                          torch.empty(n, dtype=torch.int32, device=self.dev))
-        hout, dout = self._host
-        for x, h in zip(self.X, xs_host):
-            x.copy_(h, non_blocking=True)
-        self.H.copy_(H_host, non_blocking=True)
-        self.draft.copy_(draft_host, non_blocking=True)
-        self.replay()
+        if xs_host is not None:
+            for dst, src in zip(self._X_host, xs_host):
+                if src.data_ptr() != dst.data_ptr():
+                    dst.copy_(src)
+        for dst, src in ((self._H_host, H_host), (self._draft_host, draft_host)):
+            if src is not None and src.data_ptr() != dst.data_ptr():
+                dst.copy_(src)
+        if self.graph_host is None:
+            self.capture_host()
+        self.graph_host.replay()
         B = self.B
-        dout[:B].copy_(self.accept_len)
-        dout[B:2 * B].copy_(self.bonus)
-        dout[2 * B:].copy_(self.argmax)
-        hout.copy_(dout, non_blocking=True)
-        return hout[:B], hout[B:2 * B], hout[2 * B:]
+        h = self._out_host
+        return h[:B], h[B:2 * B], h[2 * B:]
 
     def h2d_bytes(self) -> int:
-        return sum(x.numel() * 2 for x in self.X) + self.H.numel() * 2 + self.draft.numel() * 4
+        return self._in_host.numel()
 
     def d2h_bytes(self) -> int:
-        return (2 * self.B + self.M) * 4
+        return self._out_host.numel() * 4
