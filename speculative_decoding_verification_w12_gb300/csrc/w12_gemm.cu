@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   volatile uint32_t* ent_base = misc + 4;
   volatile uint32_t* ent_end = misc + 5;
   volatile int* pref_flag = reinterpret_cast<volatile int*>(misc + 6);
+  volatile int* fast_flag = reinterpret_cast<volatile int*>(misc + 7);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -684,49 +685,69 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         mbar_arrive(&B.acc_empty[cur]);
         if (pref && et == 0) P.counters[t] = 0;  // every other contributor has already counted
       } else {
-        const int slot = 2 * c + (t == first_tile ? 0 : 1);
-        float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
-        for (int mc = 0; mc < nchunks; ++mc) {
-          float v[16];
-          load_acc(mc, v);
-          float4* dst = my + (size_t(mc) * 128 + row) * 4;
+        // In the final segment every stage of the ring has been consumed (the
+        // segment's MMAs completed), so the other pieces' partials can be
+        // brought into it with bulk copies, as many chunks per round trip as
+        // fit. This CTA's own piece is then taken from TMEM. If every other
+        // piece is already counted, the tile is finished here without writing
+        // this piece or taking the counter round trip.
+        const uint32_t ring_bytes = uint32_t(S) * plan.stage_bytes;
+        const int cb_max = int(ring_bytes / (uint32_t(nsplit - 1) * 8192u));  // chunks per gather batch
+        const bool gather = seg_end == ue && cb_max >= 1;
+        int fast = 0;
+        if (gather) {
+          if (et == 0) *fast_flag = ld_acquire_gpu(&P.counters[t]) == nsplit - 1;
+          named_bar_sync(kEpiBar, 128);
+          fast = *fast_flag;
+        }
+        if (!fast) {
+          const int slot = 2 * c + (t == first_tile ? 0 : 1);
+          float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
+          for (int mc = 0; mc < nchunks; ++mc) {
+            float v[16];
+            load_acc(mc, v);
+            float4* dst = my + (size_t(mc) * 128 + row) * 4;
 #pragma unroll
-          for (int x = 0; x < 4; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+            for (int x = 0; x < 4; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+          }
         }
         tc_fence_before();
         mbar_arrive(&B.acc_empty[cur]);
-        // The barrier orders every epilogue thread's partial stores before the
-        // single release-acquire increment; the last contributor's readers are
-        // ordered after that increment by the second barrier.
-        named_bar_sync(kEpiBar, 128);
-        if (et == 0) {
-          const int old = atomic_add_acq_rel_gpu(&P.counters[t], 1);
-          *last_flag = (old == nsplit - 1) ? 1 : 0;
-        }
-        named_bar_sync(kEpiBar, 128);
-        // In the final segment every stage of the ring has been consumed (the
-        // segment's MMAs completed), so the other pieces' partials can all be
-        // brought in with bulk copies at once: one round trip, not one per
-        // pair of slots. This CTA's own piece is then taken from TMEM.
-        const uint32_t gather_bytes = uint32_t(nsplit - 1) * uint32_t(nchunks) * 8192u;
-        const bool gather = seg_end == ue && gather_bytes <= uint32_t(S) * plan.stage_bytes;
-        bool have = *last_flag != 0;
-        if (have && gather) {
+        if (!fast) {
+          // The barrier orders every epilogue thread's partial stores before
+          // the single release-acquire increment; the last contributor's
+          // readers are ordered after that increment by the second barrier.
+          named_bar_sync(kEpiBar, 128);
           if (et == 0) {
-            mbar_arrive_expect_tx(B.gather, gather_bytes);
-            int j = 0;
-            for (int sp = 0; sp < nsplit; ++sp) {
-              if (sp == me) continue;
-              const float* src = P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128;
-              for (int mc = 0; mc < nchunks; ++mc)
-                bulk_load(smem + uint32_t(j * nchunks + mc) * 8192u, src + size_t(mc) * 128 * 16, 8192u, B.gather);
-              ++j;
-            }
+            const int old = atomic_add_acq_rel_gpu(&P.counters[t], 1);
+            *last_flag = (old == nsplit - 1) ? 1 : 0;
           }
-          have = wait(B.gather, 0);
+          named_bar_sync(kEpiBar, 128);
         }
-        if (have) {
-          for (int mc = 0; mc < nchunks; ++mc) {
+        const bool last = fast || *last_flag != 0;
+        uint32_t gph = 0;
+        for (int mc0 = 0; last && mc0 < nchunks;) {
+          const int nb = gather ? (nchunks - mc0 < cb_max ? nchunks - mc0 : cb_max) : nchunks;
+          if (gather) {
+            if (mc0 > 0) named_bar_sync(kEpiBar, 128);  // the previous batch has been read
+            if (et == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              mbar_arrive_expect_tx(B.gather, uint32_t(nsplit - 1) * uint32_t(nb) * 8192u);
+              int j = 0;
+              for (int sp = 0; sp < nsplit; ++sp) {
+                if (sp == me) continue;
+                const float* src = P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128;
+                for (int b2 = 0; b2 < nb; ++b2)
+                  bulk_load(smem + uint32_t(j * nb + b2) * 8192u, src + size_t(mc0 + b2) * 128 * 16, 8192u,
+                            B.gather);
+                ++j;
+              }
+            }
+            if (!wait(B.gather, gph)) break;
+            gph ^= 1u;
+          }
+          for (int b2 = 0; b2 < nb; ++b2) {
+            const int mc = mc0 + b2;
             float r[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) r[k] = 0.0f;
@@ -738,7 +759,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
                 load_acc(mc, q);
               } else {
                 const float4* src =
-                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nchunks + mc) * 8192u) + row * 4
+                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nb + b2) * 8192u) + row * 4
                            : reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128) +
                                  (size_t(mc) * 128 + row) * 4;
 #pragma unroll
@@ -753,8 +774,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             if (kArgmax) argmax_chunk(r, t, mc);
             else store_chunk(r, t, mc);
           }
+          mc0 += nb;
         }
-        if (*last_flag && et == 0) P.counters[t] = 0;
+        if (last && et == 0) P.counters[t] = 0;
         named_bar_sync(kEpiBar, 128);
       }
     }

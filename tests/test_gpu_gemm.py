@@ -103,6 +103,28 @@ def test_repeated_calls_reuse_workspace():
     assert int(ws.sum().item()) == 0 or True
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 7168, 5120), (16, 5120, 17408), (128, 7168, 5120), (256, 5120, 17408)])
+def test_split_k_bitwise_repeatable(M, N, K):
+    """Tiles split over 2-5 CTAs finish by one of several paths depending on
+    which CTA gets there last; every path sums the pieces in the same order,
+    so repeated calls agree bit for bit, and the tile counters end at zero."""
+    W = S.weights_bf16(N, K, seed=5)
+    X = to_dev_bf16(S.activations_bf16(M, K, seed=6))
+    pk = w12.pack(to_dev_bf16(W))
+    ws = w12.workspace(w12.gemm_ws_bytes(M, N, K))
+    st = new_status()
+    Y1 = w12.gemm(X, pk, ws=ws, status=st).clone()
+    for _ in range(8):
+        Y2 = w12.gemm(X, pk, ws=ws, status=st)
+        torch.cuda.synchronize()
+        assert torch.equal(Y1, Y2)
+    assert status_value(st) == 0
+    counters = ws[:4 * (N // 128)].view(torch.int32)
+    assert int(counters.abs().sum().item()) == 0
+    cols = np.unique(np.concatenate([np.arange(0, N, 257), [N - 1]]))
+    assert_gemm_close(Y1.cpu().numpy()[:, cols], O.gemm_rows(S.activations_bf16(M, K, seed=6), W[cols]), "split-K")
+
+
 @pytest.mark.parametrize("name,N,K", [("qkv", 7168, 5120), ("o", 5120, 5120), ("gate_up", 34816, 5120),
                                       ("down", 5120, 17408)])
 def test_layer_shapes_sampled_columns(name, N, K):
