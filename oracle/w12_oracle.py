@@ -36,6 +36,14 @@ What it computes, and the passage each part follows:
   target weights; "Reasons" bullet 2: the weights are restored before the
   contraction). Products of two bf16 values are exact in float64.
 
+* ``swiglu`` / ``f64_to_bf16`` -- the gated activation between a dense
+  layer's fused gate/up projection and its down projection, for the grouped
+  launch that runs both: act = bf16(silu(g) * u), silu(g) = g / (1 + e^-g),
+  [g | u] = the two halves of the gate/up output along N, rounded to the
+  nearest bf16 (ties to even). The pages give the layer shapes' role (the
+  verify pass reads every target weight: SpecPilot digest, summary) but no
+  activation; the gated SiLU of dense decoder layers is this build's reading.
+
 * ``argmax_rows`` -- greedy target token per row, lowest index on ties, with
   the top-2 gap (SpecPilot digest, "Risks" bullet 3: lossless means every
   token is the target's greedy choice; batched verify may flip near-ties).
@@ -209,6 +217,33 @@ def gemm(X_bits: np.ndarray, pk: dict) -> np.ndarray:
 def gemm_rows(X_bits: np.ndarray, W_bits_rows: np.ndarray) -> np.ndarray:
     """Y columns for explicit weight rows (bf16 bits [n, K]) in float64."""
     return bf16_to_f64(X_bits) @ bf16_to_f64(W_bits_rows).T
+
+
+def f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    """bf16 bits (uint16) of float64 values, rounded to nearest, ties to even.
+
+    Written from the definition: bf16 keeps 8 significant bits, so with
+    x = m * 2**e (0.5 <= |m| < 1) the unit in the last place is 2**(e - 8)
+    (never below the subnormal step 2**-133); x / ulp is rounded half-even to
+    an integer and scaled back, which is exact in float64. Finite inputs
+    only; overflow past the largest bf16 becomes infinity.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    ulp_exp = np.maximum(e.astype(np.int64) - 8, -133)
+    q = np.rint(np.ldexp(x, -ulp_exp))           # np.rint rounds halves to even
+    y = np.ldexp(q, ulp_exp)
+    with np.errstate(over="ignore"):
+        b = y.astype(np.float32).view(np.uint32)
+    return (b >> 16).astype(np.uint16)
+
+
+def swiglu(Y: np.ndarray) -> np.ndarray:
+    """act bits [M, N/2] = bf16(silu(Y[:, :N/2]) * Y[:, N/2:]) from float Y [M, N]."""
+    Y = np.asarray(Y, dtype=np.float64)
+    h = Y.shape[1] // 2
+    g, u = Y[:, :h], Y[:, h:]
+    return f64_to_bf16(g / (1.0 + np.exp(-g)) * u)
 
 
 def argmax_rows(logits: np.ndarray):

@@ -226,3 +226,59 @@ def test_oracle_gap_pin_math():
     b = math.nextafter(1.0, 0.0)
     idx, gap = O.argmax_rows(np.array([[b, a, b]]))
     assert idx[0] == 1 and gap[0] == a - b
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding and the gated activation of the grouped launch
+# ---------------------------------------------------------------------------
+
+def _finite_bf16_values():
+    bits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):          # signalling-NaN patterns raise "invalid" when widened
+        vals = (bits << 16).view(np.float32).astype(np.float64)
+    ok = np.isfinite(vals)
+    return bits[ok].astype(np.uint16), vals[ok]
+
+
+def test_f64_to_bf16_hand_values():
+    # Derived by hand: 1 + 1/256 lies halfway between 1.0 (0x3F80) and
+    # 1.0078125 (0x3F81): the tie goes to the even mantissa 0x3F80; 1 + 3/256
+    # lies halfway between 0x3F81 and 0x3F82 and goes to 0x3F82.
+    # 1/(1 + e^-1) = 0.73105857... = 1.4621 * 2^-1; 0.4621 * 128 = 59.15 -> 59:
+    # exponent 126, mantissa 59 -> 0x3F3B. -2.5 = -1.25 * 2^1 -> 0xC020.
+    x = np.array([1.0, 1 + 1 / 256, 1 + 3 / 256, 1 / (1 + math.exp(-1)), -2.5, 0.0])
+    got = O.f64_to_bf16(x)
+    np.testing.assert_array_equal(got, np.array([0x3F80, 0x3F80, 0x3F82, 0x3F3B, 0xC020, 0x0000], dtype=np.uint16))
+
+
+def test_f64_to_bf16_exhaustive_exact_and_midpoints():
+    """Every finite bf16 value maps to itself; the float64 midpoint of two
+    neighbours (same sign, increasing magnitude) goes to the one with the even
+    mantissa, and one float64 step off the midpoint goes to the nearer one."""
+    bits, vals = _finite_bf16_values()
+    np.testing.assert_array_equal(O.f64_to_bf16(vals)[vals != 0], bits[vals != 0])
+    pos = (bits < 0x7F7F) & (vals > 0)            # positive, with a finite successor
+    lo_b, lo_v = bits[pos], vals[pos]
+    hi_v = ((lo_b.astype(np.uint32) + 1) << 16).view(np.float32).astype(np.float64)
+    mid = (lo_v + hi_v) / 2                        # exact in float64
+    even = np.where(lo_b % 2 == 0, lo_b, lo_b + 1).astype(np.uint16)
+    np.testing.assert_array_equal(O.f64_to_bf16(mid), even)
+    np.testing.assert_array_equal(O.f64_to_bf16(np.nextafter(mid, 0)), lo_b)
+    np.testing.assert_array_equal(O.f64_to_bf16(np.nextafter(mid, np.inf)), (lo_b + 1).astype(np.uint16))
+    np.testing.assert_array_equal(O.f64_to_bf16(-mid), even | 0x8000)
+
+
+def test_swiglu_closed_forms_and_halves():
+    # silu(0) = 0, and u = 0 zeroes the product; silu(1) * 1 = 0x3F3B (above).
+    Y = np.array([[0.0, 1.0, 3.0, 7.0],
+                  [1.0, 2.0, 1.0, 0.0]])
+    act = O.swiglu(Y)
+    assert act.shape == (2, 2)
+    assert act[0, 0] == 0 and act[1, 1] == 0
+    assert act[1, 0] == 0x3F3B
+    # Large gate: silu(g) -> g, so act -> g * u: 40 * 0.5 = 20 exactly after rounding (0x41A0).
+    assert O.swiglu(np.array([[40.0, 0.5]]))[0, 0] == 0x41A0
+    # Very negative gate: silu(g) -> 0 (|act| below the bf16 subnormal step).
+    assert O.swiglu(np.array([[-200.0, 1.0]]))[0, 0] in (0x0000, 0x8000)
+    # The gate is the first half: swapping the halves changes the result.
+    assert O.swiglu(np.array([[2.0, -1.0]]))[0, 0] != O.swiglu(np.array([[-1.0, 2.0]]))[0, 0]
