@@ -361,7 +361,28 @@ def run_ours(args, world, rank, local):
                                            for a, wb in zip(gemms, wbf)], dev, stream)
         chain["bf16_gbs"] = sum(N * K * 2 for _, N, K in LAYER) / (chain["bf16_ms"] * 1e-3) / 1e9
         chain["bf16_over_w12"] = chain["bf16_ms"] / chain["w12_ms"]
+    # The same four GEMMs as grouped launches (one persistent kernel): all
+    # four with their own inputs, and the MLP form where down multiplies
+    # SwiGLU(gate_up) computed inside the launch (its X is not an input).
+    grp = {}
+    g_ind = w12.Grouped([(x, pk, y) for x, pk, y in zip(st.X, packs, st.Y)], M_ROWS)
+    grp["w12_independent_ms"] = graph_chain_ms([g_ind.run], dev, stream)
+    g_mlp = w12.Grouped([(st.X[0], packs[0], st.Y[0]), (st.X[1], packs[1], st.Y[1]),
+                         (st.X[2], packs[2], st.Y[2]), (None, packs[3], st.Y[3])], M_ROWS, swiglu=(2, 3))
+    grp["w12_swiglu_ms"] = graph_chain_ms([g_mlp.run], dev, stream)
+    if wbf:
+        b_ind = w12.Grouped([(x, wb, y) for x, wb, y in zip(st.X, wbf, st.Y)], M_ROWS, bf16=True)
+        grp["bf16_independent_ms"] = graph_chain_ms([b_ind.run], dev, stream)
+        b_mlp = w12.Grouped([(st.X[0], wbf[0], st.Y[0]), (st.X[1], wbf[1], st.Y[1]),
+                             (st.X[2], wbf[2], st.Y[2]), (None, wbf[3], st.Y[3])], M_ROWS, swiglu=(2, 3), bf16=True)
+        grp["bf16_swiglu_ms"] = graph_chain_ms([b_mlp.run], dev, stream)
+        del b_ind, b_mlp
+    for k in list(grp):
+        grp[k.replace("_ms", "_gbs")] = ((layer_bytes if k.startswith("w12") else sum(N * K * 2 for _, N, K in LAYER))
+                                         / (grp[k] * 1e-3) / 1e9)
     bf16_detail["layer_graph_chained"] = chain
+    bf16_detail["layer_grouped_launch"] = grp
+    del g_ind, g_mlp
     del wbf
 
     if rank != 0:

@@ -154,6 +154,55 @@ int w12_gemm_noalloc(const uint16_t* X, int64_t M, const w12_weights* W, float* 
 int w12_gemm_bf16_ref(const uint16_t* X, int64_t M, const uint16_t* W, int64_t N, int64_t K,
                       float* Y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* --- Grouped verify GEMMs in one launch -------------------------------- */
+/* The verify pass reads every target weight each step (SpecPilot digest,
+ * summary); a dense layer has several such GEMMs at the same M. A grouped
+ * launch runs up to 4 of them in one persistent kernel: their 128x128 units
+ * are split evenly over the SMs as one stream (one ramp-up and one tail for
+ * the group instead of one per GEMM). With a SwiGLU link, problem `to` takes
+ * as X the gated activation of problem `from`'s output, computed inside the
+ * launch: act[m, j] = bf16(silu(Y_from[m, j]) * Y_from[m, N_from/2 + j]),
+ * silu(g) = g / (1 + exp(-g)), rounded to nearest even. The pages give no
+ * MLP activation; this is the gated SiLU of dense decoder layers, with the
+ * gate in the first half of the fused gate/up output. The target's units run
+ * after every other problem's (a second phase) and each of its k-blocks
+ * starts once that block of act is written.
+ *
+ * problems: X [M, K] bf16 row-major (16-byte aligned; unused for the link
+ * target), weights (W for w12_gemm_grouped; Wbf16 with N, K for the bf16
+ * baseline), Y [M, N] fp32 output. All problems share M (1..256). The link
+ * needs N_from % 256 == 0 and K_to == N_from / 2; act is caller-owned
+ * [M, N_from/2] bf16, 16-byte aligned, and is overwritten. Y_from is written
+ * as well. The workspace must be zero-filled before its first use; the
+ * library leaves it ready for the next call after a W12_OK call (zero it
+ * again after any error). Grouped calls that share a workspace must not
+ * overlap on the GPU. Errors: W12_ERR_ARG, W12_ERR_SHAPE (a shape rule, or
+ * more than 1023 units per SM), W12_ERR_WORKSPACE, W12_ERR_UNSUPPORTED,
+ * W12_ERR_CUDA; W12_ERR_TIMEOUT in dev_status if a wait gives up. */
+typedef struct w12_problem {
+  const uint16_t* X;
+  const w12_weights* W;
+  const uint16_t* Wbf16;
+  int64_t N, K;
+  float* Y;
+} w12_problem;
+
+typedef struct w12_swiglu {
+  int from, to;
+  uint16_t* act;
+} w12_swiglu;
+
+/* Workspace bytes for a grouped call (0 if the arguments are invalid).
+ * probs[i].W decides the mode: W12 if probs[0].W is set, else bf16. */
+size_t w12_gemm_grouped_ws_bytes(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link);
+
+int w12_gemm_grouped(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link,
+                     void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* The same grouped launch over plain bf16 weights (in-tree baseline). */
+int w12_gemm_grouped_bf16_ref(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link,
+                              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* --- Greedy block verification (SpecPilot digest, "Risks" bullet 3) ----- */
 
 /* Workspace bytes for the verify entry points with M = B*rows verified rows

@@ -1,0 +1,1278 @@
+// Grouped verify GEMMs: several W12 (or bf16) GEMMs of one layer in one
+// persistent launch, optionally with the gate/up -> SwiGLU -> down dependency
+// inside the launch.
+//
+// The verify pass reads every target weight each step (SpecPilot paper
+// digest, summary paragraph); the layer's GEMMs all share M, so their
+// 128x128 units can be split over the SMs as one stream: the launch pays one
+// ramp-up and one tail for the group instead of one per GEMM. Problems whose
+// X is produced inside the launch (the down projection, whose X is the gated
+// activation of the gate/up output) form a second phase: every CTA works
+// through its share of phase 0 and then of phase 1, and each phase-1 k-block
+// waits (bounded) for a per-block ready flag written by the CTA that completes
+// the block's two gate/up tiles. Flags carry a launch epoch, moved on by the
+// last CTA to finish, so one workspace serves consecutive launches.
+//
+// The kernel body follows the single-GEMM kernel of this library (warp roles,
+// ring, TMEM buffers, stream-K fixup), generalised from one problem to a list
+// of problems; it lives in its own translation unit and namespace so that the
+// single-GEMM kernel keeps its own tuned code.
+#include <cstring>
+
+#include "w12_dev.cuh"
+#include "w12_host.h"
+
+namespace w12 {
+namespace grouped_impl {
+
+// Decode warps: W12_DEC_GROUPS groups of 4 x W12_DEC_SPLIT warps. Each warp
+// serves one TMEM lane quarter (32 rows); the W12_DEC_SPLIT warps of a
+// quarter in a group split the unit's 4 chunks of 32 values; groups take
+// units in turn (unit i goes to group i % W12_DEC_GROUPS).
+#ifndef W12_DEC_GROUPS
+#define W12_DEC_GROUPS 2
+#endif
+#ifndef W12_DEC_SPLIT
+#define W12_DEC_SPLIT 1
+#endif
+static_assert(W12_DEC_GROUPS >= 1 && W12_DEC_GROUPS <= 3, "decode groups: 1..3");
+static_assert(W12_DEC_SPLIT == 1 || W12_DEC_SPLIT == 2 || W12_DEC_SPLIT == 4, "decode split: 1, 2 or 4");
+constexpr int kDecGroups = W12_DEC_GROUPS;
+constexpr int kDecSplit = W12_DEC_SPLIT;
+constexpr int kChunksPerThread = 4 / kDecSplit;  // 32-value chunks each decode thread restores per unit
+constexpr int kMaxStages = 8;         // smem ring depth limit (one TMEM A buffer per stage)
+constexpr int kAColsPerBuf = 64;      // 128 K values = 64 columns of bf16 pairs
+constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
+constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
+constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
+
+// One GEMM of a launch. A launch runs up to kMaxProb GEMMs (problems) that
+// share M, in at most two phases: the units of each phase are split evenly
+// over the CTAs (stream-K over the concatenated problems), and every CTA
+// works through its share of phase 0 and then of phase 1. Phase 1 holds the
+// problem whose X is produced inside the launch (the SwiGLU link below).
+struct ProbParams {
+  int N, K, KB, tiles, phase, tile0;  // tile0: first of its tiles in the launch-wide tile numbering
+  int64_t unit0;                      // first unit of the problem in its phase's unit numbering
+  const uint8_t* ebase;
+  const uint32_t* exc_off;
+  const uint32_t* exc_ent;
+  int64_t n_exc;
+  float* Y;
+};
+
+struct GemmParams {
+  int M, Mpad, grid, stages, issuers, nprob, nphase;
+  int pfirst[2];                      // first problem of each phase (problems are ordered by phase)
+  int64_t phase_units[2];
+  ProbParams pr[kMaxProb];
+  float* parts;                       // split-K partial slots: 2 per CTA per phase
+  int32_t* counters;                  // one per tile of the launch
+  float* amax_val;
+  int32_t* amax_idx;
+  // SwiGLU link: problem glu_to multiplies act = bf16(silu(g) * u), where
+  // [g | u] = Y of problem glu_from split in two halves along N; act block j
+  // (columns j*128 .. j*128+127) is written by the CTA that completes the
+  // second of its two Y tiles (j and j + N/256).
+  int glu_from, glu_to, glu_blocks;
+  uint16_t* act;
+  int32_t* glu_cnt;                   // per block: tiles completed (reset to 0 by the writer)
+  int32_t* glu_ready;                 // per block: epoch + 1 once written
+  int32_t* epoch;                     // [0] launch epoch, [1] CTAs finished in this launch
+  int32_t* status;
+  uint64_t limit_ns;
+};
+
+// Tensor maps per problem: three planes (or the bf16 matrix in slot 0) and X.
+struct GemmMaps {
+  CUtensorMap m[kMaxProb][4];
+};
+
+// Position of a unit in a CTA's sequence: phase f, problem p, the problem's
+// tile t and k-block kb, with the problem's KB and tile count cached; left =
+// units of the CTA still to come in this phase (this one included), pos =
+// this unit's place in the CTA's range of the phase. Single-thread loops
+// advance it per unit with 32-bit steps only.
+struct Cur {
+  int f, p, t, kb, KB, tiles, left, pos;
+};
+
+__device__ __forceinline__ int64_t unit_begin(int c, int64_t U, int G) { return int64_t(c) * U / G; }
+
+// CTA that owns unit u: the largest c with floor(c*U/G) <= u.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G) {
+  return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
+}
+
+// Problem of phase f that holds phase unit u.
+__device__ __forceinline__ int prob_of(const GemmParams& P, int f, int64_t u) {
+  int p = P.pfirst[f];
+  while (p + 1 < P.nprob && P.pr[p + 1].phase == f && u >= P.pr[p + 1].unit0) ++p;
+  return p;
+}
+
+// First unit of CTA c at or after phase f; false if it has none.
+__device__ __forceinline__ bool cur_phase(const GemmParams& P, int c, int f, Cur& x) {
+  for (; f < P.nphase; ++f) {
+    const int64_t ub = unit_begin(c, P.phase_units[f], P.grid);
+    const int64_t ue = unit_begin(c + 1, P.phase_units[f], P.grid);
+    if (ub < ue) {
+      x.f = f;
+      x.p = prob_of(P, f, ub);
+      x.KB = P.pr[x.p].KB;
+      x.tiles = P.pr[x.p].tiles;
+      const int64_t loc = ub - P.pr[x.p].unit0;
+      x.t = int(loc / x.KB);
+      x.kb = int(loc % x.KB);
+      x.left = int(ue - ub);
+      x.pos = 0;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Next unit of the CTA's sequence.
+__device__ __forceinline__ bool cur_next(const GemmParams& P, int c, Cur& x) {
+  if (--x.left > 0) {
+    ++x.pos;
+    if (++x.kb == x.KB) {
+      x.kb = 0;
+      if (++x.t == x.tiles) {
+        x.t = 0;
+        ++x.p;
+        x.KB = P.pr[x.p].KB;
+        x.tiles = P.pr[x.p].tiles;
+      }
+    }
+    return true;
+  }
+  return cur_phase(P, c, x.f + 1, x);
+}
+
+// Units of CTA c over all phases.
+__device__ __forceinline__ int cta_units(const GemmParams& P, int c) {
+  int n = 0;
+  for (int f = 0; f < P.nphase; ++f)
+    n += int(unit_begin(c + 1, P.phase_units[f], P.grid) - unit_begin(c, P.phase_units[f], P.grid));
+  return n;
+}
+
+template <bool kW12>
+struct Cfg {
+  static constexpr int kDecWarps = kW12 ? 4 * kDecGroups * kDecSplit : 0;
+  static constexpr int kEpiWarp0 = 4 + kDecWarps;
+  static constexpr int kThreads = (kEpiWarp0 + 4) * 32;
+  static constexpr uint32_t kABytes = kW12 ? 3 * 8192 : 2 * 16384;  // A operand bytes per stage
+  static constexpr uint32_t kEbBytes = kW12 ? 1024 : 0;             // ebase (128 B used)
+  static constexpr uint32_t kTmemCols = kW12 ? 512 : 256;
+};
+
+// Shared memory carve-up (identical on host and device).
+struct SmemPlan {
+  uint32_t stage_bytes, x_off, eb_off, stages;
+  uint32_t scratch_off, red_off, soff_off, sent_off, uprob_off, bar_off, misc_off, total;
+};
+
+template <bool kW12>
+__host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
+  SmemPlan p;
+  p.eb_off = Cfg<kW12>::kABytes;
+  p.x_off = p.eb_off + Cfg<kW12>::kEbBytes;
+  p.stage_bytes = p.x_off + 2u * Mpad * 128u;
+  p.stages = stages;
+  uint32_t off = p.stage_bytes * stages;
+  p.scratch_off = off;
+  off += 16 * kScratchStride * 4;
+  p.red_off = off;
+  off += 4 * 16 * 8;
+  p.soff_off = off;
+  off += kW12 ? (kOffCap + 4) * 4 : 0;
+  p.sent_off = off;
+  off += kW12 ? kEntCap * 4 : 0;
+  p.uprob_off = off;
+  off += kW12 ? kOffCap : 0;
+  off = (off + 15) & ~15u;
+  p.bar_off = off;
+  off += 64 * 8;
+  p.misc_off = off;
+  off += 64;
+  p.total = off + 1024;  // slack for 1024-byte alignment of the base
+  return p;
+}
+
+struct Bars {
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* a_full;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* exc_ready;
+  uint64_t* drain;
+  uint64_t* gather;
+};
+
+template <bool kW12, bool kArgmax, bool kMulti>
+__global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmMaps TM, const __grid_constant__ GemmParams P) {
+  using C = Cfg<kW12>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const SmemPlan plan = smem_plan<kW12>(P.Mpad, P.stages);
+  const int S = P.stages;
+  const int NACC = P.Mpad <= 128 ? 2 : 1;
+
+  uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + plan.bar_off);
+  Bars B;
+  B.full = bar_base;
+  B.empty = bar_base + S;
+  B.a_full = bar_base + 2 * S;
+  B.acc_full = B.a_full + S;
+  B.acc_empty = B.acc_full + 2;
+  B.exc_ready = B.acc_empty + 2;
+  B.drain = B.exc_ready + 1;
+  B.gather = B.drain + 1;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + plan.misc_off);
+  volatile uint32_t* tmem_slot = misc + 0;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(misc + 2);
+  volatile int* ent_in_smem = reinterpret_cast<volatile int*>(misc + 3);
+  volatile uint32_t* ent_base = misc + 4;
+  volatile uint32_t* ent_end = misc + 5;
+  volatile int* pref_flag = reinterpret_cast<volatile int*>(misc + 6);
+  volatile int* fast_flag = reinterpret_cast<volatile int*>(misc + 7);
+  volatile int* glu_flag = reinterpret_cast<volatile int*>(misc + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int G = P.grid;
+  const int n_units = cta_units(P, c);          // this CTA's units over all phases
+  constexpr bool single = !kMulti;  // one problem, one phase: problem 0 everywhere
+  const uint64_t lim = P.limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&B.full[s], 1);
+      mbar_init(&B.empty[s], 1);
+    }
+    if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
+      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * kDecSplit);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&B.acc_full[a], P.issuers);  // one commit per MMA issuer per segment
+      mbar_init(&B.acc_empty[a], 128);
+    }
+    mbar_init(B.exc_ready, 1);
+    mbar_init(B.drain, P.issuers);
+    mbar_init(B.gather, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(const_cast<uint32_t*>(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // TMEM columns: accumulators [0, NACC*issuers*Mpad) (buffer b, issuer k at
+  // column (b*issuers + k)*Mpad), then one 64-column A buffer per stage.
+  const int NISS = P.issuers;
+  const uint32_t a_col0 = uint32_t((NACC * NISS * P.Mpad + 63) & ~63);
+
+  auto fail = [&](int code) {
+    set_status(P.status, code);
+    *abort_flag = 1;
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < 0x80000000u; ++i) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 63u) == 63u) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > lim) {
+          fail(W12_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+    fail(W12_ERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      for (int p = 0; p < P.nprob; ++p) {
+        prefetch_tmap(&TM.m[p][3]);
+        prefetch_tmap(&TM.m[p][0]);
+        if (kW12) {
+          prefetch_tmap(&TM.m[p][1]);
+          prefetch_tmap(&TM.m[p][2]);
+        }
+      }
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t xbox = uint32_t(P.Mpad) * 128u;
+      const uint32_t tx = C::kABytes + (kW12 ? 128u : 0u) + 2u * xbox;
+      // Weight tile of the unit at cursor x into stage buffer st.
+      auto load_w = [&](const Cur& x, uint8_t* st, uint64_t* bar) {
+        const int pp = single ? 0 : x.p;
+        const CUtensorMap* m = TM.m[pp];
+        if (kW12) {
+          tma_load_2d_hint(st, &m[0], x.kb * 64, x.t * 128, bar, pol_w);
+          tma_load_2d_hint(st + 8192, &m[1], x.kb * 64, x.t * 128, bar, pol_w);
+          tma_load_2d_hint(st + 16384, &m[2], x.kb * 64, x.t * 128, bar, pol_w);
+          bulk_load(st + plan.eb_off, P.pr[pp].ebase + int64_t(x.kb) * P.pr[pp].N + int64_t(x.t) * 128, 128u, bar);
+        } else {
+          tma_load_2d_hint(st, &m[0], x.kb * 128, x.t * 128, bar, pol_w);
+          tma_load_2d_hint(st + 16384, &m[0], x.kb * 128 + 64, x.t * 128, bar, pol_w);
+        }
+      };
+      // The first ring-full of weight tiles is requested before waiting for
+      // the previous kernel on the stream (launch overlap); X is loaded, and
+      // anything else is read or written, only after that wait.
+      const int prefill = n_units < S ? n_units : S;
+      Cur x;
+      cur_phase(P, c, 0, x);
+      // One problem: plain (t, kb) counters, as cheap as possible per unit.
+      auto step = [&](Cur& y) {
+        if (kMulti) {
+          cur_next(P, c, y);
+        } else if (++y.kb == y.KB) {
+          y.kb = 0;
+          ++y.t;
+        }
+      };
+      {
+        Cur y = x;
+        for (int i = 0; i < prefill; ++i) {
+          mbar_arrive_expect_tx(&B.full[i], tx);
+          load_w(y, smem + i * plan.stage_bytes, &B.full[i]);
+          step(y);
+        }
+      }
+      grid_dep_wait();
+      const int32_t epoch = kMulti && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool gave_up = false;
+      for (; issued < n_units; ++issued) {
+        uint8_t* st = smem + s * plan.stage_bytes;
+        if (issued >= prefill) {
+          if (!wait(&B.empty[s], ph ^ 1u)) break;
+          mbar_arrive_expect_tx(&B.full[s], tx);
+          load_w(x, st, &B.full[s]);
+        }
+        if (kMulti && x.p == P.glu_to && !gave_up) {
+          // X of this problem is written by this launch: wait until its
+          // k-block is ready (bounded), then make it visible to the copy. If
+          // the wait gives up, the copies are still issued (of stale data) so
+          // that every stage's byte count completes; the status word and the
+          // abort flag already report the failure.
+          const int32_t* rdy = P.glu_ready + x.kb;
+          bool okr = ld_acquire_gpu(rdy) == epoch + 1;
+          const uint64_t t0 = globaltimer_ns();
+          while (!okr) {
+            if (*abort_flag || globaltimer_ns() - t0 > lim) {
+              fail(W12_ERR_TIMEOUT);
+              gave_up = true;
+              break;
+            }
+            okr = ld_acquire_gpu(rdy) == epoch + 1;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        const CUtensorMap* mx = &TM.m[single ? 0 : x.p][3];
+        tma_load_2d_hint(st + plan.x_off, mx, x.kb * 128, 0, &B.full[s], pol_x);
+        tma_load_2d_hint(st + plan.x_off + xbox, mx, x.kb * 128 + 64, 0, &B.full[s], pol_x);
+        step(x);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      grid_dep_launch();
+      if (*abort_flag) {
+        // Let the copies already issued land before the CTA can exit. The
+        // loop only stops at a stage boundary with every stage before it
+        // fully issued (weights and X).
+        for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+          mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, lim);
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA
+    // Issuer k (warp 1 + k, one thread) takes the units i with i % issuers == k
+    // into its own accumulator: one thread can only issue a kind::f16 MMA
+    // every few tens of cycles, so two issuers double the issue rate.
+    const int k = warp - 1;
+    if (lane == 0 && k < NISS) {
+      const uint32_t idesc = idesc_bf16(128, uint32_t(P.Mpad));
+      const uint32_t xbox = uint32_t(P.Mpad) * 128u;
+      // Descriptors of stage 0; other stages and K steps add (byte offset >> 4)
+      // to the 14-bit start-address field, which cannot overflow (smem < 256 KB).
+      const uint32_t st0 = smem_u32(smem);
+      const uint64_t bdesc0 = sdesc_k_sw128(st0 + plan.x_off);
+      const uint64_t adesc0 = sdesc_k_sw128(st0);
+      const uint32_t a_tmem0 = tmem_base + a_col0;
+      Cur x;
+      cur_phase(P, c, 0, x);
+      int s = 0, accb = 0;
+      uint32_t ph = 0, accph = 0;
+      bool started = false;  // this issuer has written its accumulator in the current segment
+      for (int i = 0; i < n_units; ++i) {
+        // A segment is the CTA's run of units of one tile.
+        const bool first = (kMulti ? x.pos == 0 : i == 0) || (x.kb == 0);
+        const bool last = (kMulti ? x.left == 1 : i + 1 == n_units) || (x.kb + 1 == x.KB);
+        if (first) {
+          if (!wait(&B.acc_empty[accb], accph ^ 1u)) break;
+          tc_fence_after();
+          started = false;
+        }
+        if (i % NISS == k) {
+          // W12: the decoders waited for the stage's copies before arriving on
+          // a_full, so "decoded" implies "landed" for X as well.
+          if (kW12 ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + uint32_t(accb * NISS + k) * uint32_t(P.Mpad);
+          const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
+          const uint32_t a_tmem = a_tmem0 + uint32_t(s * kAColsPerBuf);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t koff = uint64_t(((uint32_t(kk >> 2) * xbox) + uint32_t(kk & 3) * 32u) >> 4);
+            const uint64_t bdesc = bdesc0 + soff16 + koff;
+            const uint32_t acc = (started || kk > 0) ? 1u : 0u;
+            if (kW12) {
+              mma_bf16_ts(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
+            } else {
+              const uint64_t aoff = uint64_t((uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u) >> 4);
+              mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
+            }
+          }
+          started = true;
+          tc_commit(&B.empty[s]);  // frees the smem stage and its TMEM A buffer
+        }
+        if (last) {
+          tc_commit(&B.acc_full[accb]);  // every issuer arrives once per segment
+          if (++accb == NACC) {
+            accb = 0;
+            accph ^= 1u;
+          }
+        }
+        if (kMulti) {
+          cur_next(P, c, x);
+        } else if (++x.kb == x.KB) {
+          x.kb = 0;
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      // Make sure no MMA is in flight before TMEM is released.
+      tc_commit(B.drain);
+      mbar_wait(B.drain, 0, lim);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------- exception metadata (W12)
+    if (kW12 && !single) {
+      // Several problems: per unit i of the CTA's sequence, the start (soff)
+      // and end (sent) of its exception entries in its problem's CSR; the
+      // decoders read the entries themselves. Loads go 8 per lane at a time.
+      uint32_t* lo = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
+      uint32_t* hi = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
+      uint8_t* uprob = smem + plan.uprob_off;
+      const int64_t ub0 = unit_begin(c, P.phase_units[0], G);
+      const int n0 = int(unit_begin(c + 1, P.phase_units[0], G) - ub0);
+      const int64_t ub1 = P.nphase > 1 ? unit_begin(c, P.phase_units[1], G) : 0;
+      bool bad = false;
+      for (int i0 = 0; i0 < n_units; i0 += 32 * 8) {
+        uint32_t va[8], vb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + lane + 32 * j;
+          if (i < n_units) {
+            const int f = i < n0 ? 0 : 1;
+            const int64_t u = f == 0 ? ub0 + i : ub1 + (i - n0);
+            const int p = prob_of(P, f, u);
+            const int64_t loc = u - P.pr[p].unit0;
+            va[j] = P.pr[p].exc_off[loc];
+            vb[j] = P.pr[p].exc_off[loc + 1];
+            uprob[i] = uint8_t(p);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + lane + 32 * j;
+          if (i < n_units) {
+            lo[i] = va[j];
+            hi[i] = vb[j];
+            bad |= vb[j] < va[j];
+          }
+        }
+      }
+      bad = __any_sync(0xFFFFFFFFu, bad);
+      __syncwarp();
+      if (lane == 0) {
+        if (bad) set_status(P.status, W12_ERR_CORRUPT);
+        *ent_in_smem = 0;
+        *ent_base = 0;
+        *ent_end = 0xFFFFFFFFu;
+        mbar_arrive(B.exc_ready);
+      }
+    } else if (kW12) {
+      uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
+      uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
+      const int64_t ub = unit_begin(c, P.phase_units[0], G);
+      const uint32_t* exc_off = P.pr[0].exc_off;
+      const uint32_t* exc_ent = P.pr[0].exc_ent;
+      // Every load of a batch is issued before the batch's first store, so the
+      // window costs one memory round trip per batch rather than one per 32
+      // values: the decoders cannot start before this warp arrives.
+      const int nwin = n_units + 1;  // host guarantees nwin <= kOffCap
+      {
+        uint32_t v[kOffCap / 32];
+#pragma unroll
+        for (int j = 0; j < kOffCap / 32; ++j)
+          if (lane + 32 * j < nwin) v[j] = exc_off[ub + lane + 32 * j];
+#pragma unroll
+        for (int j = 0; j < kOffCap / 32; ++j)
+          if (lane + 32 * j < nwin) soff[lane + 32 * j] = v[j];
+      }
+      __syncwarp();
+      const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
+      bool bad = e1 < e0 || int64_t(e1) > P.pr[0].n_exc;
+      const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
+      if (fits) {
+        constexpr int kBatch = 16;  // entries per lane in flight
+        const uint32_t n = e1 - e0;
+        for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
+          uint32_t v[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            if (b0 + lane + 32 * j < n) v[j] = exc_ent[e0 + b0 + lane + 32 * j];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            if (b0 + lane + 32 * j < n) sent[b0 + lane + 32 * j] = v[j];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (bad) set_status(P.status, W12_ERR_CORRUPT);
+        *ent_in_smem = fits ? 1 : 0;
+        *ent_base = e0;
+        *ent_end = bad ? e0 : e1;
+        mbar_arrive(B.exc_ready);
+      }
+    }
+  } else if (kW12 && warp >= 4 && warp < 4 + C::kDecWarps) {
+    // --------------------------------------------------------------- decode
+    const int dw = warp - 4;
+    const int q = warp & 3;          // TMEM lane quarter of this warp
+    const int grp = (dw >> 2) / kDecSplit;  // decode group: units grp, grp + kDecGroups, ...
+    const int h = (dw >> 2) % kDecSplit;    // slice of the unit row (kChunksPerThread chunks of 32 values)
+    const int row = q * 32 + lane;   // W row within the unit
+    const uint32_t tm_lane = uint32_t(q * 32) << 16;
+    const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
+    const uint32_t* sent = reinterpret_cast<const uint32_t*>(smem + plan.sent_off);
+    bool ok = wait(B.exc_ready, 0);
+    const bool in_smem = ok && *ent_in_smem;
+    const uint32_t e_base = *ent_base;
+    const uint32_t e_end = *ent_end;
+
+    // Exceptions of unit i that fall in this warp's rows: the lane-held entry
+    // (first 32 of the unit) and one ballot mask per 32-value chunk. Prepared
+    // one unit ahead so this bookkeeping overlaps the previous unit's stores.
+    struct Exc {
+      uint32_t o0, o1, ent, mask[kChunksPerThread];
+    };
+    const uint8_t* uprob = smem + plan.uprob_off;
+    auto prep = [&](int i, Exc& x) {
+      const ProbParams& pp = P.pr[single ? 0 : uprob[i]];
+      x.o0 = soff[i];
+      x.o1 = single ? soff[i + 1] : sent[i];
+      if (x.o1 < x.o0 || int64_t(x.o1) > pp.n_exc || x.o0 < e_base || x.o1 > e_end) {
+        if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
+        x.o1 = x.o0;
+      }
+      const uint32_t nex = x.o1 - x.o0;
+      x.ent = kInvalidEnt;
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc) x.mask[cc] = 0;
+      if (nex > 0) {
+        if (uint32_t(lane) < nex) x.ent = in_smem ? sent[x.o0 - e_base + lane] : __ldg(pp.exc_ent + x.o0 + lane);
+        const bool mine = x.ent != kInvalidEnt && ((x.ent >> 28) & 3u) == uint32_t(q);
+        const uint32_t ch = (x.ent >> 21) & 3u;
+#pragma unroll
+        for (int cc = 0; cc < kChunksPerThread; ++cc)
+          x.mask[cc] = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(h * kChunksPerThread + cc));
+      }
+    };
+    Exc cur;
+    if (ok && grp < n_units) prep(grp, cur);
+
+    int s = 0;
+    uint32_t ph = 0;
+    for (int k = 0; k < grp; ++k)
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    for (int i = grp; i < n_units && ok; i += kDecGroups) {
+      // Stage s's copies can only have landed after the MMA that last read
+      // its TMEM A buffer committed, so the buffer is free once this returns.
+      if (!wait(&B.full[s], ph)) break;
+      tc_fence_after();
+      const uint8_t* st = smem + s * plan.stage_bytes;
+      const uint8_t* pl = st + row * 64;
+      const uint32_t swz = uint32_t(row >> 1) & 3u;
+      uint4 a[kChunksPerThread], b[kChunksPerThread], g[kChunksPerThread];
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc) {
+        const uint32_t off = ((uint32_t(h * kChunksPerThread + cc) ^ swz) << 4);
+        a[cc] = *reinterpret_cast<const uint4*>(pl + off);
+        b[cc] = *reinterpret_cast<const uint4*>(pl + 8192 + off);
+        g[cc] = *reinterpret_cast<const uint4*>(pl + 16384 + off);
+      }
+      const uint32_t eb = st[plan.eb_off + row];
+      const uint32_t E2 = (eb << 7) * 0x00010001u;
+
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc) {
+        const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
+        uint32_t w[16];
+        decode8(a[cc].x, b[cc].x, g[cc].x, E2, w + 0);
+        decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
+        decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
+        decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
+        uint32_t mk = cur.mask[cc];
+        while (mk) {
+          const int src = __ffs(mk) - 1;
+          mk &= mk - 1;
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
+          if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+        }
+        if (cur.o1 - cur.o0 > 32) {
+          // Rare: more than 32 exceptions in the unit; walk the rest in batches.
+          for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
+            uint32_t e2 = kInvalidEnt;
+            if (bst + lane < cur.o1)
+              e2 = in_smem ? sent[bst - e_base + lane] : __ldg(P.pr[single ? 0 : uprob[i]].exc_ent + bst + lane);
+            const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
+            uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
+            while (mk2) {
+              const int src = __ffs(mk2) - 1;
+              mk2 &= mk2 - 1;
+              const uint32_t e = __shfl_sync(0xFFFFFFFFu, e2, src);
+              if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+            }
+          }
+        }
+        tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
+      }
+      if (i + kDecGroups < n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&B.a_full[s]);
+      for (int k = 0; k < kDecGroups; ++k)
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+    }
+  } else if (warp >= C::kEpiWarp0) {
+    // ------------------------------------------------------------- epilogue
+    const int ew = warp & 3;            // TMEM lane quarter
+    const int row = ew * 32 + lane;
+    const uint32_t tm_lane = uint32_t(ew * 32) << 16;
+    const int et = threadIdx.x - C::kEpiWarp0 * 32;  // 0..127
+    float* scratch = reinterpret_cast<float*>(smem + plan.scratch_off);
+    float* red_v = reinterpret_cast<float*>(smem + plan.red_off);
+    int32_t* red_i = reinterpret_cast<int32_t*>(smem + plan.red_off + 4 * 16 * 4);
+    const int nchunks = P.Mpad / 16;
+
+    // Tile argmax over a 16-column chunk: v[r] = logit of vocab row `row`
+    // for token mc*16 + r. Lowest vocab index wins ties.
+    auto argmax_chunk = [&](const float (&v)[16], int t, int mc) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) scratch[r * kScratchStride + row] = v[r];
+      named_bar_sync(kEpiBar, 128);
+      if (lane < 16) {
+        const float* col = scratch + lane * kScratchStride + ew * 32;
+        float best = col[0];
+        int bi = 0;
+        for (int k = 1; k < 32; ++k) {
+          const float x = col[k];
+          if (x > best) {
+            best = x;
+            bi = k;
+          }
+        }
+        red_v[ew * 16 + lane] = best;
+        red_i[ew * 16 + lane] = ew * 32 + bi;
+      }
+      named_bar_sync(kEpiBar, 128);
+      if (ew == 0 && lane < 16) {
+        float best = red_v[lane];
+        int bi = red_i[lane];
+        for (int w2 = 1; w2 < 4; ++w2) {
+          const float x = red_v[w2 * 16 + lane];
+          if (x > best) {
+            best = x;
+            bi = red_i[w2 * 16 + lane];
+          }
+        }
+        const int m = mc * 16 + lane;
+        P.amax_val[int64_t(t) * P.Mpad + m] = best;
+        P.amax_idx[int64_t(t) * P.Mpad + m] = t * 128 + bi;
+      }
+      named_bar_sync(kEpiBar, 128);
+    };
+    auto store_chunk = [&](const float (&v)[16], int pi, int t, int mc) {
+      float* Y = P.pr[pi].Y;
+      const int64_t N = P.pr[pi].N;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int m = mc * 16 + r;
+        if (m < P.M) Y[int64_t(m) * N + int64_t(t) * 128 + row] = v[r];
+      }
+    };
+
+    grid_dep_wait();
+    const int32_t epoch = kMulti && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
+    // Tile t of the SwiGLU source problem is complete in Y: the CTA that
+    // completes the second tile of block j writes act block j and publishes it.
+    auto glu_tile_done = [&](int t) {
+      const ProbParams& pg = P.pr[P.glu_from];
+      const int j = t < P.glu_blocks ? t : t - P.glu_blocks;
+      named_bar_sync(kEpiBar, 128);  // every thread's Y stores of the tile are issued
+      if (et == 0) {
+        __threadfence();
+        const int old = atomic_add_acq_rel_gpu(P.glu_cnt + j, 1);
+        *glu_flag = old == 1 ? 1 : 0;
+      }
+      named_bar_sync(kEpiBar, 128);
+      if (*glu_flag) {
+        const int64_t Nh = pg.N / 2;
+        const int64_t col = int64_t(j) * 128 + et;
+        for (int m = 0; m < P.M; ++m) {
+          const float g = __ldcg(pg.Y + int64_t(m) * pg.N + col);
+          const float u = __ldcg(pg.Y + int64_t(m) * pg.N + Nh + col);
+          P.act[int64_t(m) * Nh + col] = f32_to_bf16_rne(g / (1.0f + expf(-g)) * u);
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        named_bar_sync(kEpiBar, 128);
+        if (et == 0) {
+          P.glu_cnt[j] = 0;
+          st_release_gpu(P.glu_ready + j, epoch + 1);
+        }
+      }
+    };
+    int accb = 0;
+    uint32_t accph = 0;
+    int iseq = 0;  // index of the segment's first unit in the CTA's sequence
+    // Walk the CTA's segments (its runs of units of one tile) phase by phase;
+    // only (phase, next unit, end of range) is carried between segments.
+    int fn = 0;
+    int64_t un = unit_begin(c, P.phase_units[0], G), uen = unit_begin(c + 1, P.phase_units[0], G);
+    bool more = un < uen;
+    if constexpr (kMulti) {
+      for (fn = 1; fn < P.nphase && !more; ++fn) {
+        un = unit_begin(c, P.phase_units[fn], G);
+        uen = unit_begin(c + 1, P.phase_units[fn], G);
+        more = un < uen;
+      }
+      --fn;
+      if (!more) fn = 0;
+    }
+    const int64_t ub0 = un;
+    while (more) {
+      const int f = kMulti ? fn : 0;
+      const int64_t Uf = P.phase_units[f];
+      const int64_t ub = kMulti ? unit_begin(c, Uf, G) : ub0, ue = uen;
+      const int pi = kMulti ? prob_of(P, f, un) : 0;
+      const int KBp = P.pr[pi].KB;
+      const int64_t u0p = kMulti ? P.pr[pi].unit0 : 0;
+      const int t = int((un - u0p) / KBp);
+      const int64_t tile_u0 = u0p + int64_t(t) * KBp;
+      const int64_t seg_begin = un;
+      const int64_t seg_end = tile_u0 + KBp < ue ? tile_u0 + KBp : ue;
+      un = seg_end;
+      more = un < uen;
+      if constexpr (kMulti) {
+        if (!more) {
+          for (++fn; fn < P.nphase && !more; ++fn) {
+            un = unit_begin(c, P.phase_units[fn], G);
+            uen = unit_begin(c + 1, P.phase_units[fn], G);
+            more = un < uen;
+          }
+          --fn;
+        }
+      }
+      const bool final_seg = !more;  // the CTA's last segment: the ring is idle once it is accumulated
+      const int ia = kMulti ? iseq : int(seg_begin - ub0), nseg = int(seg_end - seg_begin);
+      if (kMulti) iseq += nseg;
+      const int gt = (kMulti ? P.pr[pi].tile0 : 0) + t;   // launch-wide tile number (counters)
+      const int cur = accb;
+      const uint32_t cur_ph = accph;
+      if (++accb == NACC) {
+        accb = 0;
+        accph ^= 1u;
+      }
+      const int c_first = unit_owner(tile_u0, Uf, G);
+      const int c_last = unit_owner(tile_u0 + KBp - 1, Uf, G);
+      const int nsplit = c_last - c_first + 1;
+      // Partial slots are laid out [chunk][row][16] floats: each thread's 16
+      // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
+      // CTA cc has two slots per phase: its first piece in the phase, and
+      // its last.
+      auto slot_of = [&](int cc) {
+        const int64_t u0 = unit_begin(cc, Uf, G);
+        return 2 * (cc * P.nphase + f) + ((u0 >= tile_u0 && u0 < tile_u0 + KBp) ? 0 : 1);
+      };
+      // The CTA's final segment ends the kernel. When its tile has one other
+      // piece and that piece is already done (it was the first piece its CTA
+      // processed, so it usually is), its partial is fetched while this
+      // segment's last units are still in flight, and the tile is finished
+      // here without writing a partial or taking a counter round trip.
+      const int me = c - c_first;
+      int pref = 0;
+      if (final_seg && nsplit == 2 && nchunks == 1) {
+        if (et == 0) {
+          int done = 0;
+          const uint64_t t0 = globaltimer_ns();
+          for (;;) {
+            if (ld_acquire_gpu(&P.counters[gt]) == nsplit - 1) {
+              done = 1;
+              break;
+            }
+            if (mbar_try_wait(&B.acc_full[cur], cur_ph)) {
+              done = ld_acquire_gpu(&P.counters[gt]) == nsplit - 1;
+              break;
+            }
+            if (*abort_flag || globaltimer_ns() - t0 > lim) break;  // the wait below reports it
+          }
+          *pref_flag = done;
+        }
+        named_bar_sync(kEpiBar, 128);
+        pref = *pref_flag;
+        if (pref) {
+          const float4* s0 =
+              reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + 1 - me)) * P.Mpad * 128) + size_t(row) * 4;
+          // Parked in this thread's own column of the transpose buffer (free
+          // until this segment's epilogue writes the same places).
+          float* sc = scratch + row;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float4 f = __ldcg(s0 + x);
+            sc[(4 * x) * kScratchStride] = f.x;
+            sc[(4 * x + 1) * kScratchStride] = f.y;
+            sc[(4 * x + 2) * kScratchStride] = f.z;
+            sc[(4 * x + 3) * kScratchStride] = f.w;
+          }
+        }
+      }
+      if (!wait(&B.acc_full[cur], cur_ph)) break;
+      tc_fence_after();
+      // Issuer k wrote accumulator (cur, k) iff the segment holds a unit i
+      // (counted from the CTA's first unit) with i % issuers == k.
+      const uint32_t d_tmem = tmem_base + tm_lane + uint32_t(cur * NISS) * uint32_t(P.Mpad);
+      auto load_acc = [&](int mc, float (&v)[16]) {
+        bool have = false;
+        for (int kq = 0; kq < NISS; ++kq) {
+          if (!(nseg >= NISS || (ia % NISS) == kq)) continue;
+          uint32_t r[16];
+          tmem_ld16(d_tmem + uint32_t(kq * P.Mpad + mc * 16), r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] = have ? v[x] + __uint_as_float(r[x]) : __uint_as_float(r[x]);
+          have = true;
+        }
+      };
+      if (nsplit == 1 || pref) {
+        for (int mc = 0; mc < nchunks; ++mc) {
+          float v[16];
+          load_acc(mc, v);
+          if (pref) {
+            // Same slot-order sum as the fixup below (own piece at position me).
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const float o = scratch[x * kScratchStride + row];
+              float acc = 0.0f;
+              acc += me == 0 ? v[x] : o;
+              acc += me == 0 ? o : v[x];
+              v[x] = acc;
+            }
+          }
+          if (kArgmax) argmax_chunk(v, t, mc);
+          else store_chunk(v, pi, t, mc);
+        }
+        tc_fence_before();
+        mbar_arrive(&B.acc_empty[cur]);
+        if (pref && et == 0) P.counters[gt] = 0;  // every other contributor has already counted
+        if (kMulti && pi == P.glu_from) glu_tile_done(t);
+      } else {
+        // In the final segment every stage of the ring has been consumed (the
+        // segment's MMAs completed), so the other pieces' partials can be
+        // brought into it with bulk copies, as many chunks per round trip as
+        // fit. This CTA's own piece is then taken from TMEM. If every other
+        // piece is already counted, the tile is finished here without writing
+        // this piece or taking the counter round trip.
+        const uint32_t ring_bytes = uint32_t(S) * plan.stage_bytes;
+        const int cb_max = int(ring_bytes / (uint32_t(nsplit - 1) * 8192u));  // chunks per gather batch
+        const bool gather = final_seg && cb_max >= 1;
+        int fast = 0;
+        if (gather) {
+          if (et == 0) *fast_flag = ld_acquire_gpu(&P.counters[gt]) == nsplit - 1;
+          named_bar_sync(kEpiBar, 128);
+          fast = *fast_flag;
+        }
+        if (!fast) {
+          const int slot = 2 * (c * P.nphase + f) + (seg_begin == ub ? 0 : 1);
+          float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
+          for (int mc = 0; mc < nchunks; ++mc) {
+            float v[16];
+            load_acc(mc, v);
+            float4* dst = my + (size_t(mc) * 128 + row) * 4;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&B.acc_empty[cur]);
+        if (!fast) {
+          // The barrier orders every epilogue thread's partial stores before
+          // the single release-acquire increment; the last contributor's
+          // readers are ordered after that increment by the second barrier.
+          named_bar_sync(kEpiBar, 128);
+          if (et == 0) {
+            const int old = atomic_add_acq_rel_gpu(&P.counters[gt], 1);
+            *last_flag = (old == nsplit - 1) ? 1 : 0;
+          }
+          named_bar_sync(kEpiBar, 128);
+        }
+        const bool last = fast || *last_flag != 0;
+        uint32_t gph = 0;
+        for (int mc0 = 0; last && mc0 < nchunks;) {
+          const int nb = gather ? (nchunks - mc0 < cb_max ? nchunks - mc0 : cb_max) : nchunks;
+          if (gather) {
+            if (mc0 > 0) named_bar_sync(kEpiBar, 128);  // the previous batch has been read
+            if (et == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              mbar_arrive_expect_tx(B.gather, uint32_t(nsplit - 1) * uint32_t(nb) * 8192u);
+              int j = 0;
+              for (int sp = 0; sp < nsplit; ++sp) {
+                if (sp == me) continue;
+                const float* src = P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128;
+                for (int b2 = 0; b2 < nb; ++b2)
+                  bulk_load(smem + uint32_t(j * nb + b2) * 8192u, src + size_t(mc0 + b2) * 128 * 16, 8192u,
+                            B.gather);
+                ++j;
+              }
+            }
+            if (!wait(B.gather, gph)) break;
+            gph ^= 1u;
+          }
+          for (int b2 = 0; b2 < nb; ++b2) {
+            const int mc = mc0 + b2;
+            float r[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = 0.0f;
+            // Slot order, so the sum does not depend on which CTA finishes
+            // the tile or by which path.
+            for (int sp = 0, j = 0; sp < nsplit; ++sp) {
+              float q[16];
+              if (gather && sp == me) {
+                load_acc(mc, q);
+              } else {
+                const float4* src =
+                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nb + b2) * 8192u) + row * 4
+                           : reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128) +
+                                 (size_t(mc) * 128 + row) * 4;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                  const float4 f = gather ? src[x] : __ldcg(src + x);
+                  q[4 * x] = f.x, q[4 * x + 1] = f.y, q[4 * x + 2] = f.z, q[4 * x + 3] = f.w;
+                }
+              }
+#pragma unroll
+              for (int x = 0; x < 16; ++x) r[x] += q[x];
+            }
+            if (kArgmax) argmax_chunk(r, t, mc);
+            else store_chunk(r, pi, t, mc);
+          }
+          mc0 += nb;
+        }
+        if (last && et == 0) P.counters[gt] = 0;
+        named_bar_sync(kEpiBar, 128);
+        if (kMulti && last && pi == P.glu_from) glu_tile_done(t);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (kMulti && P.glu_to >= 0 && threadIdx.x == 0) {
+    // The last CTA to finish moves the launch epoch on, so the next launch
+    // on this workspace tells its ready flags from this one's.
+    const int32_t e = *reinterpret_cast<volatile int32_t*>(P.epoch);
+    if (atomic_add_acq_rel_gpu(P.epoch + 1, 1) == G - 1) {
+      P.epoch[1] = 0;
+      st_release_gpu(P.epoch, e + 1);
+    }
+  }
+}
+
+template <bool kW12, bool kArgmax, bool kMulti>
+static int launch_impl(int Mpad, GemmParams& P, const GemmMaps& TM, cudaStream_t stream) {
+  // Deepest ring that fits next to the fixed carve-up.
+  const int smem_max = 232448;
+  const int nacc = Mpad <= 128 ? 2 : 1;
+  // Two MMA issuers when their accumulators fit in half of TMEM (Mpad <= 64).
+  const int issuers = nacc * 2 * Mpad <= 256 ? 2 : 1;
+  const int a_col0 = (nacc * issuers * Mpad + 63) & ~63;
+  int stages = kMaxStages;
+  while (stages > 2 && (smem_plan<kW12>(Mpad, stages).total > uint32_t(smem_max) ||
+                        (kW12 && a_col0 + stages * kAColsPerBuf > 512)))
+    --stages;
+  if (kW12 && a_col0 + stages * kAColsPerBuf > 512) return W12_ERR_UNSUPPORTED;
+  const SmemPlan plan = smem_plan<kW12>(Mpad, stages);
+  if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
+  P.stages = stages;
+  P.issuers = issuers;
+  auto kern = gemm_kernel<kW12, kArgmax, kMulti>;
+  static bool attr_set[64] = {false};  // per device; setting it twice is harmless
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
+      return W12_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(P.grid));
+  cfg.blockDim = dim3(unsigned(Cfg<kW12>::kThreads));
+  cfg.dynamicSmemBytes = plan.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, TM, P));
+}
+
+// Tensor maps of one problem: planes (or the bf16 matrix) and X.
+static int encode_problem(bool w12_mode, const uint16_t* X, int64_t M, int Mpad, const w12_weights* W,
+                          const uint16_t* Wbf16, int64_t N, int64_t K, CUtensorMap* m) {
+  if (!encode_tmap_2d(&m[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(X), uint64_t(K), uint64_t(M),
+                      uint64_t(K) * 2, 64, uint32_t(Mpad), CU_TENSOR_MAP_SWIZZLE_128B))
+    return W12_ERR_CUDA;
+  if (w12_mode) {
+    const uint64_t half = uint64_t(K) / 2;
+    if (!encode_tmap_2d(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p0, half, uint64_t(N), half, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_tmap_2d(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p1, half, uint64_t(N), half, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_tmap_2d(&m[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p2, half, uint64_t(N), half, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_64B))
+      return W12_ERR_CUDA;
+  } else {
+    if (!encode_tmap_2d(&m[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(Wbf16), uint64_t(K),
+                        uint64_t(N), uint64_t(K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      return W12_ERR_CUDA;
+    m[1] = m[0];
+    m[2] = m[0];
+  }
+  return W12_OK;
+}
+
+static int check_weights(const w12_weights* W) {
+  if (!W || !W->p0 || !W->p1 || !W->p2 || !W->ebase || !W->exc_off) return W12_ERR_ARG;
+  if (W->n_exc > 0 && !W->exc_ent) return W12_ERR_ARG;
+  if (!aligned(W->p0, 16) || !aligned(W->p1, 16) || !aligned(W->p2, 16) || !aligned(W->ebase, 16))
+    return W12_ERR_ARG;
+  return W12_OK;
+}
+
+static void set_problem(ProbParams& q, bool w12_mode, const w12_weights* W, int64_t N, int64_t K, float* Y) {
+  q.N = int(N);
+  q.K = int(K);
+  q.KB = int(K / kGroup);
+  q.tiles = int(N / kGroup);
+  q.ebase = w12_mode ? W->ebase : nullptr;
+  q.exc_off = w12_mode ? W->exc_off : nullptr;
+  q.exc_ent = w12_mode ? W->exc_ent : nullptr;
+  q.n_exc = w12_mode ? W->n_exc : 0;
+  q.Y = Y;
+}
+
+// Grouped launch: problems in launch order (phase 0: every problem but the
+// SwiGLU target; phase 1: the target), with the workspace carve-up.
+struct Grouped {
+  int n, order[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks;
+  int64_t N[kMaxProb], K[kMaxProb], phase_units[2];
+  size_t counters, glu_cnt, glu_ready, epoch, parts, total;
+};
+
+static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link, bool w12_mode,
+                        Grouped* g) {
+  if (!probs || n < 1 || n > kMaxProb) return W12_ERR_ARG;
+  if (M < 1 || M > kMaxM) return W12_ERR_SHAPE;
+  memset(g, 0, sizeof(*g));
+  g->n = n;
+  g->glu_from = g->glu_to = -1;
+  for (int i = 0; i < n; ++i) {
+    const w12_weights* W = probs[i].W;
+    g->N[i] = w12_mode ? (W ? W->N : 0) : probs[i].N;
+    g->K[i] = w12_mode ? (W ? W->K : 0) : probs[i].K;
+    GemmShape sh;
+    const int st = gemm_shape(M, g->N[i], g->K[i], &sh);
+    if (st) return st;
+    g->Mpad = sh.Mpad;
+  }
+  int to = -1;
+  if (link) {
+    if (link->from < 0 || link->from >= n || link->to < 0 || link->to >= n || link->from == link->to)
+      return W12_ERR_ARG;
+    if (g->N[link->from] % (2 * kGroup) || g->K[link->to] != g->N[link->from] / 2) return W12_ERR_SHAPE;
+    to = link->to;
+  }
+  int k = 0;
+  for (int i = 0; i < n; ++i)
+    if (i != to) g->order[k++] = i;
+  if (to >= 0) g->order[k++] = to;
+  g->nphase = to >= 0 ? 2 : 1;
+  int64_t maxu = 0;
+  for (int j = 0; j < n; ++j) {
+    const int i = g->order[j];
+    const int f = (i == to) ? 1 : 0;
+    g->phase_units[f] += (g->N[i] / kGroup) * (g->K[i] / kGroup);
+    g->tiles += int(g->N[i] / kGroup);
+  }
+  for (int f = 0; f < g->nphase; ++f) maxu = g->phase_units[f] > maxu ? g->phase_units[f] : maxu;
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 256;  // sizing without a device: an upper bound
+  g->grid = int(maxu < sms ? maxu : sms);
+  int64_t per_cta = 0;
+  for (int f = 0; f < g->nphase; ++f) per_cta += (g->phase_units[f] + g->grid - 1) / g->grid;
+  if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
+  if (to >= 0) {
+    for (int j = 0; j < n; ++j)
+      if (g->order[j] == link->from) g->glu_from = j;
+    g->glu_to = n - 1;
+    g->glu_blocks = int(g->N[link->from] / (2 * kGroup));
+  }
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  g->counters = take(sizeof(int32_t) * size_t(g->tiles));
+  g->glu_cnt = take(sizeof(int32_t) * size_t(g->glu_blocks > 0 ? g->glu_blocks : 1));
+  g->glu_ready = take(sizeof(int32_t) * size_t(g->glu_blocks > 0 ? g->glu_blocks : 1));
+  g->epoch = take(sizeof(int32_t) * 2);
+  g->parts = take(sizeof(float) * size_t(2) * g->nphase * g->grid * g->Mpad * kGroup);
+  g->total = off;
+  return W12_OK;
+}
+
+static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_t M, const w12_swiglu* link,
+                          void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  Grouped g;
+  int st = plan_grouped(probs, n, M, link, w12_mode, &g);
+  if (st) return st;
+  if (!ws || !aligned(ws, 16)) return W12_ERR_ARG;
+  if (ws_bytes < g.total) return W12_ERR_WORKSPACE;
+  if (link && (!link->act || !aligned(link->act, 16) || !probs[link->from].Y)) return W12_ERR_ARG;
+  for (int i = 0; i < n; ++i) {
+    const bool is_to = link && i == link->to;
+    if (!probs[i].Y) return W12_ERR_ARG;
+    if (!is_to && (!probs[i].X || !aligned(probs[i].X, 16))) return W12_ERR_ARG;
+    if (w12_mode) {
+      if ((st = check_weights(probs[i].W))) return st;
+    } else if (!probs[i].Wbf16 || !aligned(probs[i].Wbf16, 16)) {
+      return W12_ERR_ARG;
+    }
+  }
+  if (!device_supported()) return W12_ERR_UNSUPPORTED;
+
+  GemmParams P{};
+  P.M = int(M);
+  P.Mpad = g.Mpad;
+  P.grid = g.grid;
+  P.nprob = n;
+  P.nphase = g.nphase;
+  P.phase_units[0] = g.phase_units[0];
+  P.phase_units[1] = g.phase_units[1];
+  P.pfirst[0] = 0;
+  P.pfirst[1] = g.nphase > 1 ? n - 1 : n;
+  GemmMaps TM;
+  memset(&TM, 0, sizeof(TM));
+  int64_t unit0[2] = {0, 0};
+  int tile0 = 0;
+  for (int j = 0; j < n; ++j) {
+    const int i = g.order[j];
+    const bool is_to = link && i == link->to;
+    ProbParams& q = P.pr[j];
+    set_problem(q, w12_mode, probs[i].W, g.N[i], g.K[i], probs[i].Y);
+    q.phase = is_to ? 1 : 0;
+    q.unit0 = unit0[q.phase];
+    unit0[q.phase] += int64_t(q.tiles) * q.KB;
+    q.tile0 = tile0;
+    tile0 += q.tiles;
+    const uint16_t* X = is_to ? link->act : probs[i].X;
+    if ((st = encode_problem(w12_mode, X, M, g.Mpad, probs[i].W, probs[i].Wbf16, g.N[i], g.K[i], TM.m[j])))
+      return st;
+  }
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  P.counters = reinterpret_cast<int32_t*>(wsb + g.counters);
+  P.parts = reinterpret_cast<float*>(wsb + g.parts);
+  P.glu_from = g.glu_from;
+  P.glu_to = g.glu_to;
+  P.glu_blocks = g.glu_blocks;
+  P.act = link ? link->act : nullptr;
+  P.glu_cnt = reinterpret_cast<int32_t*>(wsb + g.glu_cnt);
+  P.glu_ready = reinterpret_cast<int32_t*>(wsb + g.glu_ready);
+  P.epoch = reinterpret_cast<int32_t*>(wsb + g.epoch);
+  P.status = dev_status;
+  P.limit_ns = wait_limit_ns();
+  return w12_mode ? launch_impl<true, false, true>(g.Mpad, P, TM, stream)
+                  : launch_impl<false, false, true>(g.Mpad, P, TM, stream);
+}
+
+}  // namespace grouped_impl
+}  // namespace w12
+
+using namespace w12::grouped_impl;
+
+extern "C" {
+
+size_t w12_gemm_grouped_ws_bytes(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link) {
+  Grouped g;
+  bool w12_mode = probs && n > 0 && probs[0].W;
+  return plan_grouped(probs, n, M, link, w12_mode, &g) == W12_OK ? g.total : 0;
+}
+
+int w12_gemm_grouped(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link, void* ws, size_t ws_bytes,
+                     int32_t* dev_status, void* stream) {
+  return launch_grouped(true, probs, n, M, link, ws, ws_bytes, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int w12_gemm_grouped_bf16_ref(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link, void* ws,
+                              size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return launch_grouped(false, probs, n, M, link, ws, ws_bytes, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -11,6 +11,7 @@ namespace w12 {
 
 constexpr int kGroup = 128;            // K elements per exponent group / exception block column
 constexpr int kMaxM = 256;             // verified rows per call
+constexpr int kMaxProb = 4;            // GEMMs in one grouped launch
 constexpr int kOffCap = 1024;          // exception offsets staged in shared memory per CTA
 constexpr int kEntCap = 2048;          // exception entries staged in shared memory per CTA
 constexpr int kTreeMax = 256;          // nodes per draft tree

@@ -24,7 +24,8 @@ EXPORTS = [
     "w12_status_string", "w12_version", "w12_pack_ws_bytes", "w12_pack_query", "w12_pack", "w12_unpack",
     "w12_gemm_ws_bytes", "w12_gemm", "w12_gemm_bf16_ref", "w12_verify_ws_bytes", "w12_verify_greedy",
     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
-    "w12_set_wait_limit_us", "w12_set_overlap", "w12_gemm_noalloc",
+    "w12_set_wait_limit_us", "w12_set_overlap", "w12_gemm_noalloc", "w12_gemm_grouped_ws_bytes",
+    "w12_gemm_grouped", "w12_gemm_grouped_bf16_ref",
 ]
 
 
@@ -38,6 +39,15 @@ class _Weights(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("p0", ctypes.c_void_p), ("p1", ctypes.c_void_p),
                 ("p2", ctypes.c_void_p), ("ebase", ctypes.c_void_p), ("exc_off", ctypes.c_void_p),
                 ("exc_ent", ctypes.c_void_p), ("n_exc", ctypes.c_int64)]
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("W", ctypes.c_void_p), ("Wbf16", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("Y", ctypes.c_void_p)]
+
+
+class _Swiglu(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_int), ("dst", ctypes.c_int), ("act", ctypes.c_void_p)]
 
 
 class _Sizes(ctypes.Structure):
@@ -78,6 +88,10 @@ def lib() -> ctypes.CDLL:
             "w12_set_wait_limit_us": (i32, [i64]),
             "w12_set_overlap": (i32, [i32]),
             "w12_gemm_noalloc": (i32, [vp, i64, ctypes.POINTER(_Weights), vp, vp, vp]),
+            "w12_gemm_grouped_ws_bytes": (sz, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu)]),
+            "w12_gemm_grouped": (i32, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu), vp, sz, vp, vp]),
+            "w12_gemm_grouped_bf16_ref": (i32, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu), vp, sz,
+                                                vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -216,6 +230,67 @@ def gemm_noalloc(X: torch.Tensor, w: W12Weights, Y: torch.Tensor, status: torch.
     _check(lib().w12_gemm_noalloc(X.data_ptr(), X.shape[0], ctypes.byref(w.struct()), Y.data_ptr(), _ptr(status),
                                   _stream(stream)), "w12_gemm_noalloc")
     return Y
+
+
+class Grouped:
+    """Several verify GEMMs of one layer in one launch (w12_gemm_grouped).
+
+    items: list of (X, W, Y) with X a bf16 [M, K] tensor (None for the SwiGLU
+    target), W a W12Weights (or a bf16 [N, K] tensor with bf16=True) and Y an
+    fp32 [M, N] tensor (allocated if None). swiglu=(src, dst) makes item dst
+    take act = bf16(silu(gate) * up) of item src's output as its X; act is
+    allocated here ([M, N_src/2] bf16). The argument structs and workspace
+    are built once; run() enqueues the launch on the current stream.
+    """
+
+    def __init__(self, items, M: int, swiglu=None, bf16: bool = False, status: torch.Tensor | None = None):
+        self.M, self.bf16, self.status = M, bf16, status
+        self.items = []
+        probs = (_Problem * len(items))()
+        dev = None
+        for i, (X, W, Y) in enumerate(items):
+            if bf16:
+                N, K = W.shape
+                W = _bits16(W)
+            else:
+                N, K = W.N, W.K
+            if X is not None:
+                X = _bits16(X)
+                dev = X.device
+            dev = dev or (W.device if bf16 else W.p0.device)
+            if Y is None:
+                Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            self.items.append((X, W, Y))
+            probs[i].X = None if X is None else X.data_ptr()
+            probs[i].W = None if bf16 else ctypes.cast(ctypes.pointer(W.struct()), ctypes.c_void_p).value
+            probs[i].Wbf16 = W.data_ptr() if bf16 else None
+            probs[i].N, probs[i].K = N, K
+            probs[i].Y = Y.data_ptr()
+        self.act = None
+        self._link = None
+        if swiglu is not None:
+            src, dst = swiglu
+            Nsrc = self.items[src][2].shape[1]
+            self.act = torch.zeros((M, Nsrc // 2), dtype=torch.bfloat16, device=dev)
+            self._link = _Swiglu(src, dst, self.act.data_ptr())
+        self._probs = probs
+        self._n = len(items)
+        link = ctypes.byref(self._link) if self._link is not None else None
+        nbytes = int(lib().w12_gemm_grouped_ws_bytes(probs, self._n, M, link))
+        if nbytes == 0:
+            raise W12Error(1, "w12_gemm_grouped_ws_bytes")
+        self.ws = workspace(nbytes, dev)
+
+    @property
+    def Y(self):
+        return [Y for _, _, Y in self.items]
+
+    def run(self, stream=None):
+        link = ctypes.byref(self._link) if self._link is not None else None
+        f = lib().w12_gemm_grouped_bf16_ref if self.bf16 else lib().w12_gemm_grouped
+        _check(f(self._probs, self._n, self.M, link, self.ws.data_ptr(), self.ws.numel(), _ptr(self.status),
+                 _stream(stream)), "w12_gemm_grouped")
+        return self.Y
 
 
 def gemm_bf16_ref(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None, ws: torch.Tensor | None = None,
