@@ -164,9 +164,9 @@ int w12_gemm_bf16_ref(const uint16_t* X, int64_t M, const uint16_t* W, int64_t N
  * launch: act[m, j] = bf16(silu(Y_from[m, j]) * Y_from[m, N_from/2 + j]),
  * silu(g) = g / (1 + exp(-g)), rounded to nearest even. The pages give no
  * MLP activation; this is the gated SiLU of dense decoder layers, with the
- * gate in the first half of the fused gate/up output. The target's units run
- * after every other problem's (a second phase) and each of its k-blocks
- * starts once that block of act is written.
+ * gate in the first half of the fused gate/up output. The source's units
+ * run first, then the other problems', then the target's; each of the
+ * target's k-blocks starts once that block of act is written.
  *
  * problems: X [M, K] bf16 row-major (16-byte aligned; unused for the link
  * target), weights (W for w12_gemm_grouped; Wbf16 with N, K for the bf16

@@ -5,10 +5,10 @@
 // The verify pass reads every target weight each step (SpecPilot paper
 // digest, summary paragraph); the layer's GEMMs all share M, so their
 // 128x128 units can be split over the SMs as one stream: the launch pays one
-// ramp-up and one tail for the group instead of one per GEMM. Problems whose
-// X is produced inside the launch (the down projection, whose X is the gated
-// activation of the gate/up output) form a second phase: every CTA works
-// through its share of phase 0 and then of phase 1, and each phase-1 k-block
+// ramp-up and one tail for the group instead of one per GEMM. With a SwiGLU
+// link the launch has three phases (the gate/up source; the other problems;
+// the down projection, whose X is the gated activation of the gate/up output)
+// and every CTA works through its share of each in turn; each down k-block
 // waits (bounded) for a per-block ready flag written by the CTA that completes
 // the block's two gate/up tiles. Flags carry a launch epoch, moved on by the
 // last CTA to finish, so one workspace serves consecutive launches.
@@ -47,10 +47,10 @@ constexpr int kScratchStride = 129;   // floats per column in the argmax transpo
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
 
 // One GEMM of a launch. A launch runs up to kMaxProb GEMMs (problems) that
-// share M, in at most two phases: the units of each phase are split evenly
-// over the CTAs (stream-K over the concatenated problems), and every CTA
-// works through its share of phase 0 and then of phase 1. Phase 1 holds the
-// problem whose X is produced inside the launch (the SwiGLU link below).
+// share M, in up to kMaxProb phases: the units of each phase are split evenly
+// over the CTAs (stream-K over the phase's concatenated problems), and every
+// CTA works through its share of each phase in turn. The last phase holds
+// the problem whose X is produced inside the launch (the SwiGLU link below).
 struct ProbParams {
   int N, K, KB, tiles, phase, tile0;  // tile0: first of its tiles in the launch-wide tile numbering
   int64_t unit0;                      // first unit of the problem in its phase's unit numbering
@@ -63,8 +63,8 @@ struct ProbParams {
 
 struct GemmParams {
   int M, Mpad, grid, stages, issuers, nprob, nphase;
-  int pfirst[2];                      // first problem of each phase (problems are ordered by phase)
-  int64_t phase_units[2];
+  int pfirst[kMaxProb];               // first problem of each phase (problems are ordered by phase)
+  int64_t phase_units[kMaxProb];
   ProbParams pr[kMaxProb];
   float* parts;                       // split-K partial slots: 2 per CTA per phase
   int32_t* counters;                  // one per tile of the launch
@@ -104,6 +104,19 @@ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G) {
   return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
 }
 
+// A phase with fewer units than CTAs is shared by its first phase_units CTAs
+// only (one unit each), so that the CTAs holding pieces of one tile are
+// always consecutive; pbegin(c) is the first unit of CTA c in phase f (the
+// phase's unit count for CTAs past the sharing ones).
+__device__ __forceinline__ int phase_ctas(const GemmParams& P, int f) {
+  return P.phase_units[f] < P.grid ? int(P.phase_units[f]) : P.grid;
+}
+
+__device__ __forceinline__ int64_t pbegin(const GemmParams& P, int c, int f) {
+  const int Gf = phase_ctas(P, f);
+  return unit_begin(c < Gf ? c : Gf, P.phase_units[f], Gf);
+}
+
 // Problem of phase f that holds phase unit u.
 __device__ __forceinline__ int prob_of(const GemmParams& P, int f, int64_t u) {
   int p = P.pfirst[f];
@@ -114,8 +127,8 @@ __device__ __forceinline__ int prob_of(const GemmParams& P, int f, int64_t u) {
 // First unit of CTA c at or after phase f; false if it has none.
 __device__ __forceinline__ bool cur_phase(const GemmParams& P, int c, int f, Cur& x) {
   for (; f < P.nphase; ++f) {
-    const int64_t ub = unit_begin(c, P.phase_units[f], P.grid);
-    const int64_t ue = unit_begin(c + 1, P.phase_units[f], P.grid);
+    const int64_t ub = pbegin(P, c, f);
+    const int64_t ue = pbegin(P, c + 1, f);
     if (ub < ue) {
       x.f = f;
       x.p = prob_of(P, f, ub);
@@ -154,7 +167,7 @@ __device__ __forceinline__ bool cur_next(const GemmParams& P, int c, Cur& x) {
 __device__ __forceinline__ int cta_units(const GemmParams& P, int c) {
   int n = 0;
   for (int f = 0; f < P.nphase; ++f)
-    n += int(unit_begin(c + 1, P.phase_units[f], P.grid) - unit_begin(c, P.phase_units[f], P.grid));
+    n += int(pbegin(P, c + 1, f) - pbegin(P, c, f));
   return n;
 }
 
@@ -384,6 +397,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
               gave_up = true;
               break;
             }
+            __nanosleep(100);  // back off: every SM may be polling the same few flags
             okr = ld_acquire_gpu(rdy) == epoch + 1;
           }
           asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -488,9 +502,16 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       uint32_t* lo = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
       uint32_t* hi = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
       uint8_t* uprob = smem + plan.uprob_off;
-      const int64_t ub0 = unit_begin(c, P.phase_units[0], G);
-      const int n0 = int(unit_begin(c + 1, P.phase_units[0], G) - ub0);
-      const int64_t ub1 = P.nphase > 1 ? unit_begin(c, P.phase_units[1], G) : 0;
+      // The CTA's range in each phase: its first unit and where the range
+      // starts in the CTA's sequence.
+      int64_t fb[kMaxProb];
+      int fs[kMaxProb + 1];
+      fs[0] = 0;
+      for (int f = 0; f < kMaxProb; ++f) {
+        const bool on = f < P.nphase;
+        fb[f] = on ? pbegin(P, c, f) : 0;
+        fs[f + 1] = fs[f] + (on ? int(pbegin(P, c + 1, f) - fb[f]) : 0);
+      }
       bool bad = false;
       for (int i0 = 0; i0 < n_units; i0 += 32 * 8) {
         uint32_t va[8], vb[8];
@@ -498,8 +519,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         for (int j = 0; j < 8; ++j) {
           const int i = i0 + lane + 32 * j;
           if (i < n_units) {
-            const int f = i < n0 ? 0 : 1;
-            const int64_t u = f == 0 ? ub0 + i : ub1 + (i - n0);
+            int f = 0;
+            while (f + 1 < P.nphase && i >= fs[f + 1]) ++f;
+            const int64_t u = fb[f] + (i - fs[f]);
             const int p = prob_of(P, f, u);
             const int64_t loc = u - P.pr[p].unit0;
             va[j] = P.pr[p].exc_off[loc];
@@ -781,12 +803,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     // Walk the CTA's segments (its runs of units of one tile) phase by phase;
     // only (phase, next unit, end of range) is carried between segments.
     int fn = 0;
-    int64_t un = unit_begin(c, P.phase_units[0], G), uen = unit_begin(c + 1, P.phase_units[0], G);
+    int64_t un = pbegin(P, c, 0), uen = pbegin(P, c + 1, 0);
     bool more = un < uen;
     if constexpr (kMulti) {
       for (fn = 1; fn < P.nphase && !more; ++fn) {
-        un = unit_begin(c, P.phase_units[fn], G);
-        uen = unit_begin(c + 1, P.phase_units[fn], G);
+        un = pbegin(P, c, fn);
+        uen = pbegin(P, c + 1, fn);
         more = un < uen;
       }
       --fn;
@@ -796,7 +818,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     while (more) {
       const int f = kMulti ? fn : 0;
       const int64_t Uf = P.phase_units[f];
-      const int64_t ub = kMulti ? unit_begin(c, Uf, G) : ub0, ue = uen;
+      const int Gf = phase_ctas(P, f);
+      const int64_t ub = kMulti ? pbegin(P, c, f) : ub0, ue = uen;
       const int pi = kMulti ? prob_of(P, f, un) : 0;
       const int KBp = P.pr[pi].KB;
       const int64_t u0p = kMulti ? P.pr[pi].unit0 : 0;
@@ -809,8 +832,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       if constexpr (kMulti) {
         if (!more) {
           for (++fn; fn < P.nphase && !more; ++fn) {
-            un = unit_begin(c, P.phase_units[fn], G);
-            uen = unit_begin(c + 1, P.phase_units[fn], G);
+            un = pbegin(P, c, fn);
+            uen = pbegin(P, c + 1, fn);
             more = un < uen;
           }
           --fn;
@@ -826,15 +849,15 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         accb = 0;
         accph ^= 1u;
       }
-      const int c_first = unit_owner(tile_u0, Uf, G);
-      const int c_last = unit_owner(tile_u0 + KBp - 1, Uf, G);
+      const int c_first = unit_owner(tile_u0, Uf, Gf);
+      const int c_last = unit_owner(tile_u0 + KBp - 1, Uf, Gf);
       const int nsplit = c_last - c_first + 1;
       // Partial slots are laid out [chunk][row][16] floats: each thread's 16
       // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
       // CTA cc has two slots per phase: its first piece in the phase, and
       // its last.
       auto slot_of = [&](int cc) {
-        const int64_t u0 = unit_begin(cc, Uf, G);
+        const int64_t u0 = pbegin(P, cc, f);
         return 2 * (cc * P.nphase + f) + ((u0 >= tile_u0 && u0 < tile_u0 + KBp) ? 0 : 1);
       };
       // The CTA's final segment ends the kernel. When its tile has one other
@@ -1117,11 +1140,11 @@ static void set_problem(ProbParams& q, bool w12_mode, const w12_weights* W, int6
   q.Y = Y;
 }
 
-// Grouped launch: problems in launch order (phase 0: every problem but the
-// SwiGLU target; phase 1: the target), with the workspace carve-up.
+// Grouped launch: problems in launch order with their phases, and the
+// workspace carve-up.
 struct Grouped {
-  int n, order[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks;
-  int64_t N[kMaxProb], K[kMaxProb], phase_units[2];
+  int n, order[kMaxProb], phase[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks;
+  int64_t N[kMaxProb], K[kMaxProb], phase_units[kMaxProb];
   size_t counters, glu_cnt, glu_ready, epoch, parts, total;
 };
 
@@ -1148,16 +1171,31 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
     if (g->N[link->from] % (2 * kGroup) || g->K[link->to] != g->N[link->from] / 2) return W12_ERR_SHAPE;
     to = link->to;
   }
+  // Phases. Independent problems form one phase: their units are split over
+  // the CTAs as one stream, so a tile is cut only where a CTA's range ends.
+  // With a SwiGLU link the source forms the first phase, the other problems
+  // the second (the activation blocks complete while the CTAs work on them)
+  // and the target the last.
+  const int from = link ? link->from : -1;
   int k = 0;
+  if (from >= 0) {
+    g->order[k] = from;
+    g->phase[k++] = 0;
+  }
   for (int i = 0; i < n; ++i)
-    if (i != to) g->order[k++] = i;
-  if (to >= 0) g->order[k++] = to;
-  g->nphase = to >= 0 ? 2 : 1;
+    if (i != to && i != from) {
+      g->order[k] = i;
+      g->phase[k++] = from >= 0 ? 1 : 0;
+    }
+  g->nphase = (from >= 0 ? 1 : 0) + (n - (from >= 0 ? 2 : 0) > 0 ? 1 : 0);
+  if (to >= 0) {
+    g->order[k] = to;
+    g->phase[k++] = g->nphase++;
+  }
   int64_t maxu = 0;
   for (int j = 0; j < n; ++j) {
     const int i = g->order[j];
-    const int f = (i == to) ? 1 : 0;
-    g->phase_units[f] += (g->N[i] / kGroup) * (g->K[i] / kGroup);
+    g->phase_units[g->phase[j]] += (g->N[i] / kGroup) * (g->K[i] / kGroup);
     g->tiles += int(g->N[i] / kGroup);
   }
   for (int f = 0; f < g->nphase; ++f) maxu = g->phase_units[f] > maxu ? g->phase_units[f] : maxu;
@@ -1168,8 +1206,7 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
   for (int f = 0; f < g->nphase; ++f) per_cta += (g->phase_units[f] + g->grid - 1) / g->grid;
   if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
   if (to >= 0) {
-    for (int j = 0; j < n; ++j)
-      if (g->order[j] == link->from) g->glu_from = j;
+    g->glu_from = 0;
     g->glu_to = n - 1;
     g->glu_blocks = int(g->N[link->from] / (2 * kGroup));
   }
@@ -1214,20 +1251,18 @@ static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_
   P.grid = g.grid;
   P.nprob = n;
   P.nphase = g.nphase;
-  P.phase_units[0] = g.phase_units[0];
-  P.phase_units[1] = g.phase_units[1];
-  P.pfirst[0] = 0;
-  P.pfirst[1] = g.nphase > 1 ? n - 1 : n;
+  for (int f = 0; f < g.nphase; ++f) P.phase_units[f] = g.phase_units[f];
+  for (int j = n - 1; j >= 0; --j) P.pfirst[g.phase[j]] = j;
   GemmMaps TM;
   memset(&TM, 0, sizeof(TM));
-  int64_t unit0[2] = {0, 0};
   int tile0 = 0;
+  int64_t unit0[kMaxProb] = {0, 0, 0, 0};
   for (int j = 0; j < n; ++j) {
     const int i = g.order[j];
     const bool is_to = link && i == link->to;
     ProbParams& q = P.pr[j];
     set_problem(q, w12_mode, probs[i].W, g.N[i], g.K[i], probs[i].Y);
-    q.phase = is_to ? 1 : 0;
+    q.phase = g.phase[j];
     q.unit0 = unit0[q.phase];
     unit0[q.phase] += int64_t(q.tiles) * q.KB;
     q.tile0 = tile0;
