@@ -56,6 +56,19 @@ What it computes, and the passage each part follows:
   article, "Technical architecture": every draft token is conditioned on its
   root-to-node path; SpecPilot digest "Reasons" bullet 2: tree verification).
 
+* ``kv_commit`` / ``state_select`` / ``check_path`` -- the step right after
+  acceptance: the verify pass wrote a key/value row for every draft node
+  (node i of request b at position prefix_len[b] + i); the accepted path's
+  rows must end up contiguous after the committed prefix, and a recurrent
+  target keeps the state of the path's last node (SpecPilot digest,
+  "Reasons" bullet 2: tree verification for targets with recurrent layers;
+  JetSpec article, "Technical architecture": each draft token is conditioned
+  on its root-to-node path). The pages do not describe the cache; the reading
+  here: caches are [B, S_max, row] arrays, the path is root-first with
+  strictly increasing node indices, and the commit moves row
+  prefix+path[k] to prefix+k for k < path_len and returns the new length
+  prefix + path_len; an invalid path leaves its request unchanged.
+
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 facts fixed outside this module (hand-derived golden bytes, brute force on
 small inputs, closed forms, exact special cases). No function is unpinned.
@@ -334,3 +347,54 @@ def verify_tree(parents: np.ndarray, draft: np.ndarray, target: np.ndarray):
         acc[b] = d
         bonus[b] = int(target[b, node])
     return path, plen, acc, bonus
+
+
+# ---------------------------------------------------------------------------
+# Commit of the accepted path
+# ---------------------------------------------------------------------------
+
+def check_path(path: np.ndarray, path_len: int, prefix_len: int, S_max: int) -> bool:
+    """A usable path: 1 <= path_len <= len(path), node indices strictly
+    increasing from >= 0, every target and source row inside the cache."""
+    path = np.asarray(path)
+    n = int(path_len)
+    if n < 1 or n > len(path) or prefix_len < 0:
+        return False
+    p = [int(v) for v in path[:n]]
+    if p[0] < 0 or any(p[k + 1] <= p[k] for k in range(n - 1)):
+        return False
+    return prefix_len + p[-1] < S_max
+
+
+def kv_commit(caches, prefix_len, path, path_len):
+    """(new caches, new_len): row prefix+path[k] -> row prefix+k, k < path_len.
+
+    caches: list of arrays [B, S_max, row]; read before any write (the moves
+    are defined on the cache as it was before the commit).
+    """
+    prefix_len = np.asarray(prefix_len)
+    path = np.asarray(path)
+    path_len = np.asarray(path_len)
+    out = [np.array(c, copy=True) for c in caches]
+    B = len(prefix_len)
+    new_len = prefix_len.astype(np.int64).copy()
+    for b in range(B):
+        P = int(prefix_len[b])
+        n = int(path_len[b])
+        if not check_path(path[b], n, P, caches[0].shape[1]):
+            continue
+        src = P + path[b, :n].astype(np.int64)
+        for c_in, c_out in zip(caches, out):
+            c_out[b, P:P + n] = c_in[b, src]
+        new_len[b] = P + n
+    return out, new_len
+
+
+def state_select(states: np.ndarray, path: np.ndarray, path_len: np.ndarray) -> np.ndarray:
+    """State of each request's accepted node: states[b, path[b, path_len[b]-1]].
+
+    states: [B, T, row], one state per draft node (recurrent layers)."""
+    states = np.asarray(states)
+    path = np.asarray(path)
+    B = states.shape[0]
+    return np.stack([states[b, int(path[b, int(path_len[b]) - 1])] for b in range(B)])

@@ -282,3 +282,70 @@ def test_swiglu_closed_forms_and_halves():
     assert O.swiglu(np.array([[-200.0, 1.0]]))[0, 0] in (0x0000, 0x8000)
     # The gate is the first half: swapping the halves changes the result.
     assert O.swiglu(np.array([[2.0, -1.0]]))[0, 0] != O.swiglu(np.array([[-1.0, 2.0]]))[0, 0]
+
+
+# ---------------------------------------------------------------------------
+# Commit of the accepted path
+# ---------------------------------------------------------------------------
+
+def _pos_cache(B, S, W):
+    # Row s of request b holds the value 1000*b + s in every column, so a moved
+    # row shows where it came from.
+    return np.broadcast_to((1000 * np.arange(B)[:, None] + np.arange(S)[None, :])[:, :, None], (B, S, W)).copy()
+
+
+def test_kv_commit_hand_case():
+    c = _pos_cache(2, 10, 3)
+    # Request 0: prefix 1, path 0 -> 2 -> 5: rows 1, 3, 6 move to rows 1, 2, 3.
+    # Request 1: prefix 4, path 0 -> 1: rows 4, 5 already in place.
+    path = np.array([[0, 2, 5, -1], [0, 1, -1, -1]])
+    out, new_len = O.kv_commit([c], [1, 4], path, [3, 2])
+    exp0 = list(range(10))
+    exp0[1:4] = [1, 3, 6]
+    np.testing.assert_array_equal(out[0][0, :, 0], exp0)
+    np.testing.assert_array_equal(out[0][1, :, 0], 1000 + np.arange(10))
+    np.testing.assert_array_equal(new_len, [4, 6])
+    assert np.all(out[0][..., 0:1] == out[0])        # whole rows move
+
+
+def test_kv_commit_reads_before_writes():
+    # Path 0 -> 2 -> 3 at prefix 0: row 2 is a source (for row 1) and later a
+    # destination (for row 3's value). The definition uses the cache as it was:
+    # rows 0, 1, 2 become 0, 2, 3, not 0, 3, 3.
+    c = _pos_cache(1, 6, 2)
+    out, new_len = O.kv_commit([c, c * 2], [0], np.array([[0, 2, 3]]), [3])
+    np.testing.assert_array_equal(out[0][0, :, 0], [0, 2, 3, 3, 4, 5])
+    np.testing.assert_array_equal(out[1][0, :, 0], [0, 4, 6, 6, 8, 10])
+    assert new_len[0] == 3
+
+
+def test_kv_commit_identity_and_invalid_paths():
+    c = _pos_cache(3, 8, 2)
+    path = np.array([[0, 1, 2], [0, 2, 1], [0, 3, 9]])     # identity; not increasing; source out of range
+    out, new_len = O.kv_commit([c], [2, 2, 2], path, [3, 3, 3])
+    np.testing.assert_array_equal(out[0], c)
+    np.testing.assert_array_equal(new_len, [5, 2, 2])
+    assert O.check_path([0, 1, 2], 3, 2, 8)
+    assert not O.check_path([0, 2, 1], 3, 2, 8)
+    assert not O.check_path([0, 3, 9], 3, 2, 8)
+    assert not O.check_path([0, 1], 0, 0, 8)
+    assert not O.check_path([-1, 1], 2, 0, 8)
+
+
+def test_kv_commit_matches_tree_walk_paths():
+    """Paths from the tree oracle are valid commit paths: root first, strictly
+    increasing (a parent's index is below its child's)."""
+    g = np.random.default_rng(5)
+    parents = np.stack([S.random_tree(64, g=g) for _ in range(4)])
+    target = g.integers(0, 5, size=4 * 64)
+    draft = g.integers(0, 5, size=(4, 64))
+    path, plen, acc, _ = O.verify_tree(parents, draft, target)
+    for b in range(4):
+        assert O.check_path(path[b], plen[b], 0, 64)
+        assert plen[b] == acc[b] + 1
+
+
+def test_state_select_hand_case():
+    states = np.arange(2 * 5 * 2).reshape(2, 5, 2)
+    sel = O.state_select(states, np.array([[0, 3, -1], [0, 1, 4]]), [2, 3])
+    np.testing.assert_array_equal(sel, [[6, 7], [18, 19]])
