@@ -558,6 +558,35 @@ def run_sweep(args, local):
                         "frac_hbm": head.nbytes / (t * 1e-3) / 1e9 / hbm_peak,
                         "tflops": fl / (t * 1e-3) / 1e12, "frac_tensor": fl / (t * 1e-3) / 1e12 / tc_peak,
                         "accept_len": acc.cpu().tolist(), "planted": Ds}
+    # Commit of the accepted tree paths after verification (4 requests, the
+    # 4 x 64-node trees above): K and V caches of a 64-layer, 8 kv-head x 128
+    # target, 4096 positions each; the moved rows are the accepted paths'.
+    g = np.random.default_rng(S.SEED_TREE)
+    Bc, Tc, S_max, n_caches = 4, 64, 4096, 128
+    parents = np.stack([S.random_tree(Tc, g=g) for _ in range(Bc)])
+    path = np.full((Bc, Tc), -1, dtype=np.int32)
+    plen = np.zeros(Bc, dtype=np.int32)
+    for b in range(Bc):   # accepted node: the deepest node off the tree's spine (nodes 1..12)
+        depth = np.zeros(Tc, dtype=np.int64)
+        for i in range(1, Tc):
+            depth[i] = depth[parents[b, i]] + 1
+        node = 13 + int(np.argmax(depth[13:]))
+        p = [node]
+        while p[-1] != 0:
+            p.append(int(parents[b, p[-1]]))
+        p = p[::-1]
+        path[b, :len(p)] = p
+        plen[b] = len(p)
+    caches = [torch.zeros((Bc, S_max, 8 * 128), dtype=torch.bfloat16, device=dev) for _ in range(n_caches)]
+    prefix = torch.full((Bc,), 3000, dtype=torch.int32, device=dev)
+    dpath = torch.from_numpy(path).to(dev)
+    dplen = torch.from_numpy(plen).to(dev)
+    kc = w12.KVCommit(caches)
+    us = graph_chain_ms([lambda: kc.run(prefix, dpath, dplen)], dev, stream) * 1e3
+    moved = int(sum(int((path[b, :plen[b]] != np.arange(plen[b])).sum()) for b in range(Bc)))
+    out["kv_commit"] = {"us": us, "caches": n_caches, "requests": Bc, "rows_moved_per_cache": moved,
+                        "bytes_moved": 2 * moved * n_caches * 8 * 128 * 2, "accept_path_len": plen.tolist()}
+    del caches
     print(json.dumps(out), flush=True)
     return 0
 

@@ -203,6 +203,38 @@ int w12_gemm_grouped(const w12_problem* probs, int n, int64_t M, const w12_swigl
 int w12_gemm_grouped_bf16_ref(const w12_problem* probs, int n, int64_t M, const w12_swiglu* link,
                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* --- Commit of the accepted path ---------------------------------------- */
+/* The step after acceptance (SpecPilot digest, "Reasons" bullet 2: tree
+ * verification for targets with recurrent layers; JetSpec article,
+ * "Technical architecture": each draft token is conditioned on its
+ * root-to-node path). The verify pass wrote one row per draft node into
+ * each cache: node i of request b at position prefix_len[b] + i. The pages do
+ * not describe the cache; this library's reading is a row-major array
+ * [B, S_max, row_bytes] per cache (one per layer and per K or V, any element
+ * type; row_bytes a multiple of 16, base 16-byte aligned).
+ *
+ * w12_kv_commit moves, for every cache and request, row prefix_len[b] +
+ * path[b, k] to row prefix_len[b] + k for k < path_len[b], in place, and
+ * writes new_len[b] = prefix_len[b] + path_len[b] (new_len may be NULL).
+ * path [B, path_stride] is root-first with strictly increasing node indices
+ * (the tree verify output is such a path; a greedy block's accepted prefix is
+ * 0, 1, ..., L, which moves nothing). A request whose path is invalid (empty,
+ * longer than path_stride, not increasing, or reaching past S_max) is left
+ * unchanged, gets new_len = prefix_len, and sets W12_ERR_BAD_TREE in
+ * dev_status. caches is a HOST array of n_caches device pointers; prefix_len,
+ * path, path_len and new_len are device arrays. Rows past the new length keep
+ * whatever they held. Errors: W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_CUDA. */
+int w12_kv_commit(void* const* caches, int n_caches, int B, int64_t S_max, int64_t row_bytes,
+                  const int32_t* prefix_len, const int32_t* path, int path_stride, const int32_t* path_len,
+                  int32_t* new_len, int32_t* dev_status, void* stream);
+
+/* Recurrent state of the accepted node: out[b] = states[b, node] with node =
+ * path[b, path_len[b] - 1], states [B, T, row_bytes] (one state per draft
+ * node, written by the verify pass), out [B, row_bytes]. An invalid path sets
+ * W12_ERR_BAD_TREE in dev_status and leaves out[b] unchanged. */
+int w12_state_select(const void* states, int B, int T, int64_t row_bytes, const int32_t* path, int path_stride,
+                     const int32_t* path_len, void* out, int32_t* dev_status, void* stream);
+
 /* --- Greedy block verification (SpecPilot digest, "Risks" bullet 3) ----- */
 
 /* Workspace bytes for the verify entry points with M = B*rows verified rows

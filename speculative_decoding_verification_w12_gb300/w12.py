@@ -25,7 +25,7 @@ EXPORTS = [
     "w12_gemm_ws_bytes", "w12_gemm", "w12_gemm_bf16_ref", "w12_verify_ws_bytes", "w12_verify_greedy",
     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
     "w12_set_wait_limit_us", "w12_set_overlap", "w12_gemm_noalloc", "w12_gemm_grouped_ws_bytes",
-    "w12_gemm_grouped", "w12_gemm_grouped_bf16_ref",
+    "w12_gemm_grouped", "w12_gemm_grouped_bf16_ref", "w12_kv_commit", "w12_state_select",
 ]
 
 
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
             "w12_gemm_grouped": (i32, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu), vp, sz, vp, vp]),
             "w12_gemm_grouped_bf16_ref": (i32, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu), vp, sz,
                                                 vp, vp]),
+            "w12_kv_commit": (i32, [ctypes.POINTER(vp), i32, i32, i64, i64, vp, vp, i32, vp, vp, vp, vp]),
+            "w12_state_select": (i32, [vp, i32, i32, i64, vp, i32, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -291,6 +293,67 @@ class Grouped:
         _check(f(self._probs, self._n, self.M, link, self.ws.data_ptr(), self.ws.numel(), _ptr(self.status),
                  _stream(stream)), "w12_gemm_grouped")
         return self.Y
+
+
+def kv_commit(caches, prefix_len: torch.Tensor, path: torch.Tensor, path_len: torch.Tensor,
+              new_len: torch.Tensor | None = None, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Move each request's accepted-path rows to follow its committed prefix.
+
+    caches: list of contiguous device tensors [B, S_max, ...] (same B and
+    S_max; the trailing dimensions form one row); prefix_len, path_len int32
+    [B]; path int32 [B, stride], root-first (the tree verify output). Returns
+    new_len int32 [B] = prefix_len + path_len (prefix_len for invalid paths).
+    """
+    caches = list(caches)
+    B, S_max = caches[0].shape[:2]
+    row_bytes = caches[0][0, 0].numel() * caches[0].element_size()
+    for c in caches:
+        if not c.is_contiguous() or tuple(c.shape[:2]) != (B, S_max) or c[0, 0].numel() * c.element_size() != row_bytes:
+            raise ValueError("caches must be contiguous [B, S_max, ...] tensors with equal row sizes")
+    if new_len is None:
+        new_len = torch.empty(B, dtype=torch.int32, device=caches[0].device)
+    ptrs = (ctypes.c_void_p * len(caches))(*[c.data_ptr() for c in caches])
+    _check(lib().w12_kv_commit(ptrs, len(caches), B, S_max, row_bytes, prefix_len.data_ptr(), path.data_ptr(),
+                               path.shape[1], path_len.data_ptr(), new_len.data_ptr(), _ptr(status),
+                               _stream(stream)), "w12_kv_commit")
+    return new_len
+
+
+class KVCommit:
+    """kv_commit over a fixed set of caches, with the argument arrays built
+    once (for steps that commit every iteration, or graph capture)."""
+
+    def __init__(self, caches):
+        self.caches = list(caches)
+        c0 = self.caches[0]
+        self.B, self.S_max = c0.shape[:2]
+        self.row_bytes = c0[0, 0].numel() * c0.element_size()
+        for c in self.caches:
+            if (not c.is_contiguous() or tuple(c.shape[:2]) != (self.B, self.S_max)
+                    or c[0, 0].numel() * c.element_size() != self.row_bytes):
+                raise ValueError("caches must be contiguous [B, S_max, ...] tensors with equal row sizes")
+        self._ptrs = (ctypes.c_void_p * len(self.caches))(*[c.data_ptr() for c in self.caches])
+        self.new_len = torch.empty(self.B, dtype=torch.int32, device=c0.device)
+
+    def run(self, prefix_len: torch.Tensor, path: torch.Tensor, path_len: torch.Tensor,
+            status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        _check(lib().w12_kv_commit(self._ptrs, len(self.caches), self.B, self.S_max, self.row_bytes,
+                                   prefix_len.data_ptr(), path.data_ptr(), path.shape[1], path_len.data_ptr(),
+                                   self.new_len.data_ptr(), _ptr(status), _stream(stream)), "w12_kv_commit")
+        return self.new_len
+
+
+def state_select(states: torch.Tensor, path: torch.Tensor, path_len: torch.Tensor, out: torch.Tensor | None = None,
+                 status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[b] = states[b, path[b, path_len[b] - 1]]; states [B, T, ...] contiguous."""
+    B, T = states.shape[:2]
+    row_bytes = states[0, 0].numel() * states.element_size()
+    if out is None:
+        out = torch.empty((B,) + tuple(states.shape[2:]), dtype=states.dtype, device=states.device)
+    _check(lib().w12_state_select(states.data_ptr(), B, T, row_bytes, path.data_ptr(), path.shape[1],
+                                  path_len.data_ptr(), out.data_ptr(), _ptr(status), _stream(stream)),
+           "w12_state_select")
+    return out
 
 
 def gemm_bf16_ref(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None, ws: torch.Tensor | None = None,
