@@ -215,7 +215,8 @@ __host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
 }
 
 struct Bars {
-  uint64_t* full;
+  uint64_t* full;     // weight bytes of a stage landed (decoders wait on this)
+  uint64_t* full_x;   // X bytes of a stage landed (the MMA waits on this too)
   uint64_t* empty;
   uint64_t* a_full;
   uint64_t* acc_full;
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   B.exc_ready = B.acc_empty + 2;
   B.drain = B.exc_ready + 1;
   B.gather = B.drain + 1;
+  B.full_x = B.gather + 1;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + plan.misc_off);
   volatile uint32_t* tmem_slot = misc + 0;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -267,6 +269,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&B.full[s], 1);
+      mbar_init(&B.full_x[s], 1);
       mbar_init(&B.empty[s], 1);
     }
     if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
@@ -331,7 +334,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const uint32_t xbox = uint32_t(P.Mpad) * 128u;
-      const uint32_t tx = C::kABytes + (kW12 ? 128u : 0u) + 2u * xbox;
+      // Weights and X of a stage complete separately: the decoders can restore
+      // a stage's weights while its X is still on the way (or, for the SwiGLU
+      // target, not yet written).
+      const uint32_t tx = C::kABytes + (kW12 ? 128u : 0u);
+      const uint32_t txx = 2u * xbox;
       // Weight tile of the unit at cursor x into stage buffer st.
       auto load_w = [&](const Cur& x, uint8_t* st, uint64_t* bar) {
         const int pp = single ? 0 : x.p;
@@ -403,8 +410,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         const CUtensorMap* mx = &TM.m[single ? 0 : x.p][3];
-        tma_load_2d_hint(st + plan.x_off, mx, x.kb * 128, 0, &B.full[s], pol_x);
-        tma_load_2d_hint(st + plan.x_off + xbox, mx, x.kb * 128 + 64, 0, &B.full[s], pol_x);
+        mbar_arrive_expect_tx(&B.full_x[s], txx);
+        tma_load_2d_hint(st + plan.x_off, mx, x.kb * 128, 0, &B.full_x[s], pol_x);
+        tma_load_2d_hint(st + plan.x_off + xbox, mx, x.kb * 128 + 64, 0, &B.full_x[s], pol_x);
         step(x);
         if (++s == S) {
           s = 0;
@@ -416,8 +424,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         // Let the copies already issued land before the CTA can exit. The
         // loop only stops at a stage boundary with every stage before it
         // fully issued (weights and X).
-        for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+        for (int i = issued > S ? issued - S : 0; i < issued; ++i) {
           mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, lim);
+          mbar_wait(&B.full_x[i % S], uint32_t(i / S) & 1u, lim);
+        }
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -450,9 +460,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           started = false;
         }
         if (i % NISS == k) {
-          // W12: the decoders waited for the stage's copies before arriving on
-          // a_full, so "decoded" implies "landed" for X as well.
+          // W12: the decoders waited for the stage's weights before arriving
+          // on a_full; X completes on its own barrier.
           if (kW12 ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
+          if (!wait(&B.full_x[s], ph)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + uint32_t(accb * NISS + k) * uint32_t(P.Mpad);
           const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
@@ -540,6 +551,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
       }
       bad = __any_sync(0xFFFFFFFFu, bad);
+      __syncwarp();
       __syncwarp();
       if (lane == 0) {
         if (bad) set_status(P.status, W12_ERR_CORRUPT);
@@ -783,10 +795,19 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       if (*glu_flag) {
         const int64_t Nh = pg.N / 2;
         const int64_t col = int64_t(j) * 128 + et;
-        for (int m = 0; m < P.M; ++m) {
-          const float g = __ldcg(pg.Y + int64_t(m) * pg.N + col);
-          const float u = __ldcg(pg.Y + int64_t(m) * pg.N + Nh + col);
-          P.act[int64_t(m) * Nh + col] = f32_to_bf16_rne(g / (1.0f + expf(-g)) * u);
+        // 16 rows per batch, every load of a batch issued before its first
+        // use: one L2 round trip per 16 rows.
+        for (int m0 = 0; m0 < P.M; m0 += 16) {
+          float g[16], u[16];
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            const int m = m0 + r < P.M ? m0 + r : P.M - 1;
+            g[r] = __ldcg(pg.Y + int64_t(m) * pg.N + col);
+            u[r] = __ldcg(pg.Y + int64_t(m) * pg.N + Nh + col);
+          }
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (m0 + r < P.M) P.act[int64_t(m0 + r) * Nh + col] = f32_to_bf16_rne(g[r] / (1.0f + expf(-g[r])) * u[r]);
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
@@ -867,7 +888,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // here without writing a partial or taking a counter round trip.
       const int me = c - c_first;
       int pref = 0;
-      if (final_seg && nsplit == 2 && nchunks == 1) {
+      // (Any phase's last segment qualifies: the prefetch goes to the
+      // epilogue's own transpose buffer, not to the ring.)
+      if (seg_end == ue && nsplit == 2 && nchunks == 1) {
         if (et == 0) {
           int done = 0;
           const uint64_t t0 = globaltimer_ns();

@@ -130,3 +130,23 @@ def test_grouped_argument_errors():
     assert e.value.code == 1   # the workspace query reports invalid arguments
     with pytest.raises(w12.W12Error):
         w12.Grouped([(X, pk, None)] * 5, M)
+
+
+@pytest.mark.parametrize("zero_frac", [0.02, 0.3])
+def test_grouped_exception_heavy(zero_frac):
+    """Zeros are exceptions: 2 % keeps a CTA's exception entries in shared
+    memory, 30 % overflows it (entries then read from global memory)."""
+    M = 16
+    shapes = [(1024, 2048), (512, 1024)]
+    Ws, Xs = _problems(shapes, M, seed=21)
+    g = np.random.default_rng(5)
+    for W in Ws:
+        W[g.random(W.shape) < zero_frac] = 0
+    pks = [w12.pack(to_dev_bf16(W)) for W in Ws]
+    assert pks[0].n_exc > 0.8 * zero_frac * Ws[0].size
+    st = new_status()
+    gr = w12.Grouped([(to_dev_bf16(X), pk, None) for X, pk in zip(Xs, pks)], M, status=st)
+    Ys = gr.run()
+    assert status_value(st) == 0
+    for i, (X, W) in enumerate(zip(Xs, Ws)):
+        assert_gemm_close(Ys[i].cpu().numpy(), O.gemm(X, O.pack(W)), f"problem {i}, zeros {zero_frac}")
