@@ -69,6 +69,18 @@ What it computes, and the passage each part follows:
   prefix+path[k] to prefix+k for k < path_len and returns the new length
   prefix + path_len; an invalid path leaves its request unchanged.
 
+* ``tree_attention`` -- the attention half of the target's verify pass over
+  a causal draft tree: query row (request b, node t, head h) attends to every
+  committed prefix position of request b and to the draft positions of the
+  nodes on its own root-to-node path, itself included (JetSpec article,
+  "Technical architecture": each draft token is conditioned on the path that
+  leads to it; SpecPilot digest, "Reasons" bullet 2: tree verification). The
+  pages give no attention details; the reading here: softmax attention with
+  scores scale * q.k, grouped-query heads (query head h reads key/value head
+  h // (Hq / Hkv)), key/value caches [B, S_max, Hkv, d] with node i's row at
+  position prefix_len[b] + i, queries and outputs [B, T, Hq, d]. A block of
+  16 drafted tokens is the chain tree parents[i] = i - 1.
+
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 facts fixed outside this module (hand-derived golden bytes, brute force on
 small inputs, closed forms, exact special cases). No function is unpinned.
@@ -398,3 +410,53 @@ def state_select(states: np.ndarray, path: np.ndarray, path_len: np.ndarray) -> 
     path = np.asarray(path)
     B = states.shape[0]
     return np.stack([states[b, int(path[b, int(path_len[b]) - 1])] for b in range(B)])
+
+
+# ---------------------------------------------------------------------------
+# Tree-masked verify attention
+# ---------------------------------------------------------------------------
+
+def tree_ancestors(parents: np.ndarray) -> np.ndarray:
+    """anc[t, j] = True iff node j lies on the path root -> t (t included)."""
+    parents = np.asarray(parents)
+    T = len(parents)
+    anc = np.zeros((T, T), dtype=bool)
+    for t in range(T):
+        j = t
+        while j >= 0:
+            anc[t, j] = True
+            j = int(parents[j])
+    return anc
+
+
+def tree_attention(Q_bits, K_bits, V_bits, prefix_len, parents, scale: float) -> np.ndarray:
+    """float64 attention outputs [B, T, Hq, d] of a draft tree over its prefix.
+
+    Q_bits [B, T, Hq, d], K_bits / V_bits [B, S_max, Hkv, d] (bf16 bits).
+    Row (b, t, h) takes keys 0..prefix_len[b]-1 and the keys prefix_len[b] + j
+    of the nodes j on its root-to-node path; weights softmax(scale * q.k).
+    """
+    prefix_len = np.asarray(prefix_len)
+    parents = np.asarray(parents)
+    B, T, Hq, d = Q_bits.shape
+    Hkv = K_bits.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, T, Hq, d))
+    for b in range(B):
+        P = int(prefix_len[b])
+        L = P + T
+        allowed = np.zeros((T, L), dtype=bool)
+        allowed[:, :P] = True
+        allowed[:, P:] = tree_ancestors(parents[b])
+        for g in range(Hkv):
+            Kg = bf16_to_f64(K_bits[b, :L, g, :])            # [L, d]
+            Vg = bf16_to_f64(V_bits[b, :L, g, :])
+            for h in range(g * G, (g + 1) * G):
+                q = bf16_to_f64(Q_bits[b, :, h, :])          # [T, d]
+                s = scale * (q @ Kg.T)                        # [T, L]
+                s = np.where(allowed, s, -np.inf)
+                s = s - s.max(axis=1, keepdims=True)
+                w = np.exp(s)
+                w = w / w.sum(axis=1, keepdims=True)
+                out[b, :, h, :] = w @ Vg
+    return out

@@ -93,6 +93,17 @@ def activations_bf16(M: int, K: int, seed: int = SEED_ACTIVATIONS, std: float = 
     return f32_to_bf16_bits(g.standard_normal((M, K), dtype=np.float32) * np.float32(std))
 
 
+def attention_inputs_bf16(B: int, T: int, S_max: int, Hq: int, Hkv: int, d: int,
+                          seed: int = SEED_ACTIVATIONS, tag: int = 11):
+    """bf16 bits of the verify attention's inputs, all N(0, 1): queries
+    [B, T, Hq, d] and key / value caches [B, S_max, Hkv, d]."""
+    g = rng(seed, tag)
+    Q = f32_to_bf16_bits(g.standard_normal((B, T, Hq, d), dtype=np.float32))
+    K = f32_to_bf16_bits(g.standard_normal((B, S_max, Hkv, d), dtype=np.float32))
+    V = f32_to_bf16_bits(g.standard_normal((B, S_max, Hkv, d), dtype=np.float32))
+    return Q, K, V
+
+
 def logits_f32(M: int, V: int, seed: int = SEED_ACTIVATIONS, tag: int = 7) -> np.ndarray:
     """float32 [M, V] logits with N(0, 1) entries (for the unfused verify entry points)."""
     return rng(seed, tag).standard_normal((M, V), dtype=np.float32)
