@@ -235,6 +235,40 @@ int w12_kv_commit(void* const* caches, int n_caches, int B, int64_t S_max, int64
 int w12_state_select(const void* states, int B, int T, int64_t row_bytes, const int32_t* path, int path_stride,
                      const int32_t* path_len, void* out, int32_t* dev_status, void* stream);
 
+/* --- Tree-masked verify attention ---------------------------------------- */
+/* The attention half of the target's verify pass over a causal draft tree
+ * (JetSpec article, "Technical architecture": every draft token is
+ * conditioned on the path that leads to it; SpecPilot digest, "Reasons"
+ * bullet 2: tree verification; a block of T drafted tokens is the chain tree
+ * parents[i] = i - 1). The pages give no attention details; this library's
+ * reading:
+ *   O[b, t, h, :] = sum_j softmax_j(scale * Q[b, t, h, :] . K[b, j, h / G, :])
+ *                   * V[b, j, h / G, :],   G = Hq / Hkv,
+ * over the keys j < prefix_len[b] and j = prefix_len[b] + i for every node i
+ * on the path root -> t (t included). Layouts (all bf16, contiguous, 16-byte
+ * aligned device memory): Q and O [B, T, Hq, head_dim], K_cache and V_cache
+ * [B, S_max, Hkv, head_dim], node i's key/value at position prefix_len[b] + i
+ * (written by the verify pass before this call). parents [B, T] int32
+ * (parents[b, 0] = -1, 0 <= parents[b, i] < i), prefix_len [B] int32, both
+ * device arrays. head_dim must be 128; 1 <= T <= 128; Hq a multiple of Hkv.
+ * max_kv_len (host) bounds prefix_len[b] + T over the requests, T <= max_kv_len
+ * <= S_max; the work split is planned for it. Cache rows at or past
+ * prefix_len[b] + T are never used (they may hold anything). Computes in fp32
+ * with P rounded to bf16 for the P.V product and O rounded to bf16.
+ * Device-side errors in dev_status: W12_ERR_BAD_TREE (malformed parents; that
+ * request's outputs are unspecified), W12_ERR_ARG (prefix_len[b] < 0 or
+ * prefix_len[b] + T > max_kv_len; the request is computed with its prefix
+ * clamped into range). Returns W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_WORKSPACE,
+ * W12_ERR_UNSUPPORTED or W12_ERR_CUDA. The workspace (no zero-fill needed) is
+ * at least w12_tree_attention_ws_bytes(...) bytes, which is 0 for a shape the
+ * call rejects. */
+size_t w12_tree_attention_ws_bytes(int B, int T, int Hq, int Hkv, int64_t max_kv_len);
+
+int w12_tree_attention(const uint16_t* Q, const uint16_t* K_cache, const uint16_t* V_cache, int B, int T, int Hq,
+                       int Hkv, int head_dim, int64_t S_max, int64_t max_kv_len, const int32_t* prefix_len,
+                       const int32_t* parents, float scale, uint16_t* O, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, void* stream);
+
 /* --- Greedy block verification (SpecPilot digest, "Risks" bullet 3) ----- */
 
 /* Workspace bytes for the verify entry points with M = B*rows verified rows

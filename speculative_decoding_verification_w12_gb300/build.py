@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libw12.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["w12_capi.cu", "w12_pack.cu", "w12_gemm.cu", "w12_grouped.cu", "w12_verify.cu", "w12_commit.cu", "w12_noalloc.cu"]
+SOURCES = ["w12_capi.cu", "w12_pack.cu", "w12_gemm.cu", "w12_grouped.cu", "w12_verify.cu", "w12_commit.cu", "w12_noalloc.cu", "w12_attn.cu"]
 
 
 def nvcc() -> str:

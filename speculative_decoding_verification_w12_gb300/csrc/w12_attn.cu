@@ -1,0 +1,649 @@
+// Tree-masked verify attention on the tensor cores.
+//
+// The verify pass scores a causal draft tree (a block of drafted tokens is the
+// chain tree) in one forward pass: each draft node's query attends to the
+// committed prefix and to the draft nodes on its own root-to-node path (JetSpec
+// article, "Technical architecture": every draft token is conditioned on the
+// path that leads to it; SpecPilot digest, "Reasons" bullet 2: tree
+// verification). Query row (b, t, h) reads key/value head h / (Hq / Hkv); node
+// i's key and value sit at cache position prefix_len[b] + i.
+//
+// One CTA takes 128 query rows of one (request, kv head) -- the rows (head hh
+// of the group, node t) in head-major order, so every row of the CTA reads the
+// same keys -- over one contiguous range of 128-key blocks (a split of the
+// request's keys when there are too few (request, kv head, row tile) items to
+// fill the GPU). Per key block:
+//   S = Q K^T        tcgen05.mma, A = Q (smem), B = K (smem, both K-major),
+//                    D = S in TMEM (double-buffered so S of the next block is
+//                    computed while this one is in the softmax);
+//   P = exp2(c S - m) the softmax warpgroup reads its row of S from TMEM, masks
+//                    it, and writes P as bf16 pairs back into TMEM;
+//   O += P V         tcgen05.mma, A = P (TMEM), B = V (smem, MN-major: the
+//                    cache's head dimension is contiguous), D = O in TMEM.
+// The running maximum m only moves when a block's maximum exceeds it by more
+// than 8 (in log2 units), so P <= 256 and O is rescaled rarely; the output is
+// O / l with l the sum of the rounded P. With several splits each CTA writes
+// (O, m, l) and attn_combine_kernel merges them.
+//
+// Warp roles (256 threads): warp 0 issues the TMA copies of K and V, warp 1
+// allocates TMEM and issues the MMAs, warps 4-7 (a warpgroup: warp w reads
+// TMEM lanes 32 (w % 4) ..) run the softmax and the epilogue; all warps load Q.
+#include "w12_dev.cuh"
+#include "w12_host.h"
+
+namespace w12 {
+namespace attn_impl {
+
+constexpr int kD = 128;                         // head dimension
+constexpr int kKeys = 128;                      // keys per block
+constexpr int kThreads = 256;
+constexpr int kStages = 3;
+constexpr int kMaxT = 128;                      // draft nodes per request
+constexpr uint32_t kHalf = 128u * 128u;         // 128 rows x 64 bf16 (one 128-byte swizzled half)
+constexpr uint32_t kTile = 2u * kHalf;          // 128 rows x 128 bf16
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kStageOff = kTile;           // stage s: K at kStageOff + s*2*kTile, V right after
+constexpr uint32_t kBarOff = kStageOff + uint32_t(kStages) * 2u * kTile;
+constexpr uint32_t kSmemBytes = kBarOff + 128 + 1024;  // barriers + misc + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColP = 256, kColO = 384;
+constexpr float kRescale = 8.0f;                // log2 growth of the maximum that triggers a rescale
+
+struct AttnParams {
+  const uint16_t* Q;          // [B, T, Hq, 128]
+  uint16_t* O;                // [B, T, Hq, 128]
+  const int32_t* prefix_len;  // [B]
+  const int32_t* parents;     // [B, T]
+  float* part_o;              // [items, nsplit, 128, 128] (nsplit > 1)
+  float2* part_ml;            // [items, nsplit, 128]: (m, l)
+  int32_t* status;
+  int B, T, Hq, Hkv, G, ntile, nsplit, bps, max_len;
+  float c;                    // scale * log2(e)
+  uint64_t limit_ns;
+};
+
+// Shared-memory matrix descriptor of an MN-major operand stored with the
+// 128-byte swizzle: rows along K are 128 bytes of 64 MN-consecutive values,
+// 8-row groups 1024 bytes apart (stride byte offset), and the next 64 values
+// along MN `lbo` bytes further (leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two fp32 values -> one word of bf16 (round to nearest even): lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word_sel(const uint32_t (&a)[4], int i) {
+  return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : i == 3 ? a[3] : 0u;
+}
+
+// Bits sh .. sh+31 of the 128-bit value a (zero outside [0, 128)).
+__device__ __forceinline__ uint32_t bits32(const uint32_t (&a)[4], int sh) {
+  if (sh <= -32 || sh >= 128) return 0u;
+  const int wi = sh >= 0 ? sh >> 5 : -1;
+  const int r = sh - wi * 32;  // 0..31
+  const uint32_t lo = word_sel(a, wi), hi = word_sel(a, wi + 1);
+  return r == 0 ? lo : (lo >> r) | (hi << (32 - r));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __grid_constant__ AttnParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* empty = full + kStages;
+  uint64_t* s_full = empty + kStages;  // [2]
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* tmem_slot = misc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int idx = blockIdx.x;
+  const int tile = idx % P.ntile;
+  idx /= P.ntile;
+  const int split = idx % P.nsplit;
+  idx /= P.nsplit;
+  const int g = idx % P.Hkv;
+  const int b = idx / P.Hkv;
+  const int T = P.T;
+  const int item = (b * P.Hkv + g) * P.ntile + tile;
+
+  // Everything below reads what the previous kernel on the stream wrote.
+  grid_dep_wait();
+  int Pb = P.prefix_len[b];
+  if (Pb < 0 || Pb + T > P.max_len) {
+    if (threadIdx.x == 0 && tile == 0 && split == 0 && g == 0) set_status(P.status, W12_ERR_ARG);
+    Pb = Pb < 0 ? 0 : P.max_len - T;
+  }
+  const int L = Pb + T;                             // keys of this request
+  const int nkb = (L + kKeys - 1) / kKeys;
+  const int j0 = split * P.bps;
+  const int j1 = min(j0 + P.bps, nkb);
+  const int n = j1 - j0;                            // key blocks of this CTA
+  if (n <= 0) {
+    // Nothing to attend to in this split: an empty partial (m = -inf).
+    if (threadIdx.x < 128)
+      P.part_ml[(size_t(item) * P.nsplit + split) * 128 + threadIdx.x] = make_float2(-INFINITY, 0.f);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(const_cast<uint32_t*>(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+
+  // Q tile: 128 rows (head hh of the group, node t) in head-major order, rows
+  // past G*T zero; two 128-byte-swizzled halves of 64 dims.
+  const int Rg = P.G * T;
+  {
+    uint8_t* qs = smem + kQOff;
+    for (int cid = threadIdx.x; cid < 128 * 16; cid += kThreads) {
+      const int r = cid >> 4, c = cid & 15;
+      const int rr = tile * 128 + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (rr < Rg) {
+        const int hh = rr / T, t = rr - hh * T;
+        const uint16_t* src = P.Q + ((size_t(b) * T + t) * P.Hq + size_t(g) * P.G + hh) * kD + c * 8;
+        v = *reinterpret_cast<const uint4*>(src);
+      }
+      *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t lim = P.limit_ns;
+
+  auto fail = [&](int code) {
+    set_status(P.status, code);
+    *abort_flag = 1;
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < 0x80000000u; ++i) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 63u) == 63u) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > lim) {
+          fail(W12_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+    fail(W12_ERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      for (; issued < n; ++issued) {
+        const int s = issued % kStages;
+        if (issued >= kStages && !wait(&empty[s], uint32_t((issued / kStages) - 1) & 1u)) break;
+        uint8_t* st = smem + kStageOff + uint32_t(s) * 2u * kTile;
+        const int key0 = (j0 + issued) * kKeys;
+        mbar_arrive_expect_tx(&full[s], 2u * kTile);
+        tma_load_4d(st, &tm_k, 0, g, key0, b, &full[s], pol);
+        tma_load_4d(st + kHalf, &tm_k, 64, g, key0, b, &full[s], pol);
+        tma_load_4d(st + kTile, &tm_v, 0, g, key0, b, &full[s], pol);
+        tma_load_4d(st + kTile + kHalf, &tm_v, 64, g, key0, b, &full[s], pol);
+      }
+      grid_dep_launch();
+      if (*abort_flag) {
+        for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+          mbar_wait(&full[i % kStages], uint32_t(i / kStages) & 1u, lim);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(128, 128);
+      const uint32_t idesc_o = idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t qdesc = sdesc_k_sw128(sbase + kQOff);
+      auto issue_s = [&](int i) -> bool {
+        const int s = i % kStages;
+        if (!wait(&full[s], uint32_t(i / kStages) & 1u)) return false;
+        tc_fence_after();
+        const uint32_t kaddr = sbase + kStageOff + uint32_t(s) * 2u * kTile;
+        const uint64_t kdesc = sdesc_k_sw128(kaddr);
+        const uint32_t d = tmem + ((i & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t off = uint64_t((uint32_t(ks >> 2) * kHalf + uint32_t(ks & 3) * 32u) >> 4);
+          mma_bf16_ss(d, qdesc + off, kdesc + off, idesc_s, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[i & 1]);
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n && !issue_s(i + 1)) break;
+        if (!wait(p_full, uint32_t(i) & 1u)) break;
+        tc_fence_after();
+        const int s = i % kStages;
+        const uint32_t vaddr = sbase + kStageOff + uint32_t(s) * 2u * kTile + kTile;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t bdesc = sdesc_mn_sw128(vaddr + uint32_t(ks) * 2048u, kHalf);
+          mma_bf16_ts(tmem + kColO, tmem + kColP + uint32_t(ks) * 8u, bdesc, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(o_done);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, lim);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ softmax, epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;                   // row of the tile = TMEM lane
+    const int rr = tile * 128 + r;
+    const bool valid = rr < Rg;
+    const int hh = valid ? rr / T : 0;
+    const int t = valid ? rr - hh * T : 0;
+    const uint32_t lane_off = uint32_t(q * 32) << 16;
+    // Ancestors of node t (itself included) as a 128-bit set.
+    uint32_t anc[4] = {0u, 0u, 0u, 0u};
+    if (valid) {
+      const int32_t* pb = P.parents + size_t(b) * T;
+      int j = t;
+      for (int step = 0; step <= T && j >= 0; ++step) {
+        const uint32_t bit = 1u << (j & 31);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) anc[w] |= (j >> 5) == w ? bit : 0u;
+        const int pj = pb[j];
+        if ((j == 0) ? (pj != -1) : (pj < 0 || pj >= j)) {
+          set_status(P.status, W12_ERR_BAD_TREE);
+          break;
+        }
+        j = pj;
+      }
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    const float c = P.c;
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const int key0 = (j0 + i) * kKeys;
+      if (!wait(&s_full[i & 1], uint32_t(i >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Keys of this block the row may see: all of the prefix, and the draft
+      // keys of its ancestors; none past the request's keys.
+      uint32_t allow[4];
+      if (key0 + kKeys <= Pb) {
+        allow[0] = allow[1] = allow[2] = allow[3] = valid ? ~0u : 0u;
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int lim_w = Pb - key0 - 32 * w;  // keys 32w + k with k < lim_w are prefix keys
+          const uint32_t pre = lim_w >= 32 ? ~0u : lim_w <= 0 ? 0u : ((1u << lim_w) - 1u);
+          const uint32_t tree = bits32(anc, key0 + 32 * w - Pb);
+          allow[w] = valid ? (pre | tree) : 0u;
+        }
+        // Cache rows past the request's keys may hold anything: zero them in
+        // the V stage so that P = 0 never meets a non-finite value.
+        const int nval = L - key0;
+        if (nval < kKeys) {
+          const int s = i % kStages;
+          if (!wait(&full[s], uint32_t(i / kStages) & 1u)) {
+            ok = false;
+            break;
+          }
+          if (r >= nval) {
+            uint8_t* vrow = smem + kStageOff + uint32_t(s) * 2u * kTile + kTile + uint32_t(r) * 128u;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vrow + kHalf + k * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      // Row of S -> scaled, masked scores (log2 units).
+      const uint32_t sc = tmem + lane_off + ((i & 1) ? kColS1 : kColS0);
+      float x[kKeys];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t v[16];
+        tmem_ld16(sc + uint32_t(ch * 16), v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int kk = ch * 16 + k;
+          const bool on = (allow[kk >> 5] >> (kk & 31)) & 1u;
+          x[kk] = on ? __uint_as_float(v[k]) * c : -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kKeys; ++k) mx = fmaxf(mx, x[k]);
+      float factor = 1.f;
+      if (mx > m_ref + kRescale) {
+        factor = fast_exp2(m_ref - mx);  // 0 while m_ref = -inf
+        m_ref = mx;
+      }
+      const float mref = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pw[kKeys / 2];
+      float psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < kKeys / 2; ++k) {
+        const uint32_t w = pack_bf16x2(fast_exp2(x[2 * k] - mref), fast_exp2(x[2 * k + 1] - mref));
+        pw[k] = w;
+        psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+      }
+      // P (single buffer) and O may be touched only once PV of the previous block is done.
+      if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (i > 0 && factor < 1.f && l > 0.f) {
+        const uint32_t oc = tmem + lane_off + kColO;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[16];
+          tmem_ld16(oc + uint32_t(ch * 16), v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
+          tmem_st16(oc + uint32_t(ch * 16), v);
+        }
+      }
+      l = l * factor + psum;
+      const uint32_t pc = tmem + lane_off + kColP;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = pw[ch * 16 + k];
+        tmem_st16(pc + uint32_t(ch * 16), v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // Epilogue: O row (after the last PV) -> output or partial.
+    if (ok && wait(o_done, uint32_t(n - 1) & 1u)) {
+      tc_fence_after();
+      const uint32_t oc = tmem + lane_off + kColO;
+      if (P.nsplit == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* dst = P.O + ((size_t(b) * T + t) * P.Hq + size_t(g) * P.G + hh) * kD;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[16];
+          tmem_ld16(oc + uint32_t(ch * 16), v);
+          tmem_ld_wait(v);
+          uint4 o0, o1;
+          o0.x = pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
+          o0.y = pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+          o0.z = pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
+          o0.w = pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
+          o1.x = pack_bf16x2(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
+          o1.y = pack_bf16x2(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
+          o1.z = pack_bf16x2(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
+          o1.w = pack_bf16x2(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
+          if (valid) {
+            reinterpret_cast<uint4*>(dst)[ch * 2] = o0;
+            reinterpret_cast<uint4*>(dst)[ch * 2 + 1] = o1;
+          }
+        }
+      } else {
+        const size_t prow = (size_t(item) * P.nsplit + split) * 128 + r;
+        float4* dst = reinterpret_cast<float4*>(P.part_o + prow * kD);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[16];
+          tmem_ld16(oc + uint32_t(ch * 16), v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[ch * 4 + k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                          __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+        }
+        P.part_ml[prow] = make_float2(m_ref, l);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merge the splits of every output row: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// One warp per output row (b, t, h); lane k owns dims 4k .. 4k+3.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams P) {
+  grid_dep_wait();
+  const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = int64_t(P.B) * P.T * P.Hq;
+  if (row >= rows) return;
+  const int h = int(row % P.Hq);
+  const int64_t bt = row / P.Hq;
+  const int t = int(bt % P.T), b = int(bt / P.T);
+  const int g = h / P.G, hh = h - g * P.G;
+  const int r = hh * P.T + t;
+  const int tile = r / 128, rit = r % 128;
+  const size_t item = size_t(b * P.Hkv + g) * P.ntile + tile;
+  float M = -INFINITY;
+  for (int s = 0; s < P.nsplit; ++s) M = fmaxf(M, P.part_ml[(item * P.nsplit + s) * 128 + rit].x);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < P.nsplit; ++s) {
+      const size_t prow = (item * P.nsplit + s) * 128 + rit;
+      const float2 ml = P.part_ml[prow];
+      if (ml.x == -INFINITY) continue;
+      const float w = fast_exp2(ml.x - M);
+      const float4 o = reinterpret_cast<const float4*>(P.part_o + prow * kD)[lane];
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+      den += w * ml.y;
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint2 out;
+  out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(P.O + size_t(row) * kD)[lane] = out;
+}
+
+struct AttnPlan {
+  int ntile, nkb, nsplit, bps;
+  int64_t items;
+};
+
+// Splits of each (request, kv head, row tile) item's key blocks: the count that
+// minimises waves x blocks per split on `sms` SMs (one CTA per SM), smallest on ties.
+static AttnPlan plan_attn(int B, int T, int Hq, int Hkv, int64_t max_len, int sms) {
+  AttnPlan p{};
+  const int G = Hq / Hkv;
+  p.ntile = (G * T + 127) / 128;
+  p.nkb = int((max_len + kKeys - 1) / kKeys);
+  p.items = int64_t(B) * Hkv * p.ntile;
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int s = 1; s <= p.nkb && s <= 64; ++s) {
+    const int64_t waves = (p.items * s + sms - 1) / sms;
+    const int64_t cost = waves * ((p.nkb + s - 1) / s);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  p.bps = (p.nkb + best - 1) / best;
+  p.nsplit = (p.nkb + p.bps - 1) / p.bps;
+  return p;
+}
+
+static int sms_or_default() {
+  const int sms = device_sm_count();
+  return sms > 0 ? sms : 152;
+}
+
+static bool shape_ok(int B, int T, int Hq, int Hkv, int head_dim, int64_t S_max, int64_t max_len) {
+  return B >= 1 && B <= 65535 && T >= 1 && T <= kMaxT && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && Hq <= 1024 &&
+         head_dim == kD && S_max >= T && S_max < (int64_t(1) << 31) && max_len >= T && max_len <= S_max;
+}
+
+static size_t ws_bytes_of(const AttnPlan& p) {
+  if (p.nsplit <= 1) return 256;
+  const size_t rows = size_t(p.items) * p.nsplit * 128;
+  return rows * kD * sizeof(float) + rows * sizeof(float2) + 256;
+}
+
+}  // namespace attn_impl
+}  // namespace w12
+
+using namespace w12;
+using namespace w12::attn_impl;
+
+extern "C" {
+
+size_t w12_tree_attention_ws_bytes(int B, int T, int Hq, int Hkv, int64_t max_kv_len) {
+  if (!shape_ok(B, T, Hq, Hkv, kD, max_kv_len, max_kv_len)) return 0;
+  return ws_bytes_of(plan_attn(B, T, Hq, Hkv, max_kv_len, sms_or_default()));
+}
+
+int w12_tree_attention(const uint16_t* Q, const uint16_t* K_cache, const uint16_t* V_cache, int B, int T, int Hq,
+                       int Hkv, int head_dim, int64_t S_max, int64_t max_kv_len, const int32_t* prefix_len,
+                       const int32_t* parents, float scale, uint16_t* O, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, void* stream) {
+  if (!Q || !K_cache || !V_cache || !prefix_len || !parents || !O || !aligned(Q, 16) || !aligned(K_cache, 16) ||
+      !aligned(V_cache, 16) || !aligned(O, 16) || !(scale == scale))
+    return W12_ERR_ARG;
+  if (!shape_ok(B, T, Hq, Hkv, head_dim, S_max, max_kv_len)) return W12_ERR_SHAPE;
+  if (!device_supported()) return W12_ERR_UNSUPPORTED;
+  const AttnPlan pl = plan_attn(B, T, Hq, Hkv, max_kv_len, sms_or_default());
+  if (pl.items * pl.nsplit > 0x7FFFFFFF) return W12_ERR_SHAPE;
+  if (pl.nsplit > 1 && (!ws || !aligned(ws, 16) || ws_bytes < ws_bytes_of(pl))) return W12_ERR_WORKSPACE;
+
+  AttnParams P{};
+  P.Q = Q;
+  P.O = O;
+  P.prefix_len = prefix_len;
+  P.parents = parents;
+  if (pl.nsplit > 1) {
+    const size_t rows = size_t(pl.items) * pl.nsplit * 128;
+    P.part_o = static_cast<float*>(ws);
+    P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + rows * kD * sizeof(float));
+  }
+  P.status = dev_status;
+  P.B = B;
+  P.T = T;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.G = Hq / Hkv;
+  P.ntile = pl.ntile;
+  P.nsplit = pl.nsplit;
+  P.bps = pl.bps;
+  P.max_len = int(max_kv_len);
+  P.c = float(double(scale) * 1.4426950408889634);
+  P.limit_ns = wait_limit_ns();
+
+  // Caches [B, S_max, Hkv, 128] as 4-D maps (dim, head, position, request):
+  // a box is 128 positions x 64 dims of one head, so a block never reads
+  // another request's rows (positions past S_max read as zero).
+  CUtensorMap tk, tv;
+  const uint64_t dims[4] = {uint64_t(kD), uint64_t(Hkv), uint64_t(S_max), uint64_t(B)};
+  const uint64_t strides[3] = {uint64_t(kD) * 2, uint64_t(Hkv) * kD * 2, uint64_t(S_max) * Hkv * kD * 2};
+  const uint32_t box[4] = {64, 1, uint32_t(kKeys), 1};
+  if (!encode_tmap_4d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(K_cache), dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_4d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(V_cache), dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return W12_ERR_CUDA;
+
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
+        cudaSuccess)
+      return W12_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(pl.items * pl.nsplit));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
+  int st = cuda_status(cudaLaunchKernelEx(&cfg, attn_kernel, tk, tv, P));
+  if (st || pl.nsplit == 1) return st;
+  const int64_t rows = int64_t(B) * T * Hq;
+  cudaLaunchConfig_t cfg2 = cfg;
+  cfg2.gridDim = dim3(unsigned((rows + 7) / 8));
+  cfg2.dynamicSmemBytes = 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg2, attn_combine_kernel, P));
+}
+
+}  // extern "C"

@@ -1,6 +1,7 @@
 // Shared host code of libw12.so: status strings, device queries, tensor-map
 // encoding, workspace layout, the wait bound and the timeout self-test.
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "w12_dev.cuh"
@@ -113,6 +114,52 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uin
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  keys[slot] = key;
+  maps[slot] = *map;
+  used[slot] = true;
+  return true;
+}
+
+bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, const uint64_t dims[4],
+                    const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle) {
+  constexpr int kSlots = 64;
+  struct Key {
+    int dtype, swizzle;
+    void* base;
+    uint64_t dims[4], strides[3];
+    uint32_t box[4];
+  };
+  static std::mutex mu;
+  static Key keys[kSlots];
+  static CUtensorMap maps[kSlots];
+  static bool used[kSlots] = {false};
+  Key key{};
+  key.dtype = int(dtype);
+  key.swizzle = int(swizzle);
+  key.base = base;
+  for (int i = 0; i < 4; ++i) key.dims[i] = dims[i], key.box[i] = box[i];
+  for (int i = 0; i < 3; ++i) key.strides[i] = strides_bytes[i];
+  auto same = [](const Key& a, const Key& b) { return std::memcmp(&a, &b, sizeof(Key)) == 0; };
+  uint64_t h = (reinterpret_cast<uint64_t>(base) >> 8) ^ uint64_t(dtype) ^ (uint64_t(swizzle) << 3);
+  for (int i = 0; i < 4; ++i) h = h * 0x9E3779B97F4A7C15ull + dims[i] + (uint64_t(box[i]) << 40);
+  const int slot = int(h % kSlots);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (used[slot] && same(keys[slot], key)) {
+      *map = maps[slot];
+      return true;
+    }
+  }
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t st[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, dtype, 4, base, d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lock(mu);

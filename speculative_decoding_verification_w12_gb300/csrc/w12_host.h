@@ -33,6 +33,11 @@ bool device_supported();
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// Encode a 4-D tiled tensor map (dims and box inner first; strides of dims 1..3
+// in bytes). Returns false on failure.
+bool encode_tmap_4d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, const uint64_t dims[4],
+                    const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle);
+
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? W12_OK : W12_ERR_CUDA; }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

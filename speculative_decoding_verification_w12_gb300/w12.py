@@ -26,6 +26,7 @@ EXPORTS = [
     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
     "w12_set_wait_limit_us", "w12_set_overlap", "w12_gemm_noalloc", "w12_gemm_grouped_ws_bytes",
     "w12_gemm_grouped", "w12_gemm_grouped_bf16_ref", "w12_kv_commit", "w12_state_select",
+    "w12_tree_attention_ws_bytes", "w12_tree_attention",
 ]
 
 
@@ -94,6 +95,9 @@ def lib() -> ctypes.CDLL:
                                                 vp, vp]),
             "w12_kv_commit": (i32, [ctypes.POINTER(vp), i32, i32, i64, i64, vp, vp, i32, vp, vp, vp, vp]),
             "w12_state_select": (i32, [vp, i32, i32, i64, vp, i32, vp, vp, vp, vp]),
+            "w12_tree_attention_ws_bytes": (sz, [i32, i32, i32, i32, i64]),
+            "w12_tree_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i64, i64, vp, vp, ctypes.c_float, vp,
+                                         vp, sz, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -354,6 +358,51 @@ def state_select(states: torch.Tensor, path: torch.Tensor, path_len: torch.Tenso
                                   path_len.data_ptr(), out.data_ptr(), _ptr(status), _stream(stream)),
            "w12_state_select")
     return out
+
+
+class TreeAttention:
+    """Tree-masked verify attention with its workspace sized once.
+
+    Q [B, T, Hq, 128] and the caches [B, S_max, Hkv, 128] are bf16 (or 16-bit
+    bit patterns), contiguous; draft node i of request b has its key and value
+    at position prefix_len[b] + i. ``max_kv_len`` bounds prefix_len[b] + T over
+    the requests (default S_max); the work is planned for it.
+    """
+
+    def __init__(self, B: int, T: int, Hq: int, Hkv: int, S_max: int, max_kv_len: int | None = None,
+                 device="cuda"):
+        self.B, self.T, self.Hq, self.Hkv, self.S_max = B, T, Hq, Hkv, S_max
+        self.max_kv_len = S_max if max_kv_len is None else int(max_kv_len)
+        nbytes = lib().w12_tree_attention_ws_bytes(B, T, Hq, Hkv, self.max_kv_len)
+        if nbytes == 0:
+            raise W12Error(2, "w12_tree_attention_ws_bytes")
+        self.ws = torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+
+    def run(self, Q: torch.Tensor, K_cache: torch.Tensor, V_cache: torch.Tensor, prefix_len: torch.Tensor,
+            parents: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,
+            status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        Q, K_cache, V_cache = _bits16(Q), _bits16(K_cache), _bits16(V_cache)
+        B, T, Hq, d = Q.shape
+        if (B, T, Hq) != (self.B, self.T, self.Hq) or tuple(K_cache.shape) != (B, self.S_max, self.Hkv, d) \
+                or K_cache.shape != V_cache.shape:
+            raise ValueError("Q [B, T, Hq, d] and caches [B, S_max, Hkv, d] must match the planned shape")
+        if out is None:
+            out = torch.empty_like(Q)
+        scale = d ** -0.5 if scale is None else float(scale)
+        _check(lib().w12_tree_attention(Q.data_ptr(), K_cache.data_ptr(), V_cache.data_ptr(), B, T, Hq, self.Hkv,
+                                        d, self.S_max, self.max_kv_len, prefix_len.data_ptr(), parents.data_ptr(),
+                                        scale, out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), _ptr(status),
+                                        _stream(stream)), "w12_tree_attention")
+        return out
+
+
+def tree_attention(Q: torch.Tensor, K_cache: torch.Tensor, V_cache: torch.Tensor, prefix_len: torch.Tensor,
+                   parents: torch.Tensor, scale: float | None = None, max_kv_len: int | None = None,
+                   out: torch.Tensor | None = None, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One call of the tree-masked verify attention (see TreeAttention)."""
+    B, T, Hq, _ = Q.shape
+    a = TreeAttention(B, T, Hq, K_cache.shape[2], K_cache.shape[1], max_kv_len, device=Q.device)
+    return a.run(Q, K_cache, V_cache, prefix_len, parents, scale, out, status, stream)
 
 
 def gemm_bf16_ref(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor | None = None, ws: torch.Tensor | None = None,

@@ -49,3 +49,22 @@ def new_status():
 def status_value(st):
     torch.cuda.synchronize()
     return int(st.item())
+
+
+# Tree attention vs the float64 oracle: P rounded to bf16 for the P.V product
+# (relative error <= 2^-9 per weight) and O rounded to bf16 (<= 2^-9 relative):
+# about 1.6e-3 rms relative in all; an element can be off by 2^-8 of itself.
+ATTN_REL_FRO = 4e-3
+ATTN_MAX_ABS_OVER_RMS = 3e-2
+
+
+def assert_attn_close(O_bits: np.ndarray, O64: np.ndarray, what=""):
+    O = (O_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    err = O - O64
+    rel = np.linalg.norm(err) / max(np.linalg.norm(O64), 1e-300)
+    rms = np.sqrt(np.mean(O64 ** 2))
+    mx = np.abs(err).max()
+    assert np.isfinite(O).all(), f"{what}: non-finite output"
+    assert rel <= ATTN_REL_FRO, f"{what}: rel Frobenius {rel:.3e}"
+    assert mx <= ATTN_MAX_ABS_OVER_RMS * rms, f"{what}: max abs {mx:.3e} vs rms {rms:.3e}"
+    return rel, mx / rms
