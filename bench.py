@@ -587,8 +587,65 @@ def run_sweep(args, local):
     out["kv_commit"] = {"us": us, "caches": n_caches, "requests": Bc, "rows_moved_per_cache": moved,
                         "bytes_moved": 2 * moved * n_caches * 8 * 128 * 2, "accept_path_len": plen.tolist()}
     del caches
+    out["tree_attention"] = attention_sweep(dev, stream, per_launch_ms, hbm_peak, tc_peak)
     print(json.dumps(out), flush=True)
     return 0
+
+
+# Attention of the verify pass (40 query / 8 kv heads x 128, the 27B-class
+# layer's qkv split): 4 requests x 64-node draft trees and 16 requests x
+# 16-token blocks (chain trees), each over an 8192-token committed prefix.
+ATTN_HEADS = (40, 8)
+ATTN_CASES = [("tree_B4_T64_P8192", 4, 64, 8192, "tree"), ("block_B16_T16_P8192", 16, 16, 8192, "chain"),
+              ("tree_B4_T64_P32768", 4, 64, 32768, "tree")]
+
+
+def attention_bytes_flops(B, T, P, Hq, Hkv):
+    """Algorithmic bytes (K and V of every key once, Q, O) and useful flops
+    (QK^T and PV over every query row and key of its request; the masked
+    draft keys counted too, as the kernel computes them)."""
+    L = P + T
+    kv = B * L * Hkv * 128 * 2 * 2
+    qo = 2 * B * T * Hq * 128 * 2
+    flops = 4.0 * B * T * Hq * L * 128
+    return kv + qo, flops
+
+
+def attention_sweep(dev, stream, per_launch_ms, hbm_peak, tc_peak):
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+    Hq, Hkv = ATTN_HEADS
+    res = {}
+    for name, B, T, P, kind in ATTN_CASES:
+        S_max = P + T
+        g = S.rng(S.SEED_ACTIVATIONS, 60 + B)
+        q = torch.empty((B, T, Hq, 128), dtype=torch.bfloat16, device=dev)
+        kc = torch.empty((B, S_max, Hkv, 128), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        torch.manual_seed(60 + B)      # N(0, 1) inputs drawn on the device (seeded)
+        q.normal_()
+        kc.normal_()
+        vc.normal_()
+        if kind == "tree":
+            parents = np.stack([S.random_tree(T, g=g) for _ in range(B)])
+        else:
+            parents = np.tile(np.arange(-1, T - 1), (B, 1))
+        par = torch.from_numpy(parents.astype(np.int32)).to(dev)
+        prefix = torch.full((B,), P, dtype=torch.int32, device=dev)
+        att = w12.TreeAttention(B, T, Hq, Hkv, S_max, device=dev)
+        o = torch.empty_like(q)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        t = per_launch_ms(lambda: att.run(q, kc, vc, prefix, par, out=o, status=st))
+        assert int(st.item()) == 0
+        nbytes, fl = attention_bytes_flops(B, T, P, Hq, Hkv)
+        t_hbm = nbytes / (hbm_peak * 1e9)
+        t_tc = fl / (tc_peak * 1e12)
+        res[name] = {"us": t * 1e3, "gbs": nbytes / (t * 1e-3) / 1e9, "tflops": fl / (t * 1e-3) / 1e12,
+                     "bytes": nbytes, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                     "roofline_us": max(t_hbm, t_tc) * 1e6, "frac_roofline": max(t_hbm, t_tc) / (t * 1e-3)}
+        del q, kc, vc, o, att
+        torch.cuda.empty_cache()
+    return res
 
 
 def main(argv=None):

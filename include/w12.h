@@ -252,7 +252,7 @@ int w12_state_select(const void* states, int B, int T, int64_t row_bytes, const 
  * (parents[b, 0] = -1, 0 <= parents[b, i] < i), prefix_len [B] int32, both
  * device arrays. head_dim must be 128; 1 <= T <= 128; Hq a multiple of Hkv.
  * max_kv_len (host) bounds prefix_len[b] + T over the requests, T <= max_kv_len
- * <= S_max; the work split is planned for it. Cache rows at or past
+ * <= S_max; the work split is planned for it. scale > 0. Cache rows at or past
  * prefix_len[b] + T are never used (they may hold anything). Computes in fp32
  * with P rounded to bf16 for the P.V product and O rounded to bf16.
  * Device-side errors in dev_status: W12_ERR_BAD_TREE (malformed parents; that

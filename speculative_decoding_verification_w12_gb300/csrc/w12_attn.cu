@@ -22,7 +22,7 @@
 //                    cache's head dimension is contiguous), D = O in TMEM.
 // The running maximum m only moves when a block's maximum exceeds it by more
 // than 8 (in log2 units), so P <= 256 and O is rescaled rarely; the output is
-// O / l with l the sum of the rounded P. With several splits each CTA writes
+// O / l with l the fp32 sum of P (P itself enters P V rounded to bf16). With several splits each CTA writes
 // (O, m, l) and attn_combine_kernel merges them.
 //
 // Warp roles (256 threads): warp 0 issues the TMA copies of K and V, warp 1
@@ -47,6 +47,7 @@ constexpr uint32_t kBarOff = kStageOff + uint32_t(kStages) * 2u * kTile;
 constexpr uint32_t kSmemBytes = kBarOff + 128 + 1024;  // barriers + misc + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColP = 256, kColO = 384;
+constexpr int kCtaOverheadBlocks = 4;          // a CTA's start and finish, in key blocks
 constexpr float kRescale = 8.0f;                // log2 growth of the maximum that triggers a rescale
 
 struct AttnParams {
@@ -313,8 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         j = pj;
       }
     }
-    float m_ref = -INFINITY, l = 0.f;
-    const float c = P.c;
+    // Warps whose 32 rows are all padding keep the barrier protocol but skip the math.
+    const bool warp_live = __any_sync(0xFFFFFFFFu, valid);
+    float m_ref = -INFINITY, l = 0.f;   // running maximum (log2 units) and sum of P
+    const float c = P.c;                 // > 0
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
       const int key0 = (j0 + i) * kKeys;
@@ -323,19 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // Keys of this block the row may see: all of the prefix, and the draft
-      // keys of its ancestors; none past the request's keys.
-      uint32_t allow[4];
-      if (key0 + kKeys <= Pb) {
-        allow[0] = allow[1] = allow[2] = allow[3] = valid ? ~0u : 0u;
-      } else {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int lim_w = Pb - key0 - 32 * w;  // keys 32w + k with k < lim_w are prefix keys
-          const uint32_t pre = lim_w >= 32 ? ~0u : lim_w <= 0 ? 0u : ((1u << lim_w) - 1u);
-          const uint32_t tree = bits32(anc, key0 + 32 * w - Pb);
-          allow[w] = valid ? (pre | tree) : 0u;
-        }
+      const bool edge = key0 + kKeys > Pb;  // the block holds draft keys or keys past the request
+      if (edge) {
         // Cache rows past the request's keys may hold anything: zero them in
         // the V stage so that P = 0 never meets a non-finite value.
         const int nval = L - key0;
@@ -356,37 +348,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
       }
-      // Row of S -> scaled, masked scores (log2 units).
-      const uint32_t sc = tmem + lane_off + ((i & 1) ? kColS1 : kColS0);
-      float x[kKeys];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t v[16];
-        tmem_ld16(sc + uint32_t(ch * 16), v);
-        tmem_ld_wait(v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int kk = ch * 16 + k;
-          const bool on = (allow[kk >> 5] >> (kk & 31)) & 1u;
-          x[kk] = on ? __uint_as_float(v[k]) * c : -INFINITY;
-        }
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kKeys; ++k) mx = fmaxf(mx, x[k]);
-      float factor = 1.f;
-      if (mx > m_ref + kRescale) {
-        factor = fast_exp2(m_ref - mx);  // 0 while m_ref = -inf
-        m_ref = mx;
-      }
-      const float mref = m_ref == -INFINITY ? 0.f : m_ref;
+      float factor = 1.f, psum = 0.f;
       uint32_t pw[kKeys / 2];
-      float psum = 0.f;
+      if (warp_live) {
+        // Row of S, all 128 columns in flight at once.
+        const uint32_t sc = tmem + lane_off + ((i & 1) ? kColS1 : kColS0);
+        uint32_t v[kKeys];
 #pragma unroll
-      for (int k = 0; k < kKeys / 2; ++k) {
-        const uint32_t w = pack_bf16x2(fast_exp2(x[2 * k] - mref), fast_exp2(x[2 * k + 1] - mref));
-        pw[k] = w;
-        psum += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+        for (int ch = 0; ch < 8; ++ch) tmem_ld16(sc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
+        tmem_ld_wait128(v);
+        if (edge) {
+          // Keys the row may see: all of the prefix and the draft keys of its
+          // ancestors; none past the request's keys. Others become -inf.
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int lim_w = Pb - key0 - 32 * w;  // keys 32w + k with k < lim_w are prefix keys
+            const uint32_t pre = lim_w >= 32 ? ~0u : lim_w <= 0 ? 0u : ((1u << lim_w) - 1u);
+            const uint32_t allow = valid ? (pre | bits32(anc, key0 + 32 * w - Pb)) : 0u;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (!((allow >> k) & 1u)) v[32 * w + k] = __float_as_uint(-INFINITY);
+          }
+        }
+        // Block maximum with eight independent chains.
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(v[a]);
+#pragma unroll
+        for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(v[k]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+        if (mx > m_ref + kRescale) {
+          factor = fast_exp2(m_ref - mx);  // 0 while m_ref = -inf
+          m_ref = mx;
+        }
+        const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
+        float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kKeys / 2; ++k) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * k]), c, negm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * k + 1]), c, negm));
+          ps8[k & 7] += p0 + p1;
+          pw[k] = pack_bf16x2(p0, p1);
+        }
+        psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       }
       // P (single buffer) and O may be touched only once PV of the previous block is done.
       if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {
@@ -394,70 +399,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      if (i > 0 && factor < 1.f && l > 0.f) {
-        const uint32_t oc = tmem + lane_off + kColO;
+      if (warp_live) {
+        if (i > 0 && factor < 1.f && l > 0.f) {
+          const uint32_t oc = tmem + lane_off + kColO;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[16];
-          tmem_ld16(oc + uint32_t(ch * 16), v);
-          tmem_ld_wait(v);
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t v[16];
+            tmem_ld16(oc + uint32_t(ch * 16), v);
+            tmem_ld_wait(v);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
-          tmem_st16(oc + uint32_t(ch * 16), v);
+            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
+            tmem_st16(oc + uint32_t(ch * 16), v);
+          }
         }
-      }
-      l = l * factor + psum;
-      const uint32_t pc = tmem + lane_off + kColP;
+        l = l * factor + psum;
+        const uint32_t pc = tmem + lane_off + kColP;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = pw[ch * 16 + k];
-        tmem_st16(pc + uint32_t(ch * 16), v);
+        for (int ch = 0; ch < 4; ++ch) tmem_st16(pc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&pw[ch * 16]));
+        tmem_st_wait();
       }
-      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
     }
     // Epilogue: O row (after the last PV) -> output or partial.
-    if (ok && wait(o_done, uint32_t(n - 1) & 1u)) {
+    if (ok && warp_live && wait(o_done, uint32_t(n - 1) & 1u)) {
       tc_fence_after();
       const uint32_t oc = tmem + lane_off + kColO;
-      if (P.nsplit == 1) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint16_t* dst = P.O + ((size_t(b) * T + t) * P.Hq + size_t(g) * P.G + hh) * kD;
+      uint32_t v[kD];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[16];
-          tmem_ld16(oc + uint32_t(ch * 16), v);
-          tmem_ld_wait(v);
-          uint4 o0, o1;
-          o0.x = pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
-          o0.y = pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-          o0.z = pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
-          o0.w = pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
-          o1.x = pack_bf16x2(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
-          o1.y = pack_bf16x2(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
-          o1.z = pack_bf16x2(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
-          o1.w = pack_bf16x2(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
-          if (valid) {
-            reinterpret_cast<uint4*>(dst)[ch * 2] = o0;
-            reinterpret_cast<uint4*>(dst)[ch * 2 + 1] = o1;
+      for (int ch = 0; ch < 8; ++ch) tmem_ld16(oc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
+      tmem_ld_wait128(v);
+      if (P.nsplit == 1) {
+        if (valid) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(P.O + ((size_t(b) * T + t) * P.Hq + size_t(g) * P.G + hh) * kD);
+#pragma unroll
+          for (int k = 0; k < kD / 8; ++k) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
+            dst[k] = o;
           }
         }
       } else {
         const size_t prow = (size_t(item) * P.nsplit + split) * 128 + r;
-        float4* dst = reinterpret_cast<float4*>(P.part_o + prow * kD);
+        uint4* dst = reinterpret_cast<uint4*>(P.part_o + prow * kD);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[16];
-          tmem_ld16(oc + uint32_t(ch * 16), v);
-          tmem_ld_wait(v);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[ch * 4 + k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                          __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
-        }
+        for (int k = 0; k < kD / 4; ++k) dst[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         P.part_ml[prow] = make_float2(m_ref, l);
       }
     }
@@ -517,7 +507,8 @@ struct AttnPlan {
 };
 
 // Splits of each (request, kv head, row tile) item's key blocks: the count that
-// minimises waves x blocks per split on `sms` SMs (one CTA per SM), smallest on ties.
+// minimises waves x (blocks per split + a CTA's fixed cost) on `sms` SMs (one
+// CTA per SM), smallest on ties.
 static AttnPlan plan_attn(int B, int T, int Hq, int Hkv, int64_t max_len, int sms) {
   AttnPlan p{};
   const int G = Hq / Hkv;
@@ -528,7 +519,7 @@ static AttnPlan plan_attn(int B, int T, int Hq, int Hkv, int64_t max_len, int sm
   int64_t best_cost = -1;
   for (int s = 1; s <= p.nkb && s <= 64; ++s) {
     const int64_t waves = (p.items * s + sms - 1) / sms;
-    const int64_t cost = waves * ((p.nkb + s - 1) / s);
+    const int64_t cost = waves * ((p.nkb + s - 1) / s + kCtaOverheadBlocks);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;
@@ -573,7 +564,7 @@ int w12_tree_attention(const uint16_t* Q, const uint16_t* K_cache, const uint16_
                        const int32_t* parents, float scale, uint16_t* O, void* ws, size_t ws_bytes,
                        int32_t* dev_status, void* stream) {
   if (!Q || !K_cache || !V_cache || !prefix_len || !parents || !O || !aligned(Q, 16) || !aligned(K_cache, 16) ||
-      !aligned(V_cache, 16) || !aligned(O, 16) || !(scale == scale))
+      !aligned(V_cache, 16) || !aligned(O, 16) || !(scale > 0.f) || scale > 1e30f)
     return W12_ERR_ARG;
   if (!shape_ok(B, T, Hq, Hkv, head_dim, S_max, max_kv_len)) return W12_ERR_SHAPE;
   if (!device_supported()) return W12_ERR_UNSUPPORTED;

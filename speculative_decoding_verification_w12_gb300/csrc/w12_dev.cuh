@@ -233,6 +233,21 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[16]) {
                : "memory");
 }
 
+#define W12_TIE8(v, o)                                                                                   \
+  "+r"(v[o]), "+r"(v[o + 1]), "+r"(v[o + 2]), "+r"(v[o + 3]), "+r"(v[o + 4]), "+r"(v[o + 5]), "+r"(v[o + 6]), \
+      "+r"(v[o + 7])
+
+// Wait for every outstanding tcgen05.ld of this thread; ties all 128 values
+// to the wait (for loads issued as several 16-column pieces).
+__device__ __forceinline__ void tmem_ld_wait128(uint32_t (&v)[128]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : W12_TIE8(v, 0), W12_TIE8(v, 8), W12_TIE8(v, 16), W12_TIE8(v, 24), W12_TIE8(v, 32), W12_TIE8(v, 40),
+                 W12_TIE8(v, 48), W12_TIE8(v, 56), W12_TIE8(v, 64), W12_TIE8(v, 72), W12_TIE8(v, 80),
+                 W12_TIE8(v, 88), W12_TIE8(v, 96), W12_TIE8(v, 104), W12_TIE8(v, 112), W12_TIE8(v, 120)
+               :
+               : "memory");
+}
+
 // Programmatic dependent launch: wait until the grids this launch depends on
 // have completed and their writes are visible (returns at once for an
 // ordinary launch), and allow the next grid on the stream to start launching.

@@ -4,6 +4,8 @@
 
 --op w12 | bf16 | head (fused LM head + greedy accept); --shape one of the
 27B-class layer GEMMs (qkv, o, gate_up, down) or head (5120 -> 151936).
+--op attn runs the tree-masked verify attention (40 q / 8 kv heads x 128) for
+--B requests x --T-node random trees over a --P-token prefix.
 Prints the mean CUDA-event time per launch.
 """
 import argparse
@@ -20,7 +22,10 @@ SHAPES = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (34816, 5120), "dow
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head"])
+    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head", "attn"])
+    ap.add_argument("--B", type=int, default=4)
+    ap.add_argument("--T", type=int, default=64)
+    ap.add_argument("--P", type=int, default=8192)
     ap.add_argument("--shape", default="gate_up", choices=sorted(SHAPES))
     ap.add_argument("--M", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
@@ -31,6 +36,8 @@ def main():
     def d(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
+    if a.op == "attn":
+        return attn(a, dev)
     Wb = d(S.weights_bf16(N, K))
     X = d(S.activations_bf16(a.M, K))
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -60,6 +67,32 @@ def main():
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     print(f"{a.op} {a.shape} M={a.M}: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/launch")
+
+
+def attn(a, dev):
+    Hq, Hkv, S_max = 40, 8, a.P + a.T
+    torch.manual_seed(0)
+    q = torch.randn((a.B, a.T, Hq, 128), device=dev).to(torch.bfloat16)
+    kc = torch.randn((a.B, S_max, Hkv, 128), device=dev).to(torch.bfloat16)
+    vc = torch.randn((a.B, S_max, Hkv, 128), device=dev).to(torch.bfloat16)
+    g = S.rng(S.SEED_TREE, 1)
+    par = torch.from_numpy(np.stack([S.random_tree(a.T, max_depth=min(12, a.T - 1), g=g)
+                                     for _ in range(a.B)]).astype(np.int32)).to(dev)
+    prefix = torch.full((a.B,), a.P, dtype=torch.int32, device=dev)
+    att = w12.TreeAttention(a.B, a.T, Hq, Hkv, S_max, device=dev)
+    o = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    fn = lambda: att.run(q, kc, vc, prefix, par, out=o, status=st)  # noqa: E731
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    print(f"attn B={a.B} T={a.T} P={a.P}: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/launch")
 
 
 if __name__ == "__main__":
