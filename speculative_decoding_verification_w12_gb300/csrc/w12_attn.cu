@@ -16,8 +16,8 @@
 //   S = Q K^T        tcgen05.mma, A = Q (smem), B = K (smem, both K-major),
 //                    D = S in TMEM (double-buffered so S of the next block is
 //                    computed while this one is in the softmax);
-//   P = exp2(c S - m) the softmax warpgroup reads its row of S from TMEM, masks
-//                    it, and writes P as bf16 pairs back into TMEM;
+//   P = exp2(c S - m) the softmax warpgroup reads its row of S from TMEM,
+//                    masks it, and writes P as bf16 pairs back into TMEM;
 //   O += P V         tcgen05.mma, A = P (TMEM), B = V (smem, MN-major: the
 //                    cache's head dimension is contiguous), D = O in TMEM.
 // The running maximum m only moves when a block's maximum exceeds it by more
@@ -25,9 +25,11 @@
 // O / l with l the fp32 sum of P (P itself enters P V rounded to bf16). With several splits each CTA writes
 // (O, m, l) and attn_combine_kernel merges them.
 //
-// Warp roles (256 threads): warp 0 issues the TMA copies of K and V, warp 1
-// allocates TMEM and issues the MMAs, warps 4-7 (a warpgroup: warp w reads
-// TMEM lanes 32 (w % 4) ..) run the softmax and the epilogue; all warps load Q.
+// Warp roles (256 threads): warps 0 and 2 issue the TMA copies of K and of V
+// (separate rings: a K stage frees once S of its block is done, a V stage once
+// P V is), warps 1 and 3 issue the S and the P V MMAs (warp 1 also allocates
+// TMEM), warps 4-7 (a warpgroup: warp w reads TMEM lanes 32 (w % 4) ..) run
+// the softmax and the epilogue. All warps load Q.
 #include "w12_dev.cuh"
 #include "w12_host.h"
 
@@ -37,15 +39,18 @@ namespace attn_impl {
 constexpr int kD = 128;                         // head dimension
 constexpr int kKeys = 128;                      // keys per block
 constexpr int kThreads = 256;
+constexpr int kCombineThreads = 256;            // merge kernel: one warp per output row
 constexpr int kStages = 3;
 constexpr int kMaxT = 128;                      // draft nodes per request
 constexpr uint32_t kHalf = 128u * 128u;         // 128 rows x 64 bf16 (one 128-byte swizzled half)
 constexpr uint32_t kTile = 2u * kHalf;          // 128 rows x 128 bf16
 constexpr uint32_t kQOff = 0;
-constexpr uint32_t kStageOff = kTile;           // stage s: K at kStageOff + s*2*kTile, V right after
-constexpr uint32_t kBarOff = kStageOff + uint32_t(kStages) * 2u * kTile;
-constexpr uint32_t kSmemBytes = kBarOff + 128 + 1024;  // barriers + misc + alignment slack
+constexpr uint32_t kKOff = kTile;                                  // K ring: stage s at kKOff + s * kTile
+constexpr uint32_t kVOff = kKOff + uint32_t(kStages) * kTile;      // V ring
+constexpr uint32_t kBarOff = kVOff + uint32_t(kStages) * kTile;
+constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers + misc + alignment slack
 constexpr uint32_t kTmemCols = 512;
+// TMEM: S of even / odd blocks, P (bf16 pairs) of the current block, O.
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColP = 256, kColO = 384;
 constexpr int kCtaOverheadBlocks = 4;          // a CTA's start and finish, in key blocks
 constexpr float kRescale = 8.0f;                // log2 growth of the maximum that triggers a rescale
@@ -121,13 +126,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ AttnParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* s_full = empty + kStages;  // [2]
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kBarOff);  // K of block i landed (stage i % kStages)
+  uint64_t* kempty = kfull + kStages;                                 // S of the stage's block done
+  uint64_t* vfull = kempty + kStages;                                 // V of block i landed
+  uint64_t* vempty = vfull + kStages;                                 // P V of the stage's block done
+  uint64_t* s_full = vempty + kStages;  // [2]: S of block i in buffer i % 2
+  uint64_t* s_free = s_full + 2;       // [2]: the softmax has read S of block i (buffer i % 2)
+  uint64_t* p_full = s_free + 2;       // P of a block written
+  uint64_t* o_done = p_full + 1;       // P V of a block complete
+  uint64_t* o_final = o_done + 1;      // every MMA of the CTA complete
+  uint32_t* misc = reinterpret_cast<uint32_t*>(o_final + 1);
   volatile uint32_t* tmem_slot = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
@@ -163,14 +171,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
+    mbar_init(&s_free[0], 128);
+    mbar_init(&s_free[1], 128);
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(o_final, 2);  // one commit from each MMA issuer
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -224,72 +236,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA
+    // Warp 0 streams K, warp 2 streams V, each through its own ring: a K stage
+    // frees once S of its block is done, well before P V frees the V stage.
     if (lane == 0) {
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
+      const bool isK = warp == 0;
+      const CUtensorMap* tm = isK ? &tm_k : &tm_v;
+      uint64_t* fullb = isK ? kfull : vfull;
+      uint64_t* emptyb = isK ? kempty : vempty;
+      uint8_t* ring = smem + (isK ? kKOff : kVOff);
+      prefetch_tmap(tm);
       const uint64_t pol = policy_evict_first();
       int issued = 0;
       for (; issued < n; ++issued) {
         const int s = issued % kStages;
-        if (issued >= kStages && !wait(&empty[s], uint32_t((issued / kStages) - 1) & 1u)) break;
-        uint8_t* st = smem + kStageOff + uint32_t(s) * 2u * kTile;
+        if (issued >= kStages && !wait(&emptyb[s], uint32_t((issued / kStages) - 1) & 1u)) break;
+        uint8_t* st = ring + uint32_t(s) * kTile;
         const int key0 = (j0 + issued) * kKeys;
-        mbar_arrive_expect_tx(&full[s], 2u * kTile);
-        tma_load_4d(st, &tm_k, 0, g, key0, b, &full[s], pol);
-        tma_load_4d(st + kHalf, &tm_k, 64, g, key0, b, &full[s], pol);
-        tma_load_4d(st + kTile, &tm_v, 0, g, key0, b, &full[s], pol);
-        tma_load_4d(st + kTile + kHalf, &tm_v, 64, g, key0, b, &full[s], pol);
+        mbar_arrive_expect_tx(&fullb[s], kTile);
+        tma_load_4d(st, tm, 0, g, key0, b, &fullb[s], pol);
+        tma_load_4d(st + kHalf, tm, 64, g, key0, b, &fullb[s], pol);
       }
-      grid_dep_launch();
+      if (isK) grid_dep_launch();
       if (*abort_flag) {
         for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-          mbar_wait(&full[i % kStages], uint32_t(i / kStages) & 1u, lim);
+          mbar_wait(&fullb[i % kStages], uint32_t(i / kStages) & 1u, lim);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------------ MMA
+    // Two issuing threads on different SM sub-partitions: warp 1 issues
+    // S_j = Q K_j^T into TMEM buffer j % 2 as soon as K_j has landed and the
+    // softmax has read S_{j-2} (s_free);
+    // warp 3 issues O += P_i V_i as soon as V_i has landed and P_i is written.
+    // The softmax writes P_{i+1} only after P V_i is complete.
     if (lane == 0) {
+      const uint32_t sbase = smem_u32(smem);
+      const bool is_s = warp == 1;
+      // Descriptors are computed once; a stage or K step only adds a constant
+      // (byte offset >> 4) to the 14-bit start-address field, which cannot
+      // overflow (shared memory < 256 KB).
+      const uint64_t qd = sdesc_k_sw128(sbase + kQOff);
+      const uint64_t kd0 = sdesc_k_sw128(sbase + kKOff);
+      const uint64_t vd0 = sdesc_mn_sw128(sbase + kVOff, kHalf);
       const uint32_t idesc_s = idesc_bf16(128, 128);
       const uint32_t idesc_o = idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
-      const uint32_t sbase = smem_u32(smem);
-      const uint64_t qdesc = sdesc_k_sw128(sbase + kQOff);
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % kStages;
-        if (!wait(&full[s], uint32_t(i / kStages) & 1u)) return false;
-        tc_fence_after();
-        const uint32_t kaddr = sbase + kStageOff + uint32_t(s) * 2u * kTile;
-        const uint64_t kdesc = sdesc_k_sw128(kaddr);
-        const uint32_t d = tmem + ((i & 1) ? kColS1 : kColS0);
+      for (int j = 0; j < n; ++j) {
+        const int s = j % kStages;
+        if (is_s) {
+          if (!wait(&kfull[s], uint32_t(j / kStages) & 1u)) break;
+          if (j >= 2 && !wait(&s_free[j & 1], uint32_t((j - 2) >> 1) & 1u)) break;
+          tc_fence_after();
+          const uint64_t kd = kd0 + uint64_t((uint32_t(s) * kTile) >> 4);
+          const uint32_t d = tmem + ((j & 1) ? kColS1 : kColS0);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t off = uint64_t((uint32_t(ks >> 2) * kHalf + uint32_t(ks & 3) * 32u) >> 4);
-          mma_bf16_ss(d, qdesc + off, kdesc + off, idesc_s, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[i & 1]);
-        return true;
-      };
-      bool ok = issue_s(0);
-      for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n && !issue_s(i + 1)) break;
-        if (!wait(p_full, uint32_t(i) & 1u)) break;
-        tc_fence_after();
-        const int s = i % kStages;
-        const uint32_t vaddr = sbase + kStageOff + uint32_t(s) * 2u * kTile + kTile;
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t off = uint64_t((uint32_t(ks >> 2) * kHalf + uint32_t(ks & 3) * 32u) >> 4);
+            mma_bf16_ss(d, qd + off, kd + off, idesc_s, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[j & 1]);
+          tc_commit(&kempty[s]);
+        } else {
+          if (!wait(&vfull[s], uint32_t(j / kStages) & 1u)) break;
+          if (!wait(p_full, uint32_t(j) & 1u)) break;
+          tc_fence_after();
+          const uint64_t vd = vd0 + uint64_t((uint32_t(s) * kTile) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t bdesc = sdesc_mn_sw128(vaddr + uint32_t(ks) * 2048u, kHalf);
-          mma_bf16_ts(tmem + kColO, tmem + kColP + uint32_t(ks) * 8u, bdesc, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks) {
+            // Keys 16ks ..: V rows 128 bytes apart (the dims' second half kHalf further).
+            mma_bf16_ts(tmem + kColO, tmem + kColP + uint32_t(ks * 8), vd + uint64_t((uint32_t(ks) * 2048u) >> 4),
+                        idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(o_done);
+          tc_commit(&vempty[s]);
         }
-        tc_commit(o_done);
-        tc_commit(&empty[s]);
       }
-      tc_commit(drain);
-      mbar_wait(drain, 0, lim);
+      tc_commit(o_final);  // also drains this thread's MMAs before TMEM is released
+      mbar_wait(o_final, 0, lim);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------ softmax, epilogue
+    // Warp w handles rows 32 (w % 4) .. of the tile (its TMEM lanes), one row
+    // per thread, all 128 keys of every block.
     const int q = warp & 3;
     const int r = q * 32 + lane;                   // row of the tile = TMEM lane
     const int rr = tile * 128 + r;
@@ -297,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hh = valid ? rr / T : 0;
     const int t = valid ? rr - hh * T : 0;
     const uint32_t lane_off = uint32_t(q * 32) << 16;
+    const uint32_t o_row = tmem + lane_off + kColO;
     // Ancestors of node t (itself included) as a 128-bit set.
     uint32_t anc[4] = {0u, 0u, 0u, 0u};
     if (valid) {
@@ -326,19 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const bool edge = key0 + kKeys > Pb;  // the block holds draft keys or keys past the request
+      const bool edge = key0 + kKeys > Pb;  // draft keys or keys past the request
       if (edge) {
         // Cache rows past the request's keys may hold anything: zero them in
         // the V stage so that P = 0 never meets a non-finite value.
         const int nval = L - key0;
         if (nval < kKeys) {
           const int s = i % kStages;
-          if (!wait(&full[s], uint32_t(i / kStages) & 1u)) {
+          if (!wait(&vfull[s], uint32_t(i / kStages) & 1u)) {
             ok = false;
             break;
           }
           if (r >= nval) {
-            uint8_t* vrow = smem + kStageOff + uint32_t(s) * 2u * kTile + kTile + uint32_t(r) * 128u;
+            uint8_t* vrow = smem + kVOff + uint32_t(s) * kTile + uint32_t(r) * 128u;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
@@ -348,8 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
       }
-      float factor = 1.f, psum = 0.f;
-      uint32_t pw[kKeys / 2];
       if (warp_live) {
         // Row of S, all 128 columns in flight at once.
         const uint32_t sc = tmem + lane_off + ((i & 1) ? kColS1 : kColS0);
@@ -357,6 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) tmem_ld16(sc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
         tmem_ld_wait128(v);
+        tc_fence_before();
+        mbar_arrive(&s_free[i & 1]);
         if (edge) {
           // Keys the row may see: all of the prefix and the draft keys of its
           // ancestors; none past the request's keys. Others become -inf.
@@ -370,7 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!((allow >> k) & 1u)) v[32 * w + k] = __float_as_uint(-INFINITY);
           }
         }
-        // Block maximum with eight independent chains.
         float mx8[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(v[a]);
@@ -378,12 +407,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(v[k]));
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+        float factor = 1.f;
         if (mx > m_ref + kRescale) {
           factor = fast_exp2(m_ref - mx);  // 0 while m_ref = -inf
           m_ref = mx;
         }
         const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
         float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pw[kKeys / 2];
 #pragma unroll
         for (int k = 0; k < kKeys / 2; ++k) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * k]), c, negm));
@@ -391,43 +422,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           ps8[k & 7] += p0 + p1;
           pw[k] = pack_bf16x2(p0, p1);
         }
-        psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      }
-      // P (single buffer) and O may be touched only once PV of the previous block is done.
-      if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (warp_live) {
-        if (i > 0 && factor < 1.f && l > 0.f) {
-          const uint32_t oc = tmem + lane_off + kColO;
+        const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+        // P (one buffer) and O may be touched only once P V of the previous block is done.
+        if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // Rescale the O row when the maximum moved (warp-uniform: the TMEM
+        // accesses are collective).
+        const bool resc = i > 0 && factor < 1.f && l > 0.f;
+        if (__any_sync(0xFFFFFFFFu, resc)) {
+          const float f = resc ? factor : 1.f;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
-            uint32_t v[16];
-            tmem_ld16(oc + uint32_t(ch * 16), v);
-            tmem_ld_wait(v);
+            uint32_t o[16];
+            tmem_ld16(o_row + uint32_t(ch * 16), o);
+            tmem_ld_wait(o);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
-            tmem_st16(oc + uint32_t(ch * 16), v);
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+            tmem_st16(o_row + uint32_t(ch * 16), o);
           }
         }
         l = l * factor + psum;
-        const uint32_t pc = tmem + lane_off + kColP;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) tmem_st16(pc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&pw[ch * 16]));
+        for (int ch = 0; ch < 4; ++ch)
+          tmem_st16(tmem + lane_off + kColP + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&pw[ch * 16]));
         tmem_st_wait();
+      } else {
+        mbar_arrive(&s_free[i & 1]);
+        if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {  // stay in step with the live warps
+          ok = false;
+          break;
+        }
       }
       tc_fence_before();
       mbar_arrive(p_full);
     }
-    // Epilogue: O row (after the last PV) -> output or partial.
-    if (ok && warp_live && wait(o_done, uint32_t(n - 1) & 1u)) {
+    // Epilogue: O row (after every MMA) -> output or partial.
+    if (ok && warp_live && wait(o_final, 0)) {
       tc_fence_after();
-      const uint32_t oc = tmem + lane_off + kColO;
       uint32_t v[kD];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) tmem_ld16(oc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
+      for (int ch = 0; ch < 8; ++ch) tmem_ld16(o_row + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
       tmem_ld_wait128(v);
       if (P.nsplit == 1) {
         if (valid) {
@@ -463,9 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge the splits of every output row: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 // One warp per output row (b, t, h); lane k owns dims 4k .. 4k+3.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams P) {
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __grid_constant__ AttnParams P) {
   grid_dep_wait();
-  const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int64_t row = int64_t(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t rows = int64_t(P.B) * P.T * P.Hq;
   if (row >= rows) return;
@@ -632,7 +669,8 @@ int w12_tree_attention(const uint16_t* Q, const uint16_t* K_cache, const uint16_
   if (st || pl.nsplit == 1) return st;
   const int64_t rows = int64_t(B) * T * Hq;
   cudaLaunchConfig_t cfg2 = cfg;
-  cfg2.gridDim = dim3(unsigned((rows + 7) / 8));
+  cfg2.gridDim = dim3(unsigned((rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32)));
+  cfg2.blockDim = dim3(kCombineThreads);
   cfg2.dynamicSmemBytes = 0;
   return cuda_status(cudaLaunchKernelEx(&cfg2, attn_combine_kernel, P));
 }
