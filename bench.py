@@ -642,10 +642,31 @@ def attention_sweep(dev, stream, per_launch_ms, hbm_peak, tc_peak):
         t_tc = fl / (tc_peak * 1e12)
         res[name] = {"us": t * 1e3, "gbs": nbytes / (t * 1e-3) / 1e9, "tflops": fl / (t * 1e-3) / 1e12,
                      "bytes": nbytes, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor",
-                     "roofline_us": max(t_hbm, t_tc) * 1e6, "frac_roofline": max(t_hbm, t_tc) / (t * 1e-3)}
+                     "roofline_us": max(t_hbm, t_tc) * 1e6, "frac_roofline": max(t_hbm, t_tc) / (t * 1e-3),
+                     "cpu_baseline": attention_cpu_baseline(T, P, kind)}
         del q, kc, vc, o, att
         torch.cuda.empty_cache()
     return res
+
+
+def attention_cpu_baseline(T, P, kind):
+    """The oracle (float64, numpy) on a bounded sample of the same workload:
+    one request and one kv head (its 5 query heads), the full prefix; rate in
+    K/V bytes per second, the unit of the GPU line's "gbs"."""
+    from oracle import w12_oracle as O
+    Hq, Hkv = ATTN_HEADS
+    G = Hq // Hkv
+    Q, K, V = S.attention_inputs_bf16(1, T, P + T, G, 1, 128, tag=70)
+    g = S.rng(S.SEED_TREE, 70)
+    parents = (S.random_tree(T, g=g) if kind == "tree" else np.arange(-1, T - 1))[None, :]
+    prefix = np.array([P])
+    O.tree_attention(Q, K, V, prefix, parents, 128 ** -0.5)
+    t0 = time.perf_counter()
+    O.tree_attention(Q, K, V, prefix, parents, 128 ** -0.5)
+    dt = time.perf_counter() - t0
+    kv = (P + T) * 128 * 2 * 2
+    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"1 request x 1 kv head ({G} query heads) x {T} nodes over {P} prefix keys, float64"}
 
 
 def main(argv=None):
