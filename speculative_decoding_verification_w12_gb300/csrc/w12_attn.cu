@@ -36,6 +36,35 @@
 namespace w12 {
 namespace attn_impl {
 
+// Non-blocking probe of an mbarrier: true if the phase with the given parity
+// has completed (returns at once; mbar_try_wait may suspend the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+#define W12_TIE8(v, o)                                                                                   \
+  "+r"(v[o]), "+r"(v[o + 1]), "+r"(v[o + 2]), "+r"(v[o + 3]), "+r"(v[o + 4]), "+r"(v[o + 5]), "+r"(v[o + 6]), \
+      "+r"(v[o + 7])
+
+// Wait for every outstanding tcgen05.ld of this thread; ties all 128 values
+// to the wait (for loads issued as several 16-column pieces).
+__device__ __forceinline__ void tmem_ld_wait128(uint32_t (&v)[128]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : W12_TIE8(v, 0), W12_TIE8(v, 8), W12_TIE8(v, 16), W12_TIE8(v, 24), W12_TIE8(v, 32), W12_TIE8(v, 40),
+                 W12_TIE8(v, 48), W12_TIE8(v, 56), W12_TIE8(v, 64), W12_TIE8(v, 72), W12_TIE8(v, 80),
+                 W12_TIE8(v, 88), W12_TIE8(v, 96), W12_TIE8(v, 104), W12_TIE8(v, 112), W12_TIE8(v, 120)
+               :
+               : "memory");
+}
+
 constexpr int kD = 128;                         // head dimension
 constexpr int kKeys = 128;                      // keys per block
 constexpr int kThreads = 256;

@@ -62,19 +62,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe of the same condition (returns at once).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait until the phase with the given parity has completed. Bounded: gives up
 // after `limit_ns` of wall time (and after 2^31 polls) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -242,29 +229,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[16]) {
                : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
                  "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
                  "+r"(v[15])
-               :
-               : "memory");
-}
-
-#define W12_TIE8(v, o)                                                                                   \
-  "+r"(v[o]), "+r"(v[o + 1]), "+r"(v[o + 2]), "+r"(v[o + 3]), "+r"(v[o + 4]), "+r"(v[o + 5]), "+r"(v[o + 6]), \
-      "+r"(v[o + 7])
-
-// Wait for every outstanding tcgen05.ld of this thread; ties all 128 values
-// to the wait (for loads issued as several 16-column pieces).
-__device__ __forceinline__ void tmem_ld_wait128(uint32_t (&v)[128]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : W12_TIE8(v, 0), W12_TIE8(v, 8), W12_TIE8(v, 16), W12_TIE8(v, 24), W12_TIE8(v, 32), W12_TIE8(v, 40),
-                 W12_TIE8(v, 48), W12_TIE8(v, 56), W12_TIE8(v, 64), W12_TIE8(v, 72), W12_TIE8(v, 80),
-                 W12_TIE8(v, 88), W12_TIE8(v, 96), W12_TIE8(v, 104), W12_TIE8(v, 112), W12_TIE8(v, 120)
-               :
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld_wait64(uint32_t (&v)[64]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : W12_TIE8(v, 0), W12_TIE8(v, 8), W12_TIE8(v, 16), W12_TIE8(v, 24), W12_TIE8(v, 32), W12_TIE8(v, 40),
-                 W12_TIE8(v, 48), W12_TIE8(v, 56)
                :
                : "memory");
 }
