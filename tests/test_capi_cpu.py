@@ -76,3 +76,36 @@ def test_no_gpu_means_unsupported_not_fallback(L):
     a16 = (a + 15) // 16 * 16
     sizes = w12._Sizes()
     assert L.w12_pack_query(a16, 128, 128, ctypes.byref(sizes), a16, 1024, None) == 8
+
+
+def test_tree_attention_host_validation(L):
+    """Workspace query and argument checks of the verify attention, all on the host."""
+    assert L.w12_tree_attention_ws_bytes(4, 64, 40, 8, 8256) > 0
+    assert L.w12_tree_attention_ws_bytes(4, 129, 40, 8, 8256) == 0      # T > 128
+    assert L.w12_tree_attention_ws_bytes(4, 64, 40, 7, 8256) == 0       # Hq not a multiple of Hkv
+    assert L.w12_tree_attention_ws_bytes(4, 64, 40, 8, 63) == 0         # fewer keys than draft nodes
+    buf = (ctypes.c_uint8 * 4096)()
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    args = dict(B=1, T=16, Hq=10, Hkv=2, hd=128, S=64, L=64, scale=0.1)
+
+    def call(**kw):
+        v = dict(args, **kw)
+        q = kw.get("q", a)
+        return L.w12_tree_attention(q, a, a, v["B"], v["T"], v["Hq"], v["Hkv"], v["hd"], v["S"], v["L"], a, a,
+                                    v["scale"], a, a, 4096, None, None)
+    assert call(q=None) == 1                # null pointer
+    assert call(q=a + 2) == 1               # misaligned
+    assert call(scale=0.0) == 1             # scale must be > 0
+    assert call(scale=float("nan")) == 1
+    assert call(hd=64) == 2                 # head dim 128 only
+    assert call(L=65) == 2                  # max_kv_len > S_max
+    assert call(T=0) == 2
+
+
+def test_tree_attention_without_gpu_is_unsupported(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    buf = (ctypes.c_uint8 * 4096)()
+    a = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert L.w12_tree_attention(a, a, a, 1, 16, 10, 2, 128, 64, 64, a, a, 0.1, a, a, 4096, None, None) == 8
