@@ -136,6 +136,107 @@ __device__ __forceinline__ uint32_t bits32(const uint32_t (&a)[4], int sh) {
   return r == 0 ? lo : (lo >> r) | (hi << (32 - r));
 }
 
+// Ancestors of node t (itself included) in a parent array as a 128-bit set;
+// a malformed parent array sets W12_ERR_BAD_TREE and ends the walk.
+__device__ __forceinline__ void tree_ancestors(const int32_t* pb, int t, int T, uint32_t (&anc)[4], int32_t* status) {
+  anc[0] = anc[1] = anc[2] = anc[3] = 0u;
+  int j = t;
+  for (int step = 0; step <= T && j >= 0; ++step) {
+    const uint32_t bit = 1u << (j & 31);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) anc[w] |= (j >> 5) == w ? bit : 0u;
+    const int pj = pb[j];
+    if ((j == 0) ? (pj != -1) : (pj < 0 || pj >= j)) {
+      set_status(status, W12_ERR_BAD_TREE);
+      break;
+    }
+    j = pj;
+  }
+}
+
+// Scores of keys key0 .. key0+127 that the row may not see become -inf: it
+// sees all of the prefix (keys < Pb) and the draft keys Pb + j of its
+// ancestors j; none past the request's keys.
+__device__ __forceinline__ void mask_block(uint32_t (&v)[kKeys], int key0, int Pb, const uint32_t (&anc)[4],
+                                           bool valid) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int lim_w = Pb - key0 - 32 * w;  // keys 32w + k with k < lim_w are prefix keys
+    const uint32_t pre = lim_w >= 32 ? ~0u : lim_w <= 0 ? 0u : ((1u << lim_w) - 1u);
+    const uint32_t allow = valid ? (pre | bits32(anc, key0 + 32 * w - Pb)) : 0u;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (!((allow >> k) & 1u)) v[32 * w + k] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Maximum of the 128 scores (eight independent chains).
+__device__ __forceinline__ float block_max(const uint32_t (&v)[kKeys]) {
+  float mx8[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(v[a]);
+#pragma unroll
+  for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(v[k]));
+  return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])), fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+}
+
+// P_k = 2^(c s_k + negm), packed as bf16 pairs into v[0 .. 63] in place (pair
+// k overwrites v[k], which pair k/2 has already read); returns the fp32 sum.
+__device__ __forceinline__ float exp_pack(uint32_t (&v)[kKeys], float c, float negm) {
+  float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kKeys / 2; ++k) {
+    const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * k]), c, negm));
+    const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * k + 1]), c, negm));
+    ps8[k & 7] += p0 + p1;
+    v[k] = pack_bf16x2(p0, p1);
+  }
+  return ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+}
+
+// O row *= f (warp-collective: every lane of the warp calls it).
+__device__ __forceinline__ void rescale_row(uint32_t o_row, float f) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t o[16];
+    tmem_ld16(o_row + uint32_t(ch * 16), o);
+    tmem_ld_wait(o);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+    tmem_st16(o_row + uint32_t(ch * 16), o);
+  }
+}
+
+// Epilogue of one row (warp-collective TMEM read): O / l as bf16 into the
+// output (one split), or (O, m, l) into the partial row `prow` (several splits).
+__device__ __forceinline__ void store_row(const AttnParams& P, uint32_t o_row, float m_ref, float l, bool valid,
+                                          int b, int t, int g, int hh, size_t prow) {
+  uint32_t v[kD];
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) tmem_ld16(o_row + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
+  tmem_ld_wait128(v);
+  if (P.nsplit == 1) {
+    if (valid) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(P.O + ((size_t(b) * P.T + t) * P.Hq + size_t(g) * P.G + hh) * kD);
+#pragma unroll
+      for (int k = 0; k < kD / 8; ++k) {
+        uint4 o;
+        o.x = pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
+        o.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
+        o.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
+        o.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
+        dst[k] = o;
+      }
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(P.part_o + prow * kD);
+#pragma unroll
+    for (int k = 0; k < kD / 4; ++k) dst[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    P.part_ml[prow] = make_float2(m_ref, l);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ AttnParams P) {
@@ -342,23 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = valid ? rr - hh * T : 0;
     const uint32_t lane_off = uint32_t(q * 32) << 16;
     const uint32_t o_row = tmem + lane_off + kColO;
-    // Ancestors of node t (itself included) as a 128-bit set.
     uint32_t anc[4] = {0u, 0u, 0u, 0u};
-    if (valid) {
-      const int32_t* pb = P.parents + size_t(b) * T;
-      int j = t;
-      for (int step = 0; step <= T && j >= 0; ++step) {
-        const uint32_t bit = 1u << (j & 31);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) anc[w] |= (j >> 5) == w ? bit : 0u;
-        const int pj = pb[j];
-        if ((j == 0) ? (pj != -1) : (pj < 0 || pj >= j)) {
-          set_status(P.status, W12_ERR_BAD_TREE);
-          break;
-        }
-        j = pj;
-      }
-    }
+    if (valid) tree_ancestors(P.parents + size_t(b) * T, t, T, anc, P.status);
     // Warps whose 32 rows are all padding keep the barrier protocol but skip the math.
     const bool warp_live = __any_sync(0xFFFFFFFFu, valid);
     float m_ref = -INFINITY, l = 0.f;   // running maximum (log2 units) and sum of P
@@ -402,42 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait128(v);
         tc_fence_before();
         mbar_arrive(&s_free[i & 1]);
-        if (edge) {
-          // Keys the row may see: all of the prefix and the draft keys of its
-          // ancestors; none past the request's keys. Others become -inf.
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int lim_w = Pb - key0 - 32 * w;  // keys 32w + k with k < lim_w are prefix keys
-            const uint32_t pre = lim_w >= 32 ? ~0u : lim_w <= 0 ? 0u : ((1u << lim_w) - 1u);
-            const uint32_t allow = valid ? (pre | bits32(anc, key0 + 32 * w - Pb)) : 0u;
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (!((allow >> k) & 1u)) v[32 * w + k] = __float_as_uint(-INFINITY);
-          }
-        }
-        float mx8[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(v[a]);
-#pragma unroll
-        for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(v[k]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+        if (edge) mask_block(v, key0, Pb, anc, valid);
+        const float mx = block_max(v) * c;
         float factor = 1.f;
         if (mx > m_ref + kRescale) {
           factor = fast_exp2(m_ref - mx);  // 0 while m_ref = -inf
           m_ref = mx;
         }
-        const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
-        float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint32_t pw[kKeys / 2];
-#pragma unroll
-        for (int k = 0; k < kKeys / 2; ++k) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * k]), c, negm));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * k + 1]), c, negm));
-          ps8[k & 7] += p0 + p1;
-          pw[k] = pack_bf16x2(p0, p1);
-        }
-        const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+        const float psum = exp_pack(v, c, m_ref == -INFINITY ? 0.f : -m_ref);
         // P (one buffer) and O may be touched only once P V of the previous block is done.
         if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {
           ok = false;
@@ -447,22 +505,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Rescale the O row when the maximum moved (warp-uniform: the TMEM
         // accesses are collective).
         const bool resc = i > 0 && factor < 1.f && l > 0.f;
-        if (__any_sync(0xFFFFFFFFu, resc)) {
-          const float f = resc ? factor : 1.f;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t o[16];
-            tmem_ld16(o_row + uint32_t(ch * 16), o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-            tmem_st16(o_row + uint32_t(ch * 16), o);
-          }
-        }
+        if (__any_sync(0xFFFFFFFFu, resc)) rescale_row(o_row, resc ? factor : 1.f);
         l = l * factor + psum;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
-          tmem_st16(tmem + lane_off + kColP + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&pw[ch * 16]));
+          tmem_st16(tmem + lane_off + kColP + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
         tmem_st_wait();
       } else {
         mbar_arrive(&s_free[i & 1]);
@@ -477,31 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Epilogue: O row (after every MMA) -> output or partial.
     if (ok && warp_live && wait(o_final, 0)) {
       tc_fence_after();
-      uint32_t v[kD];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) tmem_ld16(o_row + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
-      tmem_ld_wait128(v);
-      if (P.nsplit == 1) {
-        if (valid) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          uint4* dst = reinterpret_cast<uint4*>(P.O + ((size_t(b) * T + t) * P.Hq + size_t(g) * P.G + hh) * kD);
-#pragma unroll
-          for (int k = 0; k < kD / 8; ++k) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
-            o.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
-            o.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
-            o.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
-            dst[k] = o;
-          }
-        }
-      } else {
-        const size_t prow = (size_t(item) * P.nsplit + split) * 128 + r;
-        uint4* dst = reinterpret_cast<uint4*>(P.part_o + prow * kD);
-#pragma unroll
-        for (int k = 0; k < kD / 4; ++k) dst[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        P.part_ml[prow] = make_float2(m_ref, l);
-      }
+      store_row(P, o_row, m_ref, l, valid, b, t, g, hh, (size_t(item) * P.nsplit + split) * 128 + r);
     }
   }
 
@@ -555,7 +578,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
 
 struct AttnPlan {
   int ntile, nkb, nsplit, bps;
-  int64_t items;
+  int64_t items;   // (request, kv head, row tile) items, one CTA each per split
 };
 
 // Splits of each (request, kv head, row tile) item's key blocks: the count that
