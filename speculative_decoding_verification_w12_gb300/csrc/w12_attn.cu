@@ -22,8 +22,8 @@
 //                    cache's head dimension is contiguous), D = O in TMEM.
 // The running maximum m only moves when a block's maximum exceeds it by more
 // than 8 (in log2 units), so P <= 256 and O is rescaled rarely; the output is
-// O / l with l the fp32 sum of P (P itself enters P V rounded to bf16). With several splits each CTA writes
-// (O, m, l) and attn_combine_kernel merges them.
+// O / l with l the fp32 sum of P (P itself enters P V rounded to bf16). With
+// several splits each CTA writes (O, m, l) and attn_combine_kernel merges them.
 //
 // Warp roles (256 threads): warps 0 and 2 issue the TMA copies of K and of V
 // (separate rings: a K stage frees once S of its block is done, a V stage once
