@@ -180,18 +180,43 @@ __device__ __forceinline__ float block_max(const uint32_t (&v)[kKeys]) {
   return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])), fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
 }
 
+// Two lanes of fp32 in one instruction (sm_100 family): d = a * b + c and
+// d = a + b, each lane rounded as its scalar form.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // P_k = 2^(c s_k + negm), packed as bf16 pairs into v[0 .. 63] in place (pair
 // k overwrites v[k], which pair k/2 has already read); returns the fp32 sum.
+// The scale and the sum run two lanes per instruction (the softmax is bound
+// by instruction issue, not by the exp2 unit).
 __device__ __forceinline__ float exp_pack(uint32_t (&v)[kKeys], float c, float negm) {
-  float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 c2 = make_float2(c, c), m2 = make_float2(negm, negm);
 #pragma unroll
   for (int k = 0; k < kKeys / 2; ++k) {
-    const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * k]), c, negm));
-    const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * k + 1]), c, negm));
-    ps8[k & 7] += p0 + p1;
-    v[k] = pack_bf16x2(p0, p1);
+    const float2 x = fma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c2, m2);
+    const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+    ps4[k & 3] = add2(ps4[k & 3], p);
+    v[k] = pack_bf16x2(p.x, p.y);
   }
-  return ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+  const float2 s = add2(add2(ps4[0], ps4[1]), add2(ps4[2], ps4[3]));
+  return s.x + s.y;
 }
 
 // O row *= f (warp-collective: every lane of the warp calls it).
