@@ -513,7 +513,19 @@ def run_sweep(args, local):
         del Wb, pk
         torch.cuda.empty_cache()
     V, K = HEAD[1], HEAD[2]
-    head = w12.pack(to_dev_bf16(S.weights_bf16(V, K, seed=S.SEED_WEIGHTS + 10), dev))
+    Wh = to_dev_bf16(S.weights_bf16(V, K, seed=S.SEED_WEIGHTS + 10), dev)
+    head = w12.pack(Wh)
+    # The head shape as a plain GEMM (logits out), W12 against the in-tree BF16
+    # kernel: the largest weight, where the 12/16 byte ratio shows in time.
+    out["head_gemm_m16"] = {}
+    Hs = to_dev_bf16(S.activations_bf16(16, K, tag=19), dev)
+    Ys = torch.empty((16, V), dtype=torch.float32, device=dev)
+    wsg = w12.workspace(w12.gemm_ws_bytes(16, V, K), dev)
+    tw = per_launch_ms(lambda: w12.gemm(Hs, head, Y=Ys, ws=wsg))
+    tb = per_launch_ms(lambda: w12.gemm_bf16_ref(Hs, Wh, Y=Ys, ws=wsg))
+    out["head_gemm_m16"] = {"w12_us": tw * 1e3, "bf16_us": tb * 1e3, "w12_over_bf16": tw / tb,
+                            "w12_gbs": head.nbytes / (tw * 1e-3) / 1e9, "bf16_gbs": V * K * 2 / (tb * 1e-3) / 1e9}
+    del Wh, Hs, Ys, wsg
     torch.cuda.empty_cache()
     for B in (1, 4, 8):
         M = 16 * B
