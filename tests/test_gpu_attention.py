@@ -34,6 +34,8 @@ def _run(Q, K, V, prefix, parents, scale, max_len=None, status=None):
     (1, 128, 2, 2, [129], "tree"),              # T = 128: ancestor sets over four words
     (3, 1, 4, 1, [0, 1, 250], "chain"),         # one node: the root alone
     (2, 33, 7, 7, [127, 128], "tree"),          # block-boundary prefixes, G = 1
+    (2, 48, 10, 2, [300, 61], "tree"),          # 240 rows per kv head: tiles that start and end inside a head
+    (1, 20, 32, 4, [513], "tree"),              # G = 8: 160 rows, a second tile of 32
 ])
 def test_tree_attention_matches_oracle(B, T, Hq, Hkv, prefix, kind):
     prefix = np.array(prefix, dtype=np.int32)
