@@ -223,3 +223,28 @@ def test_fused_greedy_full_head_accept_sweep(B):
         np.testing.assert_array_equal(bonus.cpu().numpy(), eb)
         if not near.any():
             np.testing.assert_array_equal(acc.cpu().numpy(), L)
+
+
+@pytest.mark.parametrize("B", [8, 16])
+def test_fused_greedy_batched_geometric_accepts(B):
+    """Batched blocks (M = 128, 256) through the fused W12 head 5120 -> 151936:
+    per-request accept lengths drawn Geometric(1/7) (mean 6) and planted."""
+    K, V, T = 5120, 151936, 16
+    M = B * T
+    Wh = S.weights_bf16(V, K, seed=91)
+    H = S.activations_bf16(M, K, seed=92 + B)
+    target, gap = _oracle_head_argmax(H, Wh)
+    L = S.accept_lengths_geometric(B, T, tag=B)
+    draft = S.plant_block_drafts(target, B, T, T, L, V, tag=B)
+    head = w12.pack(to_dev_bf16(Wh))
+    st = new_status()
+    acc, bonus, am = w12.verify_greedy_fused(to_dev_bf16(H), head, to_dev_i32(draft), T, status=st)
+    assert status_value(st) == 0
+    am = am.cpu().numpy()
+    near = gap < NEAR_TIE
+    assert np.all((am == target) | near)
+    ea, eb = O.verify_greedy(draft, am, T)
+    np.testing.assert_array_equal(acc.cpu().numpy(), ea)
+    np.testing.assert_array_equal(bonus.cpu().numpy(), eb)
+    if not near.any():
+        np.testing.assert_array_equal(acc.cpu().numpy(), L)
