@@ -527,14 +527,16 @@ def run_sweep(args, local):
                             "w12_gbs": head.nbytes / (tw * 1e-3) / 1e9, "bf16_gbs": V * K * 2 / (tb * 1e-3) / 1e9}
     del Wh, Hs, Ys, wsg
     torch.cuda.empty_cache()
-    for B in (1, 4, 8):
+    for B in (1, 4, 8, 16):
         M = 16 * B
         H = to_dev_bf16(S.activations_bf16(M, K, tag=20 + B), dev)
         ws = w12.workspace(w12.verify_ws_bytes(M, V), dev)
         draft = torch.zeros((B, 16), dtype=torch.int32, device=dev)
         acc, bonus, am = w12.verify_greedy_fused(H, head, draft, 16, ws=ws)
         torch.cuda.synchronize(dev)
-        L = S.accept_lengths_uniform(B, 16, tag=30 + B)
+        # Single requests sweep uniform lengths; batches of 8 and 16 draw them Geometric(1/7) (mean 6).
+        L = (S.accept_lengths_geometric(B, 16, tag=30 + B) if B >= 8
+             else S.accept_lengths_uniform(B, 16, tag=30 + B))
         draft.copy_(torch.from_numpy(S.plant_block_drafts(am.cpu().numpy(), B, 16, 16, L, V)))
         t = per_launch_ms(lambda: w12.verify_greedy_fused(H, head, draft, 16, ws=ws, out=(acc, bonus, am)))
         accepted = int(acc.sum().item()) + int((bonus >= 0).sum().item())
