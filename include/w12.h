@@ -258,7 +258,8 @@ int w12_state_select(const void* states, int B, int T, int64_t row_bytes, const 
  * Device-side errors in dev_status: W12_ERR_BAD_TREE (malformed parents; that
  * request's outputs are unspecified), W12_ERR_ARG (prefix_len[b] < 0 or
  * prefix_len[b] + T > max_kv_len; the request is computed with its prefix
- * clamped into range). Returns W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_WORKSPACE,
+ * clamped into range), W12_ERR_TIMEOUT (a bounded wait gave up; outputs
+ * unspecified). Returns W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_WORKSPACE,
  * W12_ERR_UNSUPPORTED or W12_ERR_CUDA. The workspace (no zero-fill needed) is
  * at least w12_tree_attention_ws_bytes(...) bytes, which is 0 for a shape the
  * call rejects. */
