@@ -42,6 +42,14 @@ namespace attn_impl {
 
 // Wait for every outstanding tcgen05.ld of this thread; ties all 128 values
 // to the wait (for loads issued as several 16-column pieces).
+__device__ __forceinline__ void tmem_ld_wait64(uint32_t (&v)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : W12_TIE8(v, 0), W12_TIE8(v, 8), W12_TIE8(v, 16), W12_TIE8(v, 24), W12_TIE8(v, 32), W12_TIE8(v, 40),
+                 W12_TIE8(v, 48), W12_TIE8(v, 56)
+               :
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait128(uint32_t (&v)[128]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : W12_TIE8(v, 0), W12_TIE8(v, 8), W12_TIE8(v, 16), W12_TIE8(v, 24), W12_TIE8(v, 32), W12_TIE8(v, 40),
@@ -53,7 +61,7 @@ __device__ __forceinline__ void tmem_ld_wait128(uint32_t (&v)[128]) {
 
 constexpr int kD = 128;                         // head dimension
 constexpr int kKeys = 128;                      // keys per block
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kCombineThreads = 256;            // merge kernel: one warp per output row
 constexpr int kStages = 3;
 constexpr int kMaxT = 128;                      // draft nodes per request
@@ -66,7 +74,7 @@ constexpr uint32_t kBarOff = kVOff + uint32_t(kStages) * kTile;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers + misc + alignment slack
 constexpr uint32_t kTmemCols = 512;
 // TMEM: S of even / odd blocks, P (bf16 pairs) of the current block, O.
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColP = 256, kColO = 384;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColOA = 256, kColOB = 384;
 constexpr int kCtaOverheadBlocks = 4;          // a CTA's start and finish, in key blocks
 constexpr float kRescale = 8.0f;                // log2 growth of the maximum that triggers a rescale
 
@@ -157,10 +165,10 @@ __device__ __forceinline__ void tree_ancestors(const int32_t* pb, int t, int T, 
 // Scores of keys key0 .. key0+127 that the row may not see become -inf: it
 // sees all of the prefix (keys < Pb) and the draft keys Pb + j of its
 // ancestors j; none past the request's keys.
-__device__ __forceinline__ void mask_block(uint32_t (&v)[kKeys], int key0, int Pb, const uint32_t (&anc)[4],
-                                           bool valid) {
+template <int N>
+__device__ __forceinline__ void mask_block(uint32_t (&v)[N], int key0, int Pb, const uint32_t (&anc)[4], bool valid) {
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
+  for (int w = 0; w < N / 32; ++w) {
     const int lim_w = Pb - key0 - 32 * w;  // keys 32w + k with k < lim_w are prefix keys
     const uint32_t pre = lim_w >= 32 ? ~0u : lim_w <= 0 ? 0u : ((1u << lim_w) - 1u);
     const uint32_t allow = valid ? (pre | bits32(anc, key0 + 32 * w - Pb)) : 0u;
@@ -170,13 +178,14 @@ __device__ __forceinline__ void mask_block(uint32_t (&v)[kKeys], int key0, int P
   }
 }
 
-// Maximum of the 128 scores (eight independent chains).
-__device__ __forceinline__ float block_max(const uint32_t (&v)[kKeys]) {
+// Maximum of the N scores (eight independent chains).
+template <int N>
+__device__ __forceinline__ float block_max(const uint32_t (&v)[N]) {
   float mx8[8];
 #pragma unroll
   for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(v[a]);
 #pragma unroll
-  for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(v[k]));
+  for (int k = 8; k < N; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], __uint_as_float(v[k]));
   return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])), fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
 }
 
@@ -201,15 +210,16 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return d;
 }
 
-// P_k = 2^(c s_k + negm), packed as bf16 pairs into v[0 .. 63] in place (pair
-// k overwrites v[k], which pair k/2 has already read); returns the fp32 sum.
+// P_k = 2^(c s_k + negm), packed as bf16 pairs into v[0 .. N/2-1] in place
+// (pair k overwrites v[k], which pair k/2 has already read); returns the fp32 sum.
 // The scale and the sum run two lanes per instruction (the softmax is bound
 // by instruction issue, not by the exp2 unit).
-__device__ __forceinline__ float exp_pack(uint32_t (&v)[kKeys], float c, float negm) {
+template <int N>
+__device__ __forceinline__ float exp_pack(uint32_t (&v)[N], float c, float negm) {
   float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   const float2 c2 = make_float2(c, c), m2 = make_float2(negm, negm);
 #pragma unroll
-  for (int k = 0; k < kKeys / 2; ++k) {
+  for (int k = 0; k < N / 2; ++k) {
     const float2 x = fma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c2, m2);
     const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
     ps4[k & 3] = add2(ps4[k & 3], p);
@@ -272,10 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* vfull = kempty + kStages;                                 // V of block i landed
   uint64_t* vempty = vfull + kStages;                                 // P V of the stage's block done
   uint64_t* s_full = vempty + kStages;  // [2]: S of block i in buffer i % 2
-  uint64_t* s_free = s_full + 2;       // [2]: the softmax has read S of block i (buffer i % 2)
-  uint64_t* p_full = s_free + 2;       // P of a block written
-  uint64_t* o_done = p_full + 1;       // P V of a block complete
-  uint64_t* o_final = o_done + 1;      // every MMA of the CTA complete
+  uint64_t* p_full = s_full + 2;        // [2][2]: P of block i (buffer i % 2), key half h
+  uint64_t* o_done = p_full + 4;        // [2]: P V of block i (both halves) complete
+  uint64_t* o_final = o_done + 2;       // every MMA of the CTA complete
   uint32_t* misc = reinterpret_cast<uint32_t*>(o_final + 1);
   volatile uint32_t* tmem_slot = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -317,12 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&s_free[0], 128);
-    mbar_init(&s_free[1], 128);
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&s_full[k], 1);
+      mbar_init(&o_done[k], 1);
+    }
+    for (int k = 0; k < 4; ++k) mbar_init(&p_full[k], 128);
     mbar_init(o_final, 2);  // one commit from each MMA issuer
     *abort_flag = 0;
     fence_barrier_init();
@@ -407,11 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------------ MMA
-    // Two issuing threads on different SM sub-partitions: warp 1 issues
-    // S_j = Q K_j^T into TMEM buffer j % 2 as soon as K_j has landed and the
-    // softmax has read S_{j-2} (s_free);
-    // warp 3 issues O += P_i V_i as soon as V_i has landed and P_i is written.
-    // The softmax writes P_{i+1} only after P V_i is complete.
+    // Two issuing threads on different SM sub-partitions. Warp 1 issues
+    // S_j = Q K_j^T into TMEM buffer j % 2 once K_j has landed and P V of block
+    // j - 2 is complete (its P sits in that buffer). Warp 3 issues, for each
+    // key half h, O_h += P_h V_h once V_j has landed and that half's P is written.
     if (lane == 0) {
       const uint32_t sbase = smem_u32(smem);
       const bool is_s = warp == 1;
@@ -425,31 +432,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
       for (int j = 0; j < n; ++j) {
         const int s = j % kStages;
+        const uint32_t sb = tmem + ((j & 1) ? kColS1 : kColS0);
         if (is_s) {
           if (!wait(&kfull[s], uint32_t(j / kStages) & 1u)) break;
-          if (j >= 2 && !wait(&s_free[j & 1], uint32_t((j - 2) >> 1) & 1u)) break;
+          if (j >= 2 && !wait(&o_done[j & 1], uint32_t((j - 2) >> 1) & 1u)) break;
           tc_fence_after();
           const uint64_t kd = kd0 + uint64_t((uint32_t(s) * kTile) >> 4);
-          const uint32_t d = tmem + ((j & 1) ? kColS1 : kColS0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t off = uint64_t((uint32_t(ks >> 2) * kHalf + uint32_t(ks & 3) * 32u) >> 4);
-            mma_bf16_ss(d, qd + off, kd + off, idesc_s, ks > 0 ? 1u : 0u);
+            mma_bf16_ss(sb, qd + off, kd + off, idesc_s, ks > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[j & 1]);
           tc_commit(&kempty[s]);
         } else {
           if (!wait(&vfull[s], uint32_t(j / kStages) & 1u)) break;
-          if (!wait(p_full, uint32_t(j) & 1u)) break;
-          tc_fence_after();
           const uint64_t vd = vd0 + uint64_t((uint32_t(s) * kTile) >> 4);
+          bool got = true;
+          for (int h = 0; h < 2; ++h) {
+            if (!wait(&p_full[(j & 1) * 2 + h], uint32_t(j >> 1) & 1u)) {
+              got = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            // Keys 16ks ..: V rows 128 bytes apart (the dims' second half kHalf further).
-            mma_bf16_ts(tmem + kColO, tmem + kColP + uint32_t(ks * 8), vd + uint64_t((uint32_t(ks) * 2048u) >> 4),
-                        idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) {
+              // Keys 64h + 16ks ..: V rows 128 bytes apart (the dims' second half kHalf further);
+              // P_h sits over the first 32 of this half's 64 S columns.
+              const uint64_t off = uint64_t((uint32_t(h) * 8192u + uint32_t(ks) * 2048u) >> 4);
+              mma_bf16_ts(tmem + (h ? kColOB : kColOA), sb + uint32_t(64 * h + 8 * ks), vd + off, idesc_o,
+                          (j > 0 || ks > 0) ? 1u : 0u);
+            }
           }
-          tc_commit(o_done);
+          if (!got) break;
+          tc_commit(&o_done[j & 1]);
           tc_commit(&vempty[s]);
         }
       }
@@ -459,97 +475,137 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------ softmax, epilogue
     // Warp w handles rows 32 (w % 4) .. of the tile (its TMEM lanes), one row
-    // per thread, all 128 keys of every block.
+    // per thread, over the keys of half h = (w - 4) / 4 (64 keys of every
+    // block) with its own running maximum, sum and O accumulator; the two
+    // halves are merged in the epilogue.
     const int q = warp & 3;
+    const int h = (warp - 4) >> 2;
     const int r = q * 32 + lane;                   // row of the tile = TMEM lane
     const int rr = tile * 128 + r;
     const bool valid = rr < Rg;
     const int hh = valid ? rr / T : 0;
     const int t = valid ? rr - hh * T : 0;
     const uint32_t lane_off = uint32_t(q * 32) << 16;
-    const uint32_t o_row = tmem + lane_off + kColO;
+    const uint32_t o_own = tmem + lane_off + (h ? kColOB : kColOA);
     uint32_t anc[4] = {0u, 0u, 0u, 0u};
     if (valid) tree_ancestors(P.parents + size_t(b) * T, t, T, anc, P.status);
     // Warps whose 32 rows are all padding keep the barrier protocol but skip the math.
     const bool warp_live = __any_sync(0xFFFFFFFFu, valid);
-    float m_ref = -INFINITY, l = 0.f;   // running maximum (log2 units) and sum of P
+    float m_ref = -INFINITY, l = 0.f;   // this half's running maximum (log2 units) and sum of P
     const float c = P.c;                 // > 0
     bool ok = true;
-    for (int i = 0; i < n && ok; ++i) {
-      const int key0 = (j0 + i) * kKeys;
+    for (int i = 0; i < n; ++i) {
+      const int kb = (j0 + i) * kKeys + 64 * h;     // first key of this half
       if (!wait(&s_full[i & 1], uint32_t(i >> 1) & 1u)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool edge = key0 + kKeys > Pb;  // draft keys or keys past the request
-      if (edge) {
-        // Cache rows past the request's keys may hold anything: zero them in
-        // the V stage so that P = 0 never meets a non-finite value.
-        const int nval = L - key0;
-        if (nval < kKeys) {
-          const int s = i % kStages;
-          if (!wait(&vfull[s], uint32_t(i / kStages) & 1u)) {
-            ok = false;
-            break;
-          }
-          if (r >= nval) {
-            uint8_t* vrow = smem + kVOff + uint32_t(s) * kTile + uint32_t(r) * 128u;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(vrow + kHalf + k * 16) = make_uint4(0, 0, 0, 0);
-            }
-          }
-          fence_proxy_async_smem();
+      const bool edge = kb + 64 > Pb;               // draft keys or keys past the request
+      if (edge && L - kb < 64) {
+        // Cache rows past the request's keys may hold anything: zero this
+        // half's such rows in the V stage so that P = 0 never meets a
+        // non-finite value (thread r takes row 64h + r / 2, dims half r % 2).
+        const int s = i % kStages;
+        if (!wait(&vfull[s], uint32_t(i / kStages) & 1u)) {
+          ok = false;
+          break;
         }
+        if ((r >> 1) >= L - kb) {
+          uint8_t* vrow = smem + kVOff + uint32_t(s) * kTile + uint32_t(r & 1) * kHalf + uint32_t(kb - (j0 + i) * kKeys + (r >> 1)) * 128u;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(vrow + k * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
       }
       if (warp_live) {
-        // Row of S, all 128 columns in flight at once.
-        const uint32_t sc = tmem + lane_off + ((i & 1) ? kColS1 : kColS0);
-        uint32_t v[kKeys];
+        const uint32_t sc = tmem + lane_off + ((i & 1) ? kColS1 : kColS0) + uint32_t(64 * h);
+        uint32_t v[64];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) tmem_ld16(sc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
-        tmem_ld_wait128(v);
-        tc_fence_before();
-        mbar_arrive(&s_free[i & 1]);
-        if (edge) mask_block(v, key0, Pb, anc, valid);
-        const float mx = block_max(v) * c;
+        for (int ch = 0; ch < 4; ++ch) tmem_ld16(sc + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
+        tmem_ld_wait64(v);
+        if (edge) mask_block<64>(v, kb, Pb, anc, valid);
+        const float mx = block_max<64>(v) * c;
         float factor = 1.f;
         if (mx > m_ref + kRescale) {
           factor = fast_exp2(m_ref - mx);  // 0 while m_ref = -inf
           m_ref = mx;
         }
-        const float psum = exp_pack(v, c, m_ref == -INFINITY ? 0.f : -m_ref);
-        // P (one buffer) and O may be touched only once P V of the previous block is done.
-        if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // Rescale the O row when the maximum moved (warp-uniform: the TMEM
-        // accesses are collective).
+        const float psum = exp_pack<64>(v, c, m_ref == -INFINITY ? 0.f : -m_ref);
+        // Rescale this half's O row when its maximum moved (warp-uniform: the
+        // TMEM accesses are collective), once P V of the previous block is done.
         const bool resc = i > 0 && factor < 1.f && l > 0.f;
-        if (__any_sync(0xFFFFFFFFu, resc)) rescale_row(o_row, resc ? factor : 1.f);
-        l = l * factor + psum;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          tmem_st16(tmem + lane_off + kColP + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
-        tmem_st_wait();
-      } else {
-        mbar_arrive(&s_free[i & 1]);
-        if (i > 0 && !wait(o_done, uint32_t(i - 1) & 1u)) {  // stay in step with the live warps
-          ok = false;
-          break;
+        if (__any_sync(0xFFFFFFFFu, resc)) {
+          if (!wait(&o_done[(i - 1) & 1], uint32_t((i - 1) >> 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          rescale_row(o_own, resc ? factor : 1.f);
         }
+        l = l * factor + psum;
+        // P over the first 32 of this half's S columns (this thread has read them).
+        tmem_st16(sc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        tmem_st16(sc + 16u, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+        tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[(i & 1) * 2 + h]);
     }
-    // Epilogue: O row (after every MMA) -> output or partial.
-    if (ok && warp_live && wait(o_final, 0)) {
+    // Epilogue: merge the halves, O = (2^(ma-M) Oa + 2^(mb-M) Ob) / (2^(ma-M) la + 2^(mb-M) lb).
+    // Every softmax thread reaches the exchange barrier, also after a failed wait.
+    const bool fin = ok && wait(o_final, 0);
+    float2* xch = reinterpret_cast<float2*>(smem + kKOff);  // the K ring is idle once every MMA is done
+    xch[h * 128 + r] = make_float2(m_ref, l);
+    named_bar_sync(1, 256);
+    if (fin && warp_live) {
       tc_fence_after();
-      store_row(P, o_row, m_ref, l, valid, b, t, g, hh, (size_t(item) * P.nsplit + split) * 128 + r);
+      const float2 other = xch[(1 - h) * 128 + r];
+      const float ma = h ? other.x : m_ref, la = h ? other.y : l;
+      const float mb = h ? m_ref : other.x, lb = h ? l : other.y;
+      const float M = fmaxf(ma, mb);
+      const float wa = ma == -INFINITY ? 0.f : fast_exp2(ma - M);
+      const float wb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
+      const float den = wa * la + wb * lb;
+      // This thread writes dims 64h .. 64h+63 of its row.
+      uint32_t v[128];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        tmem_ld16(tmem + lane_off + kColOA + uint32_t(64 * h + ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
+        tmem_ld16(tmem + lane_off + kColOB + uint32_t(64 * h + ch * 16),
+                  *reinterpret_cast<uint32_t(*)[16]>(&v[64 + ch * 16]));
+      }
+      tmem_ld_wait128(v);
+      if (P.nsplit == 1) {
+        if (valid) {
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(P.O + ((size_t(b) * T + t) * P.Hq + size_t(g) * P.G + hh) * kD + 64 * h);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o[e] = (wa * __uint_as_float(v[8 * k + e]) + wb * __uint_as_float(v[64 + 8 * k + e])) * inv;
+            uint4 w;
+            w.x = pack_bf16x2(o[0], o[1]);
+            w.y = pack_bf16x2(o[2], o[3]);
+            w.z = pack_bf16x2(o[4], o[5]);
+            w.w = pack_bf16x2(o[6], o[7]);
+            dst[k] = w;
+          }
+        }
+      } else {
+        const size_t prow = (size_t(item) * P.nsplit + split) * 128 + r;
+        float4* dst = reinterpret_cast<float4*>(P.part_o + prow * kD + 64 * h);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[e] = wa * __uint_as_float(v[4 * k + e]) + wb * __uint_as_float(v[64 + 4 * k + e]);
+          dst[k] = make_float4(o[0], o[1], o[2], o[3]);
+        }
+        if (h == 0) P.part_ml[prow] = make_float2(M, den);
+      }
     }
   }
 
