@@ -16,20 +16,25 @@
 //   S = Q K^T        tcgen05.mma, A = Q (smem), B = K (smem, both K-major),
 //                    D = S in TMEM (double-buffered so S of the next block is
 //                    computed while this one is in the softmax);
-//   P = exp2(c S - m) the softmax warpgroup reads its row of S from TMEM,
-//                    masks it, and writes P as bf16 pairs back into TMEM;
-//   O += P V         tcgen05.mma, A = P (TMEM), B = V (smem, MN-major: the
-//                    cache's head dimension is contiguous), D = O in TMEM.
-// The running maximum m only moves when a block's maximum exceeds it by more
-// than 8 (in log2 units), so P <= 256 and O is rescaled rarely; the output is
-// O / l with l the fp32 sum of P (P itself enters P V rounded to bf16). With
-// several splits each CTA writes (O, m, l) and attn_combine_kernel merges them.
+//   P = exp2(c S - m) two softmax warpgroups, one per 64-key half, read their
+//                    half of each row of S from TMEM, mask it, and write P as
+//                    bf16 pairs over the first 32 of the half's S columns;
+//   O_h += P_h V_h   tcgen05.mma, A = P_h (TMEM), B = V (smem, MN-major: the
+//                    cache's head dimension is contiguous), D = O_h in TMEM,
+//                    one accumulator per half, merged in the epilogue.
+// Each half's running maximum m only moves when a block's maximum exceeds it
+// by more than 8 (in log2 units), so P <= 256 and O_h is rescaled rarely; the
+// output is (sum_h 2^(m_h - M) O_h) / (sum_h 2^(m_h - M) l_h) with l_h the fp32
+// sum of the half's P (P itself enters P V rounded to bf16). With several
+// splits each CTA writes (O, m, l) and attn_combine_kernel merges them.
 //
-// Warp roles (256 threads): warps 0 and 2 issue the TMA copies of K and of V
+// Warp roles (384 threads): warps 0 and 2 issue the TMA copies of K and of V
 // (separate rings: a K stage frees once S of its block is done, a V stage once
 // P V is), warps 1 and 3 issue the S and the P V MMAs (warp 1 also allocates
-// TMEM), warps 4-7 (a warpgroup: warp w reads TMEM lanes 32 (w % 4) ..) run
-// the softmax and the epilogue. All warps load Q.
+// TMEM; S of block j waits for P V of block j - 2, whose P sits in the buffer
+// S overwrites), warps 4-7 and 8-11 (warpgroups: warp w reads TMEM lanes
+// 32 (w % 4) ..) run the softmax of the first and second key half and the
+// epilogue. All warps load Q.
 #include "w12_dev.cuh"
 #include "w12_host.h"
 
