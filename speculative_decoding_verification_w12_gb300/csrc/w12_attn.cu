@@ -78,7 +78,8 @@ constexpr uint32_t kVOff = kKOff + uint32_t(kStages) * kTile;      // V ring
 constexpr uint32_t kBarOff = kVOff + uint32_t(kStages) * kTile;
 constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers + misc + alignment slack
 constexpr uint32_t kTmemCols = 512;
-// TMEM: S of even / odd blocks, P (bf16 pairs) of the current block, O.
+// TMEM: S of even / odd blocks (each key half's P over its first 32 columns),
+// and the O accumulators of the two key halves.
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColOA = 256, kColOB = 384;
 constexpr int kCtaOverheadBlocks = 4;          // a CTA's start and finish, in key blocks
 constexpr float kRescale = 8.0f;                // log2 growth of the maximum that triggers a rescale
