@@ -248,36 +248,6 @@ __device__ __forceinline__ void rescale_row(uint32_t o_row, float f) {
   }
 }
 
-// Epilogue of one row (warp-collective TMEM read): O / l as bf16 into the
-// output (one split), or (O, m, l) into the partial row `prow` (several splits).
-__device__ __forceinline__ void store_row(const AttnParams& P, uint32_t o_row, float m_ref, float l, bool valid,
-                                          int b, int t, int g, int hh, size_t prow) {
-  uint32_t v[kD];
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) tmem_ld16(o_row + uint32_t(ch * 16), *reinterpret_cast<uint32_t(*)[16]>(&v[ch * 16]));
-  tmem_ld_wait128(v);
-  if (P.nsplit == 1) {
-    if (valid) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(P.O + ((size_t(b) * P.T + t) * P.Hq + size_t(g) * P.G + hh) * kD);
-#pragma unroll
-      for (int k = 0; k < kD / 8; ++k) {
-        uint4 o;
-        o.x = pack_bf16x2(__uint_as_float(v[8 * k]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
-        o.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
-        o.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
-        o.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
-        dst[k] = o;
-      }
-    }
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(P.part_o + prow * kD);
-#pragma unroll
-    for (int k = 0; k < kD / 4; ++k) dst[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-    P.part_ml[prow] = make_float2(m_ref, l);
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ AttnParams P) {
