@@ -50,6 +50,48 @@ def test_gemm_brute_force_exact_rational():
             assert abs(Y[m, n] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
 
 
+# gemm_rows: the same contraction over explicit bf16 weight rows (used where a
+# test samples output columns of a large GEMM). Pinned on its own, not against
+# gemm: a transposed or mis-sliced operand fails every one of these.
+
+def test_gemm_rows_unit_rows_select_x_columns_exactly():
+    M, K = 7, 300                                     # M != n != K, K not a multiple of 128
+    X = S.activations_bf16(M, K, seed=61)
+    cols = np.array([0, 299, 5, 128, 5, 77])          # repeated and unordered picks
+    W = np.zeros((len(cols), K), dtype=np.uint16)
+    W[np.arange(len(cols)), cols] = 0x3F80            # row j = unit vector e_{cols[j]}
+    Y = O.gemm_rows(X, W)
+    assert Y.shape == (M, len(cols))
+    np.testing.assert_array_equal(Y, S.bf16_bits_to_f32(X).astype(np.float64)[:, cols])
+    W[2, cols[2]] = 0xC000                            # -2.0 scales exactly one output column
+    np.testing.assert_array_equal(O.gemm_rows(X, W)[:, 2], -2.0 * S.bf16_bits_to_f32(X)[:, 5].astype(np.float64))
+
+
+def test_gemm_rows_small_integers_exact():
+    g = S.rng(62)
+    M, n, K = 3, 11, 257
+    Xi = g.integers(-8, 9, size=(M, K))
+    Wi = g.integers(-8, 9, size=(n, K))
+    Y = O.gemm_rows(S.f32_to_bf16_bits(Xi.astype(np.float32)), S.f32_to_bf16_bits(Wi.astype(np.float32)))
+    exact = [[sum(int(Xi[m, k]) * int(Wi[j, k]) for k in range(K)) for j in range(n)] for m in range(M)]
+    np.testing.assert_array_equal(Y, np.array(exact, dtype=np.float64))
+
+
+def test_gemm_rows_brute_force_exact_rational_with_specials():
+    M, n, K = 2, 5, 40
+    X = S.activations_bf16(M, K, seed=63)
+    W = S.weights_bf16(128, K, seed=64)[:n].copy()
+    W[0, :4] = [0x0000, 0x8000, 0x0001, 0x807F]       # +0, -0, the smallest subnormal, a negative subnormal
+    W[3, 10] = 0x7F7F                                 # the largest finite bf16
+    Y = O.gemm_rows(X, W)
+    xf = S.bf16_bits_to_f32(X)
+    wf = S.bf16_bits_to_f32(W)
+    for m in range(M):
+        for j in range(n):
+            exact = sum(Fraction(float(xf[m, k])) * Fraction(float(wf[j, k])) for k in range(K))
+            assert abs(Y[m, j] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
+
+
 # ---------------------------------------------------------------------------
 # argmax
 # ---------------------------------------------------------------------------
