@@ -118,8 +118,12 @@ int w12_pack_query(const uint16_t* W, int64_t N, int64_t K, w12_sizes* out,
  * W12_ERR_WORKSPACE if the exceptions exceed the capacity. Synchronises. */
 int w12_pack(const uint16_t* W, int64_t N, int64_t K, const w12_weights* dst, void* stream);
 
-/* Restore bf16 W_out[N, K] bit-exactly from a packed matrix. */
-int w12_unpack(const w12_weights* src, uint16_t* W_out, void* stream);
+/* Restore bf16 W_out[N, K] bit-exactly from a packed matrix. A corrupt
+ * exception CSR (offsets that decrease, an offset past n_exc, or an entry
+ * whose row field is 128 or more) stores W12_ERR_CORRUPT in dev_status
+ * (nullable); the affected block's exceptions are then not applied, and no
+ * store ever lands outside W_out. */
+int w12_unpack(const w12_weights* src, uint16_t* W_out, int32_t* dev_status, void* stream);
 
 /* --- Verify GEMM (SpecPilot digest, summary; "Reasons" bullet 2) -------- */
 
@@ -127,7 +131,10 @@ int w12_unpack(const w12_weights* src, uint16_t* W_out, void* stream);
 size_t w12_gemm_ws_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Y[M, N] (fp32, row-major) = X[M, K] (bf16, row-major) * W^T, W restored
- * from its three planes inside the kernel. X must be 16-byte aligned. */
+ * from its three planes inside the kernel. X must be 16-byte aligned. A
+ * corrupt exception CSR (as for w12_unpack) stores W12_ERR_CORRUPT in
+ * dev_status; the output is then unspecified, and no access leaves the
+ * buffers the descriptor names. */
 int w12_gemm(const uint16_t* X, int64_t M, const w12_weights* W, float* Y,
              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
@@ -140,8 +147,9 @@ int w12_gemm(const uint16_t* X, int64_t M, const w12_weights* W, float* Y,
  * holds in device memory on every GPU where it is loaded, until the process
  * exits. It serves M <= 16 rows, N <= 524288 (4096 tiles of 128), and GPUs
  * with up to 192 SMs; larger shapes return W12_ERR_WORKSPACE (use w12_gemm).
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture. Every
+ * The first call in each CUDA context (the device's primary context, or one
+ * the caller created) looks up the array's device address in that context,
+ * with it current; make that first call before any stream capture. Every
  * call clears the tile counters it uses and allocates nothing. All calls
  * share the one array: calls that overlap on the GPU (other streams, or
  * several host threads) race and corrupt each other's results; serialise

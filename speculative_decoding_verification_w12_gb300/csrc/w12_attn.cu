@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (isK) grid_dep_launch();
       if (*abort_flag) {
         for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-          mbar_wait(&fullb[i % kStages], uint32_t(i / kStages) & 1u, lim);
+          mbar_wait(&fullb[i % kStages], uint32_t(i / kStages) & 1u, drain_limit_ns(lim));
       }
     }
   } else if (warp == 1 || warp == 3) {
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_commit(o_final);  // also drains this thread's MMAs before TMEM is released
-      mbar_wait(o_final, 0, lim);
+      mbar_wait(o_final, 0, drain_limit_ns(lim));
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------ softmax, epilogue
@@ -472,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int kb = (j0 + i) * kKeys + 64 * h;     // first key of this half
-      if (!wait(&s_full[i & 1], uint32_t(i >> 1) & 1u)) {
+      // Waits are one decision per warp: the TMEM loads and stores below are warp-collective.
+      if (!__all_sync(0xFFFFFFFFu, wait(&s_full[i & 1], uint32_t(i >> 1) & 1u))) {
         ok = false;
         break;
       }
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half's such rows in the V stage so that P = 0 never meets a
         // non-finite value (thread r takes row 64h + r / 2, dims half r % 2).
         const int s = i % kStages;
-        if (!wait(&vfull[s], uint32_t(i / kStages) & 1u)) {
+        if (!__all_sync(0xFFFFFFFFu, wait(&vfull[s], uint32_t(i / kStages) & 1u))) {
           ok = false;
           break;
         }
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // TMEM accesses are collective), once P V of the previous block is done.
         const bool resc = i > 0 && factor < 1.f && l > 0.f;
         if (__any_sync(0xFFFFFFFFu, resc)) {
-          if (!wait(&o_done[(i - 1) & 1], uint32_t((i - 1) >> 1) & 1u)) {
+          if (!__all_sync(0xFFFFFFFFu, wait(&o_done[(i - 1) & 1], uint32_t((i - 1) >> 1) & 1u))) {
             ok = false;
             break;
           }
@@ -530,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Epilogue: merge the halves, O = (2^(ma-M) Oa + 2^(mb-M) Ob) / (2^(ma-M) la + 2^(mb-M) lb).
     // Every softmax thread reaches the exchange barrier, also after a failed wait.
-    const bool fin = ok && wait(o_final, 0);
+    const bool fin = __all_sync(0xFFFFFFFFu, ok && wait(o_final, 0));
     float2* xch = reinterpret_cast<float2*>(smem + kKOff);  // the K ring is idle once every MMA is done
     xch[h * 128 + r] = make_float2(m_ref, l);
     named_bar_sync(1, 256);

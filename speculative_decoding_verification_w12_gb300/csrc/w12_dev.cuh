@@ -74,6 +74,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return false;
 }
 
+// Bound for the waits that drain a CTA's own asynchronous work (copies in
+// flight, MMAs issued) before it exits or releases tensor memory. These end
+// within microseconds, but they must not be cut short by a tiny caller limit:
+// a CTA may not exit with copies still landing in its shared memory.
+__device__ __forceinline__ uint64_t drain_limit_ns(uint64_t lim) {
+  return lim > 50000000ull ? lim : 50000000ull;
+}
+
 // ---------------------------------------------------------------------------
 // TMA and bulk copies (global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
@@ -269,6 +277,23 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
 // Named barrier over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier over `nthreads` threads that also returns, to every one of
+// them, whether `pred` held in any. Used to take a wait's outcome as one
+// decision for a group of threads, so that all of them leave a loop at the
+// same barrier count when one of them gives up.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------------------

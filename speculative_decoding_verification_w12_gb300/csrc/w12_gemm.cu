@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       if (*abort_flag) {
         // Let the copies already issued land before the CTA can exit.
         for (int i = issued > S ? issued - S : 0; i < issued; ++i)
-          mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, lim);
+          mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, drain_limit_ns(lim));
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
       // Make sure no MMA is in flight before TMEM is released.
       tc_commit(B.drain);
-      mbar_wait(B.drain, 0, lim);
+      mbar_wait(B.drain, 0, drain_limit_ns(lim));
     }
   } else if (warp == 3) {
     // ---------------------------------------------- exception metadata (W12)
@@ -388,8 +388,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
       bool bad = e1 < e0 || int64_t(e1) > P.n_exc;
       const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
+      constexpr int kBatch = 16;  // entries per lane in flight
+      uint32_t seen = 0;          // OR of the entries' top bits (a row field >= 128 is corrupt)
       if (fits) {
-        constexpr int kBatch = 16;  // entries per lane in flight
         const uint32_t n = e1 - e0;
         for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
           uint32_t v[kBatch];
@@ -398,7 +399,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             if (b0 + lane + 32 * j < n) v[j] = P.exc_ent[e0 + b0 + lane + 32 * j];
 #pragma unroll
           for (int j = 0; j < kBatch; ++j)
-            if (b0 + lane + 32 * j < n) sent[b0 + lane + 32 * j] = v[j];
+            if (b0 + lane + 32 * j < n) {
+              sent[b0 + lane + 32 * j] = v[j];
+              seen |= v[j];
+            }
         }
       }
       __syncwarp();
@@ -409,6 +413,18 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         *ent_end = bad ? e0 : e1;
         mbar_arrive(B.exc_ready);
       }
+      if (!bad && !fits) {
+        // Entries left in global memory: scanned here, off the decoders' path.
+        const uint32_t n = e1 - e0;
+        for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
+          uint32_t v[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) v[j] = (b0 + lane + 32 * j < n) ? __ldg(P.exc_ent + e0 + b0 + lane + 32 * j) : 0u;
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) seen |= v[j];
+        }
+      }
+      if (__any_sync(0xFFFFFFFFu, (seen >> 30) != 0) && lane == 0) set_status(P.status, W12_ERR_CORRUPT);
     }
   } else if (kW12 && warp >= 4 && warp < 4 + C::kDecWarps) {
     // --------------------------------------------------------------- decode
@@ -420,7 +436,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const uint32_t tm_lane = uint32_t(q * 32) << 16;
     const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
     const uint32_t* sent = reinterpret_cast<const uint32_t*>(smem + plan.sent_off);
-    bool ok = wait(B.exc_ready, 0);
+    // Waits are taken as one decision per warp: the loop below uses
+    // warp-collective instructions (shuffles, ballots, tcgen05.st).
+    bool ok = __all_sync(0xFFFFFFFFu, wait(B.exc_ready, 0));
     const bool in_smem = ok && *ent_in_smem;
     const uint32_t e_base = *ent_base;
     const uint32_t e_end = *ent_end;
@@ -444,7 +462,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < kChunksPerThread; ++cc) x.mask[cc] = 0;
       if (nex > 0) {
-        if (uint32_t(lane) < nex) x.ent = in_smem ? sent[x.o0 - e_base + lane] : __ldg(P.exc_ent + x.o0 + lane);
+        if (uint32_t(lane) < nex) {
+          // An entry with a row field of 128 or more is corrupt: it is never
+          // applied (warp 3 reports it).
+          const uint32_t v = in_smem ? sent[x.o0 - e_base + lane] : __ldg(P.exc_ent + x.o0 + lane);
+          x.ent = (v >> 30) ? kInvalidEnt : v;
+        }
         const bool mine = x.ent != kInvalidEnt && ((x.ent >> 28) & 3u) == uint32_t(q);
         const uint32_t ch = (x.ent >> 21) & 3u;
 #pragma unroll
@@ -465,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     for (int i = grp; i < n_units && ok; i += kDecGroups) {
       // Stage s's copies can only have landed after the MMA that last read
       // its TMEM A buffer committed, so the buffer is free once this returns.
-      if (!wait(&B.full[s], ph)) break;
+      if (!__all_sync(0xFFFFFFFFu, wait(&B.full[s], ph))) break;
       tc_fence_after();
       const uint8_t* st = smem + s * plan.stage_bytes;
       const uint8_t* pl = st + row * 64;
@@ -500,7 +523,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           // Rare: more than 32 exceptions in the unit; walk the rest in batches.
           for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
             uint32_t e2 = kInvalidEnt;
-            if (bst + lane < cur.o1) e2 = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
+            if (bst + lane < cur.o1) {
+              const uint32_t v = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
+              e2 = (v >> 30) ? kInvalidEnt : v;
+            }
             const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
             uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
             while (mk2) {
@@ -583,6 +609,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     grid_dep_wait();
     int accb = 0;
     uint32_t accph = 0;
+    int gather_pending = -1;  // phase of a gather of partials that was given up on
     int t = first_tile;
     for (int64_t u = ub; u < ue; ++t) {
       const int64_t seg_begin = u;
@@ -645,7 +672,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           }
         }
       }
-      if (!wait(&B.acc_full[cur], cur_ph)) break;
+      // One decision for the 128 epilogue threads, which meet at named barriers below.
+      if (named_bar_any(kEpiBar, 128, !wait(&B.acc_full[cur], cur_ph))) break;
       tc_fence_after();
       // Issuer k wrote accumulator (cur, k) iff the segment holds a unit i
       // (counted from the CTA's first unit) with i % issuers == k.
@@ -743,7 +771,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
                 ++j;
               }
             }
-            if (!wait(B.gather, gph)) break;
+            if (named_bar_any(kEpiBar, 128, !wait(B.gather, gph))) {
+              gather_pending = int(gph);  // drained before the CTA exits
+              break;
+            }
             gph ^= 1u;
           }
           for (int b2 = 0; b2 < nb; ++b2) {
@@ -780,6 +811,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         named_bar_sync(kEpiBar, 128);
       }
     }
+    // Partials requested into shared memory must land before the CTA exits.
+    if (gather_pending >= 0) mbar_wait(B.gather, uint32_t(gather_pending), drain_limit_ns(lim));
   }
 
   __syncthreads();

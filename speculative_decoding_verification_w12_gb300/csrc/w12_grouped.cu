@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         // loop only stops at a stage boundary with every stage before it
         // fully issued (weights and X).
         for (int i = issued > S ? issued - S : 0; i < issued; ++i) {
-          mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, lim);
-          mbar_wait(&B.full_x[i % S], uint32_t(i / S) & 1u, lim);
+          mbar_wait(&B.full[i % S], uint32_t(i / S) & 1u, drain_limit_ns(lim));
+          mbar_wait(&B.full_x[i % S], uint32_t(i / S) & 1u, drain_limit_ns(lim));
         }
       }
     }
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
       // Make sure no MMA is in flight before TMEM is released.
       tc_commit(B.drain);
-      mbar_wait(B.drain, 0, lim);
+      mbar_wait(B.drain, 0, drain_limit_ns(lim));
     }
   } else if (warp == 3) {
     // ---------------------------------------------- exception metadata (W12)
@@ -615,8 +615,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const uint32_t tm_lane = uint32_t(q * 32) << 16;
     const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
     const uint32_t* sent = reinterpret_cast<const uint32_t*>(smem + plan.sent_off);
-    bool ok = wait(B.exc_ready, 0);
+    // Waits are taken as one decision per warp: the loop below uses
+    // warp-collective instructions (shuffles, ballots, tcgen05.st).
+    bool ok = __all_sync(0xFFFFFFFFu, wait(B.exc_ready, 0));
     const bool in_smem = ok && *ent_in_smem;
+    uint32_t seen = 0;  // OR of the entries read (a row field >= 128 is corrupt)
     const uint32_t e_base = *ent_base;
     const uint32_t e_end = *ent_end;
 
@@ -640,7 +643,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < kChunksPerThread; ++cc) x.mask[cc] = 0;
       if (nex > 0) {
-        if (uint32_t(lane) < nex) x.ent = in_smem ? sent[x.o0 - e_base + lane] : __ldg(pp.exc_ent + x.o0 + lane);
+        if (uint32_t(lane) < nex) {
+          // An entry with a row field of 128 or more is corrupt: never applied,
+          // reported once the loop ends.
+          const uint32_t v = in_smem ? sent[x.o0 - e_base + lane] : __ldg(pp.exc_ent + x.o0 + lane);
+          seen |= v;
+          x.ent = (v >> 30) ? kInvalidEnt : v;
+        }
         const bool mine = x.ent != kInvalidEnt && ((x.ent >> 28) & 3u) == uint32_t(q);
         const uint32_t ch = (x.ent >> 21) & 3u;
 #pragma unroll
@@ -661,7 +670,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     for (int i = grp; i < n_units && ok; i += kDecGroups) {
       // Stage s's copies can only have landed after the MMA that last read
       // its TMEM A buffer committed, so the buffer is free once this returns.
-      if (!wait(&B.full[s], ph)) break;
+      if (!__all_sync(0xFFFFFFFFu, wait(&B.full[s], ph))) break;
       tc_fence_after();
       const uint8_t* st = smem + s * plan.stage_bytes;
       const uint8_t* pl = st + row * 64;
@@ -696,8 +705,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           // Rare: more than 32 exceptions in the unit; walk the rest in batches.
           for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
             uint32_t e2 = kInvalidEnt;
-            if (bst + lane < cur.o1)
-              e2 = in_smem ? sent[bst - e_base + lane] : __ldg(P.pr[single ? 0 : uprob[i]].exc_ent + bst + lane);
+            if (bst + lane < cur.o1) {
+              const uint32_t v =
+                  in_smem ? sent[bst - e_base + lane] : __ldg(P.pr[single ? 0 : uprob[i]].exc_ent + bst + lane);
+              seen |= v;
+              e2 = (v >> 30) ? kInvalidEnt : v;
+            }
             const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
             uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
             while (mk2) {
@@ -720,6 +733,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           ph ^= 1u;
         }
     }
+    if ((seen >> 30) != 0) set_status(P.status, W12_ERR_CORRUPT);
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------- epilogue
     const int ew = warp & 3;            // TMEM lane quarter
@@ -820,6 +834,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     };
     int accb = 0;
     uint32_t accph = 0;
+    int gather_pending = -1;  // phase of a gather of partials that was given up on
     int iseq = 0;  // index of the segment's first unit in the CTA's sequence
     // Walk the CTA's segments (its runs of units of one tile) phase by phase;
     // only (phase, next unit, end of range) is carried between segments.
@@ -925,7 +940,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           }
         }
       }
-      if (!wait(&B.acc_full[cur], cur_ph)) break;
+      // One decision for the 128 epilogue threads, which meet at named barriers below.
+      if (named_bar_any(kEpiBar, 128, !wait(&B.acc_full[cur], cur_ph))) break;
       tc_fence_after();
       // Issuer k wrote accumulator (cur, k) iff the segment holds a unit i
       // (counted from the CTA's first unit) with i % issuers == k.
@@ -1023,7 +1039,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
                 ++j;
               }
             }
-            if (!wait(B.gather, gph)) break;
+            if (named_bar_any(kEpiBar, 128, !wait(B.gather, gph))) {
+              gather_pending = int(gph);  // drained before the CTA exits
+              break;
+            }
             gph ^= 1u;
           }
           for (int b2 = 0; b2 < nb; ++b2) {
@@ -1061,6 +1080,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         if (kMulti && last && pi == P.glu_from) glu_tile_done(t);
       }
     }
+    // Partials requested into shared memory must land before the CTA exits.
+    if (gather_pending >= 0) mbar_wait(B.gather, uint32_t(gather_pending), drain_limit_ns(lim));
   }
 
   __syncthreads();

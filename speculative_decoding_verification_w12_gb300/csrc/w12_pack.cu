@@ -174,6 +174,12 @@ __global__ void __launch_bounds__(128) unpack_exc_kernel(const uint32_t* __restr
   }
   for (uint32_t i = o0 + threadIdx.x; i < o1; i += blockDim.x) {
     const uint32_t e = exc_ent[i];
+    // A valid entry has bits 31..30 clear (row field < 128); anything else
+    // would address a row outside the block, so it is reported, not written.
+    if (e >> 30) {
+      set_status(status, W12_ERR_CORRUPT);
+      continue;
+    }
     const int64_t n = int64_t(bn) * kGroup + (e >> 23);
     const int64_t k = int64_t(bk) * kGroup + ((e >> 16) & 0x7F);
     out[n * K + k] = static_cast<uint16_t>(e & 0xFFFF);
@@ -250,7 +256,7 @@ int w12_pack(const uint16_t* W, int64_t N, int64_t K, const w12_weights* dst, vo
   return cuda_status(cudaStreamSynchronize(s));
 }
 
-int w12_unpack(const w12_weights* src, uint16_t* W_out, void* stream) {
+int w12_unpack(const w12_weights* src, uint16_t* W_out, int32_t* dev_status, void* stream) {
   if (!src || !W_out) return W12_ERR_ARG;
   int st = check_pack_shape(src->N, src->K);
   if (st) return st;
@@ -266,7 +272,7 @@ int w12_unpack(const w12_weights* src, uint16_t* W_out, void* stream) {
   unpack_main_kernel<<<static_cast<unsigned>((groups + 255) / 256), 256, 0, s>>>(src->p0, src->p1, src->p2,
                                                                                 src->ebase, int(N), int(K), W_out);
   unpack_exc_kernel<<<static_cast<unsigned>(U), 128, 0, s>>>(src->exc_off, src->exc_ent, src->n_exc, int(N), int(K),
-                                                            W_out, nullptr);
+                                                            W_out, dev_status);
   return cuda_status(cudaGetLastError());
 }
 

@@ -74,7 +74,7 @@ def lib() -> ctypes.CDLL:
             "w12_pack_ws_bytes": (sz, [i64, i64]),
             "w12_pack_query": (i32, [vp, i64, i64, ctypes.POINTER(_Sizes), vp, sz, vp]),
             "w12_pack": (i32, [vp, i64, i64, ctypes.POINTER(_Weights), vp]),
-            "w12_unpack": (i32, [ctypes.POINTER(_Weights), vp, vp]),
+            "w12_unpack": (i32, [ctypes.POINTER(_Weights), vp, vp, vp]),
             "w12_gemm_ws_bytes": (sz, [i64, i64, i64]),
             "w12_gemm": (i32, [vp, i64, ctypes.POINTER(_Weights), vp, vp, sz, vp, vp]),
             "w12_gemm_bf16_ref": (i32, [vp, i64, vp, i64, i64, vp, vp, sz, vp, vp]),
@@ -194,9 +194,10 @@ def pack(W: torch.Tensor, stream=None) -> W12Weights:
     return out
 
 
-def unpack(w: W12Weights, stream=None) -> torch.Tensor:
+def unpack(w: W12Weights, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 [N, K] restored bit-exactly from a packed matrix."""
     out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=w.p0.device)
-    _check(lib().w12_unpack(ctypes.byref(w.struct()), out.data_ptr(), _stream(stream)), "w12_unpack")
+    _check(lib().w12_unpack(ctypes.byref(w.struct()), out.data_ptr(), _ptr(status), _stream(stream)), "w12_unpack")
     return out
 
 

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.w12_version() == 100
+    assert L.w12_version() == 200
     for code in range(0, 9):
         assert len(w12.status_string(code)) > 0
     assert w12.status_string(6).startswith("a device-side bounded wait")
