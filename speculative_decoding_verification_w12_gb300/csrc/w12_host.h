@@ -29,6 +29,10 @@ int device_sm_count();
 // True if the current device is an sm_103 part this library was built for.
 bool device_supported();
 
+// Unique id of the CUDA context current on this thread (unique for the
+// process lifetime, unlike the context handle). False if none is current.
+bool current_context_id(unsigned long long* id);
+
 // Encode a 2-D tiled tensor map (inner dimension first). Returns false on failure.
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);

@@ -25,27 +25,41 @@ constexpr size_t kNoAllocBytes = kNoAllocCounterBytes + kNoAllocPartBytes;  // 3
 // loads the library holds these bytes until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-// Device address of g_noalloc_scratch on the current device. In host code the
-// array's name only stands in for the symbol, so the address is looked up
-// once per device (with that device current) and cached.
+// Device address of g_noalloc_scratch in the current CUDA context. In host
+// code the array's name only stands in for the symbol, so the address is
+// looked up once per context (with that context current) and cached under the
+// context's unique id: a context created later (cuCtxCreate, or a primary
+// context re-created after cudaDeviceReset) gets its own lookup, never a stale
+// address from another context.
 static int noalloc_scratch(void** out) {
+  struct Entry {
+    unsigned long long ctx;
+    void* addr;
+  };
+  constexpr int kSlots = 64;
   static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  static Entry cache[kSlots];
+  static int used = 0, next = 0;
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
+  std::lock_guard<std::mutex> lock(mu);
+  if (have_id)
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ctx == id) {
+        *out = cache[i].addr;
+        return W12_OK;
+      }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
     cudaGetLastError();
     return W12_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return W12_ERR_CUDA;
-    }
-    addr[dev] = p;
+  if (!have_id) have_id = current_context_id(&id);  // the lookup made the primary context current
+  if (have_id) {
+    const int slot = used < kSlots ? used++ : (next++ % kSlots);
+    cache[slot] = Entry{id, p};
   }
-  *out = addr[dev];
+  *out = p;
   return W12_OK;
 }
 

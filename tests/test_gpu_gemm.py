@@ -100,7 +100,11 @@ def test_repeated_calls_reuse_workspace():
         Y2 = w12.gemm(xd, pk, ws=ws)
     torch.cuda.synchronize()
     assert torch.equal(Y1, Y2)                         # deterministic split-K order
-    assert int(ws.sum().item()) == 0 or True
+    # The split-K tile counters (the first N/128 int32 of the workspace) are
+    # back at zero, so the workspace is ready for the next call; the partial
+    # slots after them may keep data.
+    counters = ws[:4 * (1024 // 128)].view(torch.int32)
+    assert int(counters.abs().sum().item()) == 0
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 7168, 5120), (16, 5120, 17408), (128, 7168, 5120), (256, 5120, 17408)])
@@ -140,10 +144,12 @@ def test_layer_shapes_sampled_columns(name, N, K):
     assert_gemm_close(Y[:, cols], Y64, name)
 
 
-def test_extreme_group_offsets_both_restore_paths():
-    """Rows with offsets above 127 (|w| >= 2^16) use the integer restore, the
-    rest the power-of-two multiply; rows below 2^-112 have offset 0. Checked
-    per row group so small rows are not hidden by large ones."""
+def test_extreme_group_offsets():
+    """Group offsets (ebase) across the exponent range: above 127 (|w| >= 2^16),
+    0 (every value below 2^-112) and near the top (235). The decode adds
+    ebase << 7 to the 11-bit code in integer arithmetic, which must not carry
+    into the sign for any offset. Checked per row group so small rows are
+    not hidden by large ones."""
     W = S.weights_bf16(512, 1024, seed=14)
     Wf = S.bf16_bits_to_f32(W).copy()
     Wf[0:64] *= np.float32(2.0 ** 30)        # offsets ~138
