@@ -64,11 +64,20 @@ def profiled_traffic():
 
 
 def peaks():
+    """(HBM GB/s, sustained bf16 TFLOP/s, source): the denominators for kernels timed inside a long step."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
         return float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
     return 6800.0, 1700.0, "fallback"
+
+
+def burst_tensor_peak():
+    """bf16 TFLOP/s for a kernel timed alone (burst), and its source."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 class Clocks:
@@ -384,6 +393,10 @@ def run_ours(args, world, rank, local):
     bf16_detail["layer_graph_chained"] = chain
     bf16_detail["layer_grouped_launch"] = grp
     del g_ind, g_mlp
+    # Every other workload configuration (tiny, batched layer, head + greedy at M = 16..256, head + tree).
+    tc_burst, _ = burst_tensor_peak()
+    configs = measure_configs(dev, stream, packs, wbf, head, flush_buf, hbm_peak, tc_burst)
+    step_near_ties = near_tie_rows(st.H, head)
     del wbf
 
     if rank != 0:
@@ -406,7 +419,9 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T_BLOCK, "parallelism": f"replicas{world}",
                    "l2": "no flush: 1.67 GB of weights streamed per step > 129 MB L2",
-                   "packed_bytes_per_step": step_bytes, "launch": "CUDA graph of the step's 6 kernels"},
+                   "packed_bytes_per_step": step_bytes,
+                   "launch": f"CUDA graph of the step's {nk} kernels (the layer's 4 GEMMs as one grouped launch, "
+                             "the fused head GEMM, its reduce/accept kernel)"},
         "fraction_of_peak": value / world / hbm_peak,
         "verified_tokens_per_s": world * verified_tokens / (ms * 1e-3),
         "accept_len": accepted,
@@ -419,9 +434,14 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": st.h2d_bytes(), "d2h_bytes_per_step": st.d2h_bytes(), "ms_per_step": e2e_ms},
         "gpu_launches": nk * args.steps,
         "clocks": clk.summary(),
+        "near_tie_rows": {"step": step_near_ties, "rule": "top-2 logit gap < 1e-3 (fp32 logits of the W12 GEMM); "
+                          "counted and reported, not failed", **{k: v["near_tie_rows"] for k, v in configs.items()
+                                                                 if "near_tie_rows" in v}},
         "detail": {"kernel_ms_eager": per, "layer_ms_eager": layer_ms,
                    "layer_gbs_eager": layer_bytes / (layer_ms * 1e-3) / 1e9,
-                   "head_ms": head_ms, "gemm_kernels": bf16_detail},
+                   "head_ms": head_ms, "gemm_kernels": bf16_detail,
+                   "configs": configs, "configs_note": "each launch after an L2 flush; tensor fractions against "
+                   f"the burst bf16 peak {tc_burst} TFLOP/s; HBM fractions against {hbm_peak} GB/s"},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -471,6 +491,167 @@ def cold_launch_ms(fn, flush_buf, stream, dev, reps):
     return statistics.median(a.elapsed_time(b) for a, b in ts)
 
 
+def gemm_roofline(nbytes, flops, ms, hbm_peak, tc_peak):
+    """Achieved rates of one launch against both ceilings; the bound is the larger ideal time."""
+    t = ms * 1e-3
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
+    return {"us": ms * 1e3, "gbs": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak,
+            "tflops": flops / t / 1e12, "frac_tensor": flops / t / 1e12 / tc_peak,
+            "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac_of_bound": max(t_hbm, t_tc) / t}
+
+
+def near_tie_rows(H, head):
+    """Verified rows whose two best logits are within 1e-3 (batched verification may flip such a greedy
+    choice). Counted from the fp32 logits of the W12 GEMM; the parity tests apply the same rule to the
+    float64 logits."""
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+    Y = w12.gemm(H, head)
+    top = torch.topk(Y, 2, dim=1).values
+    n = int(((top[:, 0] - top[:, 1]) < 1e-3).sum().item())
+    del Y
+    return n
+
+
+def head_greedy_case(dev, head, B, geometric, tag, per_launch_ms, hbm_peak, tc_peak):
+    """Fused W12 LM head + row argmax + greedy acceptance of B requests x 16-token blocks, with accept
+    lengths planted against the target's own argmax (uniform 0..16, or Geometric(1/7) with mean 6)."""
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+    M, V, K = 16 * B, head.N, head.K
+    H = to_dev_bf16(S.activations_bf16(M, K, tag=tag), dev)
+    ws = w12.workspace(w12.verify_ws_bytes(M, V), dev)
+    draft = torch.zeros((B, 16), dtype=torch.int32, device=dev)
+    acc, bonus, am = w12.verify_greedy_fused(H, head, draft, 16, ws=ws)
+    torch.cuda.synchronize(dev)
+    L = S.accept_lengths_geometric(B, 16, tag=tag) if geometric else S.accept_lengths_uniform(B, 16, tag=tag)
+    draft.copy_(torch.from_numpy(S.plant_block_drafts(am.cpu().numpy(), B, 16, 16, L, V)))
+    t = per_launch_ms(lambda: w12.verify_greedy_fused(H, head, draft, 16, ws=ws, out=(acc, bonus, am)))
+    accepted = int(acc.sum().item()) + int((bonus >= 0).sum().item())
+    r = gemm_roofline(head.nbytes, 2.0 * M * V * K, t, hbm_peak, tc_peak)
+    r.update({"verified_tokens_per_s": accepted / (t * 1e-3), "accept_len": acc.cpu().tolist(),
+              "planted": L.tolist(), "near_tie_rows": near_tie_rows(H, head), "rows": M})
+    return r
+
+
+def head_tree_case(dev, head, B, T, per_launch_ms, hbm_peak, tc_peak):
+    """Fused W12 LM head + tree acceptance of B causal draft trees of T nodes (one target path planted per
+    tree to a depth drawn uniform 0..12)."""
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+    V, K = head.N, head.K
+    g = S.rng(S.SEED_TREE, 5)
+    parents = np.stack([S.random_tree(T, g=g) for _ in range(B)])
+    H = to_dev_bf16(S.activations_bf16(B * T, K, tag=40), dev)
+    ws = w12.workspace(w12.verify_ws_bytes(B * T, V), dev)
+    par = torch.from_numpy(parents).to(dev)
+    draft = torch.zeros((B, T), dtype=torch.int32, device=dev)
+    _, _, _, _, am = w12.verify_tree_fused(H, head, par, draft, ws=ws)
+    torch.cuda.synchronize(dev)
+    amn = am.cpu().numpy()
+    dr = np.zeros((B, T), dtype=np.int32)
+    Ds = []
+    for b in range(B):
+        D = int(g.integers(0, 13))
+        Ds.append(D)
+        dr[b], _ = S.plant_tree_drafts(parents[b], amn[b * T:(b + 1) * T], D, V, g)
+    draft.copy_(torch.from_numpy(dr))
+    res = {}
+
+    def tree():
+        res["r"] = w12.verify_tree_fused(H, head, par, draft, ws=ws)
+
+    t = per_launch_ms(tree)
+    _, plen, acc, bonus, _ = res["r"]
+    r = gemm_roofline(head.nbytes, 2.0 * B * T * V * K, t, hbm_peak, tc_peak)
+    accepted = int(acc.sum().item()) + int((bonus >= 0).sum().item())
+    r.update({"verified_tokens_per_s": accepted / (t * 1e-3), "accept_len": acc.cpu().tolist(), "planted": Ds,
+              "near_tie_rows": near_tie_rows(H, head), "rows": B * T})
+    return r
+
+
+def layer_batched_case(dev, stream, packs, wbf, M, per_launch_ms, hbm_peak, tc_peak):
+    """The layer's four GEMMs at M verified rows: each launch after an L2 flush, W12 against the in-tree
+    BF16 kernel, and all four as one grouped launch (weights larger than L2, graph replays)."""
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+    out = {"per_gemm": {}}
+    Xs, Ys = [], []
+    for i, ((name, N, K), pk) in enumerate(zip(LAYER, packs)):
+        X = to_dev_bf16(S.activations_bf16(M, K, tag=i), dev)
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ws = w12.workspace(w12.gemm_ws_bytes(M, N, K), dev)
+        fl = 2.0 * M * N * K
+        tw = per_launch_ms(lambda: w12.gemm(X, pk, Y=Y, ws=ws))
+        e = {"w12": gemm_roofline(pk.nbytes, fl, tw, hbm_peak, tc_peak)}
+        if wbf:
+            tb = per_launch_ms(lambda: w12.gemm_bf16_ref(X, wbf[i], Y=Y, ws=ws))
+            e["bf16"] = gemm_roofline(N * K * 2, fl, tb, hbm_peak, tc_peak)
+            e["w12_over_bf16"] = tw / tb
+        out["per_gemm"][name] = e
+        Xs.append(X)
+        Ys.append(Y)
+    fl = sum(2.0 * M * N * K for _, N, K in LAYER)
+    g = w12.Grouped([(x, pk, y) for x, pk, y in zip(Xs, packs, Ys)], M)
+    out["grouped_w12"] = gemm_roofline(sum(pk.nbytes for pk in packs), fl, graph_chain_ms([g.run], dev, stream),
+                                       hbm_peak, tc_peak)
+    if wbf:
+        gb = w12.Grouped([(x, wb, y) for x, wb, y in zip(Xs, wbf, Ys)], M, bf16=True)
+        out["grouped_bf16"] = gemm_roofline(sum(N * K * 2 for _, N, K in LAYER), fl,
+                                            graph_chain_ms([gb.run], dev, stream), hbm_peak, tc_peak)
+        out["grouped_w12_over_bf16"] = out["grouped_w12"]["us"] / out["grouped_bf16"]["us"]
+    return out
+
+
+def tiny_case(dev, per_launch_ms, hbm_peak, tc_peak):
+    """One W12 linear 512 -> 1024 at M = 16, then the verify head 1024 -> 4096 on its output rounded to
+    bf16, with an accept length planted uniform 0..16 against the target's own argmax."""
+    import torch
+    from speculative_decoding_verification_w12_gb300 import w12
+    M, K, N, V = 16, 512, 1024, 4096
+    lin = w12.pack(to_dev_bf16(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS), dev))
+    head = w12.pack(to_dev_bf16(S.weights_bf16(V, N, seed=S.SEED_WEIGHTS + 100), dev))
+    X = to_dev_bf16(S.activations_bf16(M, K), dev)
+    Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    ws = w12.workspace(w12.gemm_ws_bytes(M, N, K), dev)
+    tl = per_launch_ms(lambda: w12.gemm(X, lin, Y=Y, ws=ws))
+    H = Y.to(torch.bfloat16)
+    hws = w12.workspace(w12.verify_ws_bytes(M, V), dev)
+    draft = torch.zeros((1, 16), dtype=torch.int32, device=dev)
+    acc, bonus, am = w12.verify_greedy_fused(H, head, draft, 16, ws=hws)
+    torch.cuda.synchronize(dev)
+    L = S.accept_lengths_uniform(1, 16)
+    draft.copy_(torch.from_numpy(S.plant_block_drafts(am.cpu().numpy(), 1, 16, 16, L, V)))
+    th = per_launch_ms(lambda: w12.verify_greedy_fused(H, head, draft, 16, ws=hws, out=(acc, bonus, am)))
+    return {"linear": gemm_roofline(lin.nbytes, 2.0 * M * N * K, tl, hbm_peak, tc_peak),
+            "head_greedy": gemm_roofline(head.nbytes, 2.0 * M * V * N, th, hbm_peak, tc_peak),
+            "accept_len": acc.cpu().tolist(), "planted": L.tolist(), "near_tie_rows": near_tie_rows(H, head),
+            "note": "0.8 MB + 6.2 MB of weights: launch-latency bound, not a bandwidth figure"}
+
+
+def measure_configs(dev, stream, packs, wbf, head, flush_buf, hbm_peak, tc_peak, reps=10):
+    """Every workload configuration beside the headline step, one timed launch form each, every launch
+    after an L2 flush (a 512 MB read)."""
+    import torch
+
+    def per_launch_ms(fn):
+        return cold_launch_ms(fn, flush_buf, stream, dev, reps)
+
+    out = {"tiny_linear_512x1024_head_4096": tiny_case(dev, per_launch_ms, hbm_peak, tc_peak)}
+    for M in (128, 256):
+        out[f"layer_M{M}"] = layer_batched_case(dev, stream, packs, wbf, M, per_launch_ms, hbm_peak, tc_peak)
+        torch.cuda.empty_cache()
+    for B in (1, 4, 8):
+        out[f"head_greedy_M{16 * B}"] = head_greedy_case(dev, head, B, False, 30 + B, per_launch_ms, hbm_peak,
+                                                         tc_peak)
+    for B in (8, 16):
+        out[f"head_greedy_M{16 * B}_geometric"] = head_greedy_case(dev, head, B, True, 50 + B, per_launch_ms,
+                                                                   hbm_peak, tc_peak)
+    out["head_tree_B4_T64"] = head_tree_case(dev, head, 4, 64, per_launch_ms, hbm_peak, tc_peak)
+    return out
+
+
 def run_sweep(args, local):
     """The other workloads: batched layer GEMMs (M = 16, 128, 256) against the
     BF16 kernel (HBM vs tensor-pipe crossover), the fused head + greedy verify
@@ -483,10 +664,7 @@ def run_sweep(args, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     hbm_peak, _, _ = peaks()
-    tc_peak = 1929.0
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        tc_peak = float(json.load(open(pk_path))["bf16_tflops"])
+    tc_peak, _ = burst_tensor_peak()
 
     flush_buf = torch.zeros(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
@@ -528,51 +706,10 @@ def run_sweep(args, local):
     del Wh, Hs, Ys, wsg
     torch.cuda.empty_cache()
     for B in (1, 4, 8, 16):
-        M = 16 * B
-        H = to_dev_bf16(S.activations_bf16(M, K, tag=20 + B), dev)
-        ws = w12.workspace(w12.verify_ws_bytes(M, V), dev)
-        draft = torch.zeros((B, 16), dtype=torch.int32, device=dev)
-        acc, bonus, am = w12.verify_greedy_fused(H, head, draft, 16, ws=ws)
-        torch.cuda.synchronize(dev)
         # Single requests sweep uniform lengths; batches of 8 and 16 draw them Geometric(1/7) (mean 6).
-        L = (S.accept_lengths_geometric(B, 16, tag=30 + B) if B >= 8
-             else S.accept_lengths_uniform(B, 16, tag=30 + B))
-        draft.copy_(torch.from_numpy(S.plant_block_drafts(am.cpu().numpy(), B, 16, 16, L, V)))
-        t = per_launch_ms(lambda: w12.verify_greedy_fused(H, head, draft, 16, ws=ws, out=(acc, bonus, am)))
-        accepted = int(acc.sum().item()) + int((bonus >= 0).sum().item())
-        out["head_greedy"][f"M{M}"] = {"us": t * 1e3, "gbs": head.nbytes / (t * 1e-3) / 1e9,
-                                       "frac_hbm": head.nbytes / (t * 1e-3) / 1e9 / hbm_peak,
-                                       "verified_tokens_per_s": accepted / (t * 1e-3),
-                                       "accept_len": acc.cpu().tolist(), "planted": L.tolist()}
-    B, T = 4, 64
-    g = S.rng(S.SEED_TREE, 5)
-    parents = np.stack([S.random_tree(T, g=g) for _ in range(B)])
-    H = to_dev_bf16(S.activations_bf16(B * T, K, tag=40), dev)
-    ws = w12.workspace(w12.verify_ws_bytes(B * T, V), dev)
-    par = torch.from_numpy(parents).to(dev)
-    draft = torch.zeros((B, T), dtype=torch.int32, device=dev)
-    _, _, _, _, am = w12.verify_tree_fused(H, head, par, draft, ws=ws)
-    torch.cuda.synchronize(dev)
-    amn = am.cpu().numpy()
-    dr = np.zeros((B, T), dtype=np.int32)
-    Ds = []
-    for b in range(B):
-        D = int(g.integers(0, 13))
-        Ds.append(D)
-        dr[b], _ = S.plant_tree_drafts(parents[b], amn[b * T:(b + 1) * T], D, V, g)
-    draft.copy_(torch.from_numpy(dr))
-    res = {}
-
-    def tree():
-        res["r"] = w12.verify_tree_fused(H, head, par, draft, ws=ws)
-
-    t = per_launch_ms(tree)
-    _, plen, acc, bonus, _ = res["r"]
-    fl = 2.0 * B * T * V * K
-    out["head_tree"] = {"us": t * 1e3, "gbs": head.nbytes / (t * 1e-3) / 1e9,
-                        "frac_hbm": head.nbytes / (t * 1e-3) / 1e9 / hbm_peak,
-                        "tflops": fl / (t * 1e-3) / 1e12, "frac_tensor": fl / (t * 1e-3) / 1e12 / tc_peak,
-                        "accept_len": acc.cpu().tolist(), "planted": Ds}
+        out["head_greedy"][f"M{16 * B}"] = head_greedy_case(dev, head, B, B >= 8, 20 + B, per_launch_ms, hbm_peak,
+                                                            tc_peak)
+    out["head_tree"] = head_tree_case(dev, head, 4, 64, per_launch_ms, hbm_peak, tc_peak)
     # Commit of the accepted tree paths after verification (4 requests, the
     # 4 x 64-node trees above): K and V caches of a 64-layer, 8 kv-head x 128
     # target, 4096 positions each; the moved rows are the accepted paths'.

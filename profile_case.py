@@ -1,20 +1,24 @@
 """Run one verify-path kernel on a seeded workload a few times (for ncu).
 
-  python -m speculative_decoding_verification_w12_gb300.profile_case --op w12 --shape gate_up --M 16 --iters 3
+  python profile_case.py --op w12 --shape gate_up --M 16 --iters 3
 
 --op w12 | bf16 | head (fused LM head + greedy accept); --shape one of the
 27B-class layer GEMMs (qkv, o, gate_up, down) or head (5120 -> 151936).
+--op step replays the benchmarked verify step (layer + fused head) at M = 16.
 --op attn runs the tree-masked verify attention (40 q / 8 kv heads x 128) for
 --B requests x --T-node random trees over a --P-token prefix.
 Prints the mean CUDA-event time per launch.
 """
 import argparse
+import os
+import sys
 
 import numpy as np
 import torch
 
-from . import synthetic as S
-from . import w12
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from speculative_decoding_verification_w12_gb300 import synthetic as S  # noqa: E402
+from speculative_decoding_verification_w12_gb300 import w12  # noqa: E402
 
 SHAPES = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (34816, 5120), "down": (5120, 17408),
           "head": (151936, 5120)}
@@ -22,7 +26,7 @@ SHAPES = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (34816, 5120), "dow
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head", "attn"])
+    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head", "attn", "step"])
     ap.add_argument("--B", type=int, default=4)
     ap.add_argument("--T", type=int, default=64)
     ap.add_argument("--P", type=int, default=8192)
@@ -38,6 +42,8 @@ def main():
 
     if a.op == "attn":
         return attn(a, dev)
+    if a.op == "step":
+        return step(a, dev, d)
     Wb = d(S.weights_bf16(N, K))
     X = d(S.activations_bf16(a.M, K))
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -67,6 +73,30 @@ def main():
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     print(f"{a.op} {a.shape} M={a.M}: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/launch")
+
+
+def step(a, dev, d):
+    """The benchmarked verify step at M = 16: the 27B-class layer's four W12 GEMMs (one grouped launch),
+    the fused W12 LM head and greedy acceptance, replayed as one CUDA graph."""
+    from speculative_decoding_verification_w12_gb300.engine import VerifyStep
+    layers = [w12.pack(d(S.weights_bf16(N, K, seed=S.SEED_WEIGHTS + i)))
+              for i, (N, K) in enumerate(SHAPES[n] for n in ("qkv", "o", "gate_up", "down"))]
+    head = w12.pack(d(S.weights_bf16(*SHAPES["head"], seed=S.SEED_WEIGHTS + 10)))
+    torch.cuda.empty_cache()
+    st = VerifyStep(layers, head, B=1, T=16, device=dev)
+    for i, x in enumerate(st.X):
+        x.copy_(d(S.activations_bf16(16, x.shape[1], tag=i)))
+    st.H.copy_(d(S.activations_bf16(16, SHAPES["head"][1], tag=10)))
+    st.capture()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        st.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
+    print(f"step M=16: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/step ({st.launches} launches per step)")
 
 
 def attn(a, dev):

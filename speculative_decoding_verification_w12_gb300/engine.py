@@ -3,9 +3,11 @@ device buffers, captured once into a CUDA graph and replayed per step.
 
 A verify step at batch B x block T runs each target linear (W12 GEMM) on its
 activation rows and finishes with the fused W12 LM head, row argmax and
-greedy acceptance. Capturing the launches removes per-call host overhead
-(Python, ctypes, argument checks), which otherwise dominates the short
-layer GEMMs at M = 16.
+greedy acceptance. The layer's GEMMs, whose inputs are all given, run as one
+grouped launch (w12_gemm_grouped: one persistent kernel, one ramp-up and one
+tail for all of them) unless grouped=False asks for one launch per GEMM.
+Capturing the launches removes per-call host overhead (Python, ctypes,
+argument checks), which otherwise dominates the short layer GEMMs at M = 16.
 
 Inputs (activations X, hidden states H, draft block) live in one device
 buffer mirrored by one pinned host buffer, and the results (accept_len,
@@ -22,7 +24,7 @@ from . import w12
 
 class VerifyStep:
     def __init__(self, layers: list[w12.W12Weights], head: w12.W12Weights, B: int = 1, T: int = 16,
-                 T_rows: int | None = None, device=None):
+                 T_rows: int | None = None, device=None, grouped: bool = True):
         self.dev = torch.device(device or "cuda")
         self.B, self.T = B, T
         self.T_rows = T if T_rows is None else T_rows
@@ -53,6 +55,10 @@ class VerifyStep:
         self._out_dev = torch.zeros(2 * B + M, dtype=torch.int32, device=self.dev)
         self._out_host = torch.zeros(2 * B + M, dtype=torch.int32).pin_memory()
         self.accept_len, self.bonus, self.argmax = self._out_dev[:B], self._out_dev[B:2 * B], self._out_dev[2 * B:]
+        # All layer GEMMs in one launch (up to 4 per launch).
+        self.groups = ([w12.Grouped([(x, w, y) for x, w, y in zip(self.X[i:i + 4], layers[i:i + 4], self.Y[i:i + 4])],
+                                    M, status=self.status) for i in range(0, len(layers), 4)]
+                       if grouped and layers else None)
         self.graph = None
         self.graph_host = None
 
@@ -63,12 +69,17 @@ class VerifyStep:
 
     @property
     def launches(self) -> int:
-        return len(self.layers) + 2
+        """Kernel launches per step: the layer GEMMs, the fused head GEMM and its reduce/accept kernel."""
+        return (len(self.groups) if self.groups is not None else len(self.layers)) + 2
 
     def run(self):
         """Enqueue one step on the current stream (eager libw12 calls)."""
-        for x, w, y, ws in zip(self.X, self.layers, self.Y, self.ws):
-            w12.gemm(x, w, Y=y, ws=ws, status=self.status)
+        if self.groups is not None:
+            for g in self.groups:
+                g.run()
+        else:
+            for x, w, y, ws in zip(self.X, self.layers, self.Y, self.ws):
+                w12.gemm(x, w, Y=y, ws=ws, status=self.status)
         w12.verify_greedy_fused(self.H, self.head, self.draft, self.T_rows, ws=self.hws, status=self.status,
                                 out=(self.accept_len, self.bonus, self.argmax))
 

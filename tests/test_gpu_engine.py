@@ -5,6 +5,7 @@ import pytest
 import torch
 
 from gpu_util import NEAR_TIE, assert_gemm_close, to_dev_bf16
+from near_ties import block_requests_clear
 from oracle import w12_oracle as O
 from speculative_decoding_verification_w12_gb300 import synthetic as S
 
@@ -46,11 +47,18 @@ def _check(step, Ws, Wh, Xs, H, draft, acc, bonus, am):
     ea, eb = O.verify_greedy(draft, am, T)
     np.testing.assert_array_equal(acc, ea)
     np.testing.assert_array_equal(bonus, eb)
+    # Against the oracle's own argmax, where the deciding rows hold no near tie.
+    ta, tb = O.verify_greedy(draft, target, T)
+    clear = block_requests_clear(near, B, T, ta)
+    np.testing.assert_array_equal(acc[clear], ta[clear])
+    np.testing.assert_array_equal(bonus[clear], tb[clear])
 
 
-def test_host_path_matches_oracle_over_changing_inputs():
+@pytest.mark.parametrize("grouped", [True, False])
+def test_host_path_matches_oracle_over_changing_inputs(grouped):
     Ws, Wh, layers, head = _setup(500)
-    step = engine.VerifyStep(layers, head, B=B, T=T)
+    step = engine.VerifyStep(layers, head, B=B, T=T, grouped=grouped)
+    assert step.launches == (1 if grouped else len(LAYERS)) + 2
     assert int(step.status.item()) == 0
     hX, hH, hdraft = step.host_inputs()
     for it in range(3):
