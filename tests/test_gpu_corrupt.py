@@ -96,21 +96,22 @@ def test_unpack_reports_corrupt_csr(kind):
         np.testing.assert_array_equal(got[in_window], W[in_window])
 
 
+@pytest.mark.parametrize("M", [16, 128])
 @pytest.mark.parametrize("kind", KINDS)
-def test_gemm_reports_corrupt_csr(kind):
+def test_gemm_reports_corrupt_csr(kind, M):
     W = _weights()
     w = _upload(_corrupt(_packed(W), kind))
-    X = to_dev_bf16(S.activations_bf16(16, K, seed=73))
+    X = to_dev_bf16(S.activations_bf16(M, K, seed=73))
     st = new_status()
     Y = w12.gemm(X, w, status=st)
     assert status_value(st) == W12_ERR_CORRUPT
-    assert Y.shape == (16, N)
+    assert Y.shape == (M, N)
     # The context is usable and an intact matrix still multiplies correctly.
     good = _upload(_packed(W))
     st2 = new_status()
     Y2 = w12.gemm(X, good, status=st2).cpu().numpy().astype(np.float64)
     assert status_value(st2) == 0
-    Y64 = O.gemm(S.activations_bf16(16, K, seed=73), _packed(W))
+    Y64 = O.gemm(S.activations_bf16(M, K, seed=73), _packed(W))
     assert np.linalg.norm(Y2 - Y64) / np.linalg.norm(Y64) <= 1e-3
 
 

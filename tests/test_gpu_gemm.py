@@ -72,8 +72,10 @@ def test_split_k_shapes(N, K):
     assert_gemm_close(Yr, Y64, "bf16")
 
 
-def test_exception_heavy_weights():
-    """Dense exceptions: zero groups, >32 exceptions per unit, specials."""
+@pytest.mark.parametrize("M", [16, 128])
+def test_exception_heavy_weights(M):
+    """Dense exceptions: zero groups, >32 exceptions per unit, specials (M=128
+    runs on CTA pairs, whose exception window spans both tiles of a pair)."""
     g = S.rng(5)
     N, K = 512, 1024
     W = S.weights_bf16(N, K, seed=6)
@@ -81,7 +83,7 @@ def test_exception_heavy_weights():
     W[0:128, 0:128] = 0
     W[200, 300:428] = g.integers(1, 0x80, 128)       # subnormals
     W[300, ::3] = 0x0001
-    X = S.activations_bf16(16, K)
+    X = S.activations_bf16(M, K)
     pk = O.pack(W)
     assert pk["n_exc"] > 20000
     Y64 = O.gemm(X, pk)
@@ -178,3 +180,17 @@ def test_batched_layer_shapes_sampled_columns(M, name, N, K):
     assert status_value(st) == 0
     cols = np.unique(np.concatenate([np.arange(0, N, 131), [N - 1]]))
     assert_gemm_close(Y[:, cols], O.gemm_rows(X, W[cols]), f"{name} M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1152, 1280), (200, 1152, 1280), (256, 128, 4096), (96, 640, 4096),
+                                   (128, 25600, 128), (80, 3200, 2048)])
+def test_pair_shapes(M, N, K):
+    """M >= 49 runs on CTA pairs (two 128-row tiles per MMA): odd tile counts
+    (the last pair's second tile lies past N), a single tile, deep and wide
+    shapes, ragged M; W12 and the bf16 kernel against the oracle."""
+    W = S.weights_bf16(N, K, seed=M + N)
+    X = S.activations_bf16(M, K, seed=K + 1)
+    Y64 = O.gemm(X, O.pack(W))
+    Y, Yr = run_both(X, W)
+    assert_gemm_close(Y, Y64, f"w12 M={M} N={N} K={K}")
+    assert_gemm_close(Yr, Y64, f"bf16 M={M} N={N} K={K}")
