@@ -210,8 +210,6 @@ int gemm_shape(int64_t M, int64_t N, int64_t K, GemmShape* s) {
   int sms = device_sm_count();
   if (sms <= 0) sms = 256;  // sizing without a device: an upper bound
   s->grid = static_cast<int>(s->units < sms ? s->units : sms);
-  const int64_t punits = int64_t((s->tiles + 1) / 2) * s->KB;
-  s->pgrid = static_cast<int>(punits < sms / 2 ? punits : sms / 2);
   return W12_OK;
 }
 
@@ -224,9 +222,7 @@ WsLayout ws_layout(const GemmShape& s, int64_t partial_tiles) {
     return at;
   };
   L.counters = take(sizeof(int32_t) * s.tiles);
-  // Two partial slots per CTA: grid CTAs, or pgrid pairs of CTAs.
-  const int ctas = s.grid > 2 * s.pgrid ? s.grid : 2 * s.pgrid;
-  L.parts = take(sizeof(float) * size_t(2) * ctas * s.Mpad * kGroup);
+  L.parts = take(sizeof(float) * size_t(2) * s.grid * s.Mpad * kGroup);
   L.amax_val = take(sizeof(float) * size_t(partial_tiles) * s.Mpad);
   L.amax_idx = take(sizeof(int32_t) * size_t(partial_tiles) * s.Mpad);
   L.argmax = take(sizeof(int32_t) * s.Mpad);
@@ -307,8 +303,7 @@ size_t w12_verify_ws_bytes(int64_t M, int64_t V) {
   int64_t Vr = round_up(V < kGroup ? kGroup : V, kGroup);
   if (gemm_shape(M, Vr, kGroup, &s) != W12_OK) return 0;
   int sms = device_sm_count();
-  s.grid = sms > 0 ? sms : 256;  // the fused head runs one CTA per SM (or one pair per two)
-  s.pgrid = s.grid / 2;
+  s.grid = sms > 0 ? sms : 256;  // the fused head runs one CTA per SM
   int64_t parts = s.tiles;
   return ws_layout(s, parts).total;
 }

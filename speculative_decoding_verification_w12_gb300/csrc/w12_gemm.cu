@@ -50,14 +50,11 @@ constexpr int kAColsPerBuf = 64;      // 128 K values = 64 columns of bf16 pairs
 constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
 constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
-constexpr int kDeferMinMpad = 128;    // from this many padded rows, split tiles are summed by a second kernel
-constexpr int kPairMinMpad = 64;      // from this many padded rows, CTA pairs share each MMA (cta_group::2)
-constexpr int kEntCapPair = 4096;     // exception entries staged per CTA of a pair (its window spans both tiles)
+constexpr int kDeferMinMpad = 128;    // from this many padded rows, split tiles may be summed by a second kernel
 
 struct GemmParams {
   int M, Mpad, N, K, KB, tiles, grid, stages, issuers;
-  int defer;   // split tiles only write their partials; splitk_reduce_kernel sums them
-  int wtiles;  // tiles of the stream-K schedule: 128-row tiles, or 256-row tile pairs for CTA pairs
+  int defer;  // split tiles only write their partials; splitk_reduce_kernel sums them
   int64_t units;
   const uint8_t* ebase;
   const uint32_t* exc_off;
@@ -88,13 +85,12 @@ struct SmemPlan {
   uint32_t scratch_off, red_off, soff_off, sent_off, bar_off, misc_off, total;
 };
 
-template <bool kW12, bool kPair>
+template <bool kW12>
 __host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
   SmemPlan p;
   p.eb_off = Cfg<kW12>::kABytes;
   p.x_off = p.eb_off + Cfg<kW12>::kEbBytes;
-  // X rows per CTA: all Mpad tokens, or half of them in a CTA pair.
-  p.stage_bytes = p.x_off + 2u * uint32_t(kPair ? Mpad / 2 : Mpad) * 128u;
+  p.stage_bytes = p.x_off + 2u * Mpad * 128u;
   p.stages = stages;
   uint32_t off = p.stage_bytes * stages;
   p.scratch_off = off;
@@ -104,7 +100,7 @@ __host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
   p.soff_off = off;
   off += kW12 ? (kOffCap + 4) * 4 : 0;
   p.sent_off = off;
-  off += kW12 ? uint32_t(kPair ? kEntCapPair : kEntCap) * 4 : 0;
+  off += kW12 ? kEntCap * 4 : 0;
   off = (off + 15) & ~15u;
   p.bar_off = off;
   off += 64 * 8;
@@ -132,15 +128,7 @@ struct Bars {
   uint64_t* gather;
 };
 
-// kPair: launched as clusters of two CTAs on neighbouring SMs. The pair takes
-// 256 weight rows (two 128-row tiles, one per CTA) per unit, and each CTA
-// holds half of X's token columns. The first CTA of the pair issues one MMA
-// over both (tcgen05.mma.cta_group::2, M = 256): every X tile is loaded once
-// per 256 weight rows instead of once per 128, which halves the X bytes per
-// stage and deepens the ring at large M. Each CTA decodes its own tile into
-// its own tensor memory; the second CTA's decoders and epilogue arrive on the
-// first CTA's barriers, and the MMA's commits arrive in both CTAs.
-template <bool kW12, bool kArgmax, bool kPair>
+template <bool kW12, bool kArgmax>
 __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                 const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_x,
@@ -148,7 +136,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   using C = Cfg<kW12>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemPlan plan = smem_plan<kW12, kPair>(P.Mpad, P.stages);
+  const SmemPlan plan = smem_plan<kW12>(P.Mpad, P.stages);
   const int S = P.stages;
   const int NACC = P.Mpad <= 128 ? 2 : 1;
 
@@ -174,54 +162,24 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Stream-K worker: this CTA, or this CTA's pair. `rank` is the CTA's place
-  // in the pair; its output tile of worker tile t is 2t + rank.
-  const int rank = kPair ? int(cluster_ctarank()) : 0;
-  const int c = kPair ? int(cluster_id_x()) : int(blockIdx.x);
-  const int cta = kPair ? 2 * c + rank : c;  // owner of the partial slots 2*cta, 2*cta+1
-  const bool leader = rank == 0;             // issues the MMAs
+  const int c = blockIdx.x;
   const int64_t U = P.units;
   const int G = P.grid;
   const int64_t ub = unit_begin(c, U, G), ue = unit_begin(c + 1, U, G);
   const int KB = P.KB;
   const uint64_t lim = P.limit_ns;
-  // Exception blocks of this CTA's units. Without pairs unit i of the range is
-  // block ub + i. In a pair, unit i (worker tile pt0 + q, k-block kb) is block
-  // (2(pt0 + q) + rank) KB + kb: contiguous within a worker tile, skipping the
-  // other CTA's tile between worker tiles. The staged window of offsets runs
-  // from the first unit's block to the last valid unit's block + 1; only the
-  // pair's second tile of the last worker tile can be invalid (odd N/128).
-  const int i0 = int(ub % KB);
-  const int64_t pt0 = ub / KB;
-  int n_valid = int(ue - ub);
-  if (kPair && rank == 1 && (P.tiles & 1)) {
-    const int64_t first_bad = int64_t(P.wtiles - 1) * KB;  // first unit of the last worker tile
-    n_valid = first_bad <= ub ? 0 : int((first_bad < ue ? first_bad : ue) - ub);
-  }
-  auto local_block = [&](int i) -> int {  // block of unit i relative to the first unit's block
-    if constexpr (kPair) {
-      const int qq = (i0 + i) / KB;
-      return 2 * qq * KB + (i0 + i - qq * KB) - i0;
-    } else {
-      return i;
-    }
-  };
-  const int64_t win_b0 = kPair ? (2 * pt0 + rank) * KB + i0 : ub;
-  const int win_n = kPair ? (n_valid > 0 ? local_block(n_valid - 1) + 2 : 0) : int(ue - ub) + 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&B.full[s], 1);
       mbar_init(&B.empty[s], 1);
     }
-    // a_full: decoded (or, for bf16 pairs, landed) A operand of a stage;
-    // in a pair both CTAs arrive on the first CTA's barrier.
-    if (kW12 || kPair) {
-      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], kW12 ? (kPair ? 2 : 1) * 128 * kDecSplit : 2);
+    if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
+      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * kDecSplit);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&B.acc_full[a], P.issuers);  // one commit per MMA issuer per segment
-      mbar_init(&B.acc_empty[a], kPair ? 256 : 128);
+      mbar_init(&B.acc_empty[a], 128);
     }
     mbar_init(B.exc_ready, 1);
     mbar_init(B.drain, P.issuers);
@@ -231,18 +189,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 2) {
-    if constexpr (kPair) {
-      tmem_alloc_pair(const_cast<uint32_t*>(tmem_slot), C::kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(const_cast<uint32_t*>(tmem_slot), C::kTmemCols);
-      tmem_relinquish();
-    }
+    tmem_alloc(const_cast<uint32_t*>(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
   }
   tc_fence_before();
-  // In a pair, no remote arrival may reach a barrier before it is initialised.
-  if constexpr (kPair) cluster_sync_all();
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // TMEM columns: accumulators [0, NACC*issuers*Mpad) (buffer b, issuer k at
@@ -254,22 +205,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     set_status(P.status, code);
     *abort_flag = 1;
   };
-  // Barriers that the other CTA of a pair arrives on are waited on with
-  // cluster-scope acquire.
-  auto try_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if constexpr (kPair) return mbar_try_wait_cluster(bar, parity);
-    else return mbar_try_wait(bar, parity);
-  };
-  // Arrive on the first CTA's copy of this barrier (this CTA's own without pairs).
-  auto arrive_leader = [&](uint64_t* bar) {
-    if constexpr (kPair) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
-    else mbar_arrive(bar);
-  };
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0; i < 0x80000000u; ++i) {
-      if (try_wait(bar, parity)) return true;
+      if (mbar_try_wait(bar, parity)) return true;
       if ((i & 63u) == 63u) {
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > lim) {
@@ -293,27 +233,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      // X rows of this CTA: all tokens, or its half of them in a pair.
-      const int xrows = kPair ? P.Mpad / 2 : P.Mpad;
-      const int xrow0 = kPair ? rank * xrows : 0;
-      const uint32_t xbox = uint32_t(xrows) * 128u;
-      const uint32_t wbytes = C::kABytes + (kW12 ? 128u : 0u);
-      // Weight tiles of worker tile t (only the pair's second tile can lie
-      // past N, when N/128 is odd: then nothing is loaded for it).
-      auto load_w = [&](uint8_t* st, int t, int kb, uint64_t* bar) {
-        const int to = kPair ? 2 * t + rank : t;
-        if (to >= P.tiles) return;
-        if (kW12) {
-          tma_load_2d_hint(st, &tm_a0, kb * 64, to * 128, bar, pol_w);
-          tma_load_2d_hint(st + 8192, &tm_a1, kb * 64, to * 128, bar, pol_w);
-          tma_load_2d_hint(st + 16384, &tm_a2, kb * 64, to * 128, bar, pol_w);
-          bulk_load(st + plan.eb_off, P.ebase + int64_t(kb) * P.N + int64_t(to) * 128, 128u, bar);
-        } else {
-          tma_load_2d_hint(st, &tm_a0, kb * 128, to * 128, bar, pol_w);
-          tma_load_2d_hint(st + 16384, &tm_a0, kb * 128 + 64, to * 128, bar, pol_w);
-        }
-      };
-      auto tx_of = [&](int t) { return ((kPair ? 2 * t + rank : t) < P.tiles ? wbytes : 0u) + 2u * xbox; };
+      const uint32_t xbox = uint32_t(P.Mpad) * 128u;
+      const uint32_t tx = C::kABytes + (kW12 ? 128u : 0u) + 2u * xbox;
       // Per-unit state kept incrementally in 32-bit registers (no 64-bit
       // division in this single-thread loop).
       int t = int(ub / KB), kb = int(ub % KB);
@@ -326,8 +247,16 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         int t0 = t, kb0 = kb;
         for (int i = 0; i < prefill; ++i) {
           uint8_t* st = smem + i * plan.stage_bytes;
-          mbar_arrive_expect_tx(&B.full[i], tx_of(t0));
-          load_w(st, t0, kb0, &B.full[i]);
+          mbar_arrive_expect_tx(&B.full[i], tx);
+          if (kW12) {
+            tma_load_2d_hint(st, &tm_a0, kb0 * 64, t0 * 128, &B.full[i], pol_w);
+            tma_load_2d_hint(st + 8192, &tm_a1, kb0 * 64, t0 * 128, &B.full[i], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a2, kb0 * 64, t0 * 128, &B.full[i], pol_w);
+            bulk_load(st + plan.eb_off, P.ebase + int64_t(kb0) * P.N + int64_t(t0) * 128, 128u, &B.full[i]);
+          } else {
+            tma_load_2d_hint(st, &tm_a0, kb0 * 128, t0 * 128, &B.full[i], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a0, kb0 * 128 + 64, t0 * 128, &B.full[i], pol_w);
+          }
           if (++kb0 == KB) {
             kb0 = 0;
             ++t0;
@@ -342,11 +271,19 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         uint8_t* st = smem + s * plan.stage_bytes;
         if (issued >= prefill) {
           if (!wait(&B.empty[s], ph ^ 1u)) break;
-          mbar_arrive_expect_tx(&B.full[s], tx_of(t));
-          load_w(st, t, kb, &B.full[s]);
+          mbar_arrive_expect_tx(&B.full[s], tx);
+          if (kW12) {
+            tma_load_2d_hint(st, &tm_a0, kb * 64, t * 128, &B.full[s], pol_w);
+            tma_load_2d_hint(st + 8192, &tm_a1, kb * 64, t * 128, &B.full[s], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a2, kb * 64, t * 128, &B.full[s], pol_w);
+            bulk_load(st + plan.eb_off, P.ebase + int64_t(kb) * P.N + int64_t(t) * 128, 128u, &B.full[s]);
+          } else {
+            tma_load_2d_hint(st, &tm_a0, kb * 128, t * 128, &B.full[s], pol_w);
+            tma_load_2d_hint(st + 16384, &tm_a0, kb * 128 + 64, t * 128, &B.full[s], pol_w);
+          }
         }
-        tma_load_2d_hint(st + plan.x_off, &tm_x, kb * 128, xrow0, &B.full[s], pol_x);
-        tma_load_2d_hint(st + plan.x_off + xbox, &tm_x, kb * 128 + 64, xrow0, &B.full[s], pol_x);
+        tma_load_2d_hint(st + plan.x_off, &tm_x, kb * 128, 0, &B.full[s], pol_x);
+        tma_load_2d_hint(st + plan.x_off + xbox, &tm_x, kb * 128 + 64, 0, &B.full[s], pol_x);
         if (++kb == KB) {
           kb = 0;
           ++t;
@@ -368,11 +305,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     // Issuer k (warp 1 + k, one thread) takes the units i with i % issuers == k
     // into its own accumulator: one thread can only issue a kind::f16 MMA
     // every few tens of cycles, so two issuers double the issue rate.
-    // In a pair only the first CTA issues: each MMA covers both CTAs' rows.
     const int k = warp - 1;
-    if (lane == 0 && k < NISS && leader) {
-      const uint32_t idesc = idesc_bf16(kPair ? 256 : 128, uint32_t(P.Mpad));
-      const uint32_t xbox = uint32_t(kPair ? P.Mpad / 2 : P.Mpad) * 128u;
+    if (lane == 0 && k < NISS) {
+      const uint32_t idesc = idesc_bf16(128, uint32_t(P.Mpad));
+      const uint32_t xbox = uint32_t(P.Mpad) * 128u;
       // Descriptors of stage 0; other stages and K steps add (byte offset >> 4)
       // to the 14-bit start-address field, which cannot overflow (smem < 256 KB).
       const uint32_t st0 = smem_u32(smem);
@@ -394,9 +330,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
         if (i % NISS == k) {
           // W12: the decoders waited for the stage's copies before arriving on
-          // a_full, so "decoded" implies "landed" for X as well. bf16 pairs:
-          // warp 3 of each CTA forwards its stage's arrival to a_full.
-          if ((kW12 || kPair) ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
+          // a_full, so "decoded" implies "landed" for X as well.
+          if (kW12 ? !wait(&B.a_full[s], ph) : !wait(&B.full[s], ph)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + uint32_t(accb * NISS + k) * uint32_t(P.Mpad);
           const uint64_t soff16 = uint64_t((uint32_t(s) * plan.stage_bytes) >> 4);
@@ -407,23 +342,17 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             const uint64_t bdesc = bdesc0 + soff16 + koff;
             const uint32_t acc = (started || kk > 0) ? 1u : 0u;
             if (kW12) {
-              if constexpr (kPair) mma_bf16_ts_pair(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
-              else mma_bf16_ts(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
+              mma_bf16_ts(d_tmem, a_tmem + uint32_t(kk * 8), bdesc, idesc, acc);
             } else {
               const uint64_t aoff = uint64_t((uint32_t(kk >> 2) * 16384u + uint32_t(kk & 3) * 32u) >> 4);
-              if constexpr (kPair) mma_bf16_ss_pair(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
-              else mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
+              mma_bf16_ss(d_tmem, adesc0 + soff16 + aoff, bdesc, idesc, acc);
             }
           }
           started = true;
-          // Frees the smem stage and its TMEM A buffer (in both CTAs of a pair).
-          if constexpr (kPair) tc_commit_pair_mc(&B.empty[s], 0x3);
-          else tc_commit(&B.empty[s]);
+          tc_commit(&B.empty[s]);  // frees the smem stage and its TMEM A buffer
         }
         if (last) {
-          // Every issuer arrives once per segment (in both CTAs of a pair).
-          if constexpr (kPair) tc_commit_pair_mc(&B.acc_full[accb], 0x3);
-          else tc_commit(&B.acc_full[accb]);
+          tc_commit(&B.acc_full[accb]);  // every issuer arrives once per segment
           if (++accb == NACC) {
             accb = 0;
             accph ^= 1u;
@@ -436,8 +365,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
       }
       // Make sure no MMA is in flight before TMEM is released.
-      if constexpr (kPair) tc_commit_pair(B.drain);
-      else tc_commit(B.drain);
+      tc_commit(B.drain);
       mbar_wait(B.drain, 0, drain_limit_ns(lim));
     }
   } else if (warp == 3) {
@@ -448,20 +376,20 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // Every load of a batch is issued before the batch's first store, so the
       // window costs one memory round trip per batch rather than one per 32
       // values: the decoders cannot start before this warp arrives.
-      const int nwin = win_n;  // host guarantees nwin <= kOffCap
+      const int nwin = int(ue - ub) + 1;  // host guarantees nwin <= kOffCap
       {
         uint32_t v[kOffCap / 32];
 #pragma unroll
         for (int j = 0; j < kOffCap / 32; ++j)
-          if (lane + 32 * j < nwin) v[j] = P.exc_off[win_b0 + lane + 32 * j];
+          if (lane + 32 * j < nwin) v[j] = P.exc_off[ub + lane + 32 * j];
 #pragma unroll
         for (int j = 0; j < kOffCap / 32; ++j)
           if (lane + 32 * j < nwin) soff[lane + 32 * j] = v[j];
       }
       __syncwarp();
-      const uint32_t e0 = nwin > 0 ? soff[0] : 0u, e1 = nwin > 0 ? soff[nwin - 1] : 0u;
+      const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
       bool bad = e1 < e0 || int64_t(e1) > P.n_exc;
-      const bool fits = !bad && (e1 - e0) <= uint32_t(kPair ? kEntCapPair : kEntCap);
+      const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
       constexpr int kBatch = 16;  // entries per lane in flight
       uint32_t seen = 0;          // OR of the entries' top bits (a row field >= 128 is corrupt)
       if (fits) {
@@ -499,21 +427,6 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
       }
       if (__any_sync(0xFFFFFFFFu, (seen >> 30) != 0) && lane == 0) set_status(P.status, W12_ERR_CORRUPT);
-    } else if (kPair) {
-      // bf16 pair: no decoders; forward each stage's landed copies to the
-      // first CTA's a_full so that its MMA knows both CTAs' operands are in.
-      if (lane == 0) {
-        int s = 0;
-        uint32_t ph = 0;
-        for (int i = 0; i < int(ue - ub); ++i) {
-          if (!wait(&B.full[s], ph)) break;
-          arrive_leader(&B.a_full[s]);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
     }
   } else if (kW12 && warp >= 4 && warp < 4 + C::kDecWarps) {
     // --------------------------------------------------------------- decode
@@ -540,13 +453,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       uint32_t o0, o1, ent, mask[kChunksPerThread];
     };
     auto prep = [&](int i, Exc& x) {
-      if (kPair && i >= n_valid) {
-        x.o0 = x.o1 = e_base;  // a tile past N has no exceptions
-      } else {
-        const int lb = local_block(i);
-        x.o0 = soff[lb];
-        x.o1 = soff[lb + 1];
-      }
+      x.o0 = soff[i];
+      x.o1 = soff[i + 1];
       if (x.o1 < x.o0 || int64_t(x.o1) > P.n_exc || x.o0 < e_base || x.o1 > e_end) {
         if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
         x.o1 = x.o0;
@@ -584,63 +492,64 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // its TMEM A buffer committed, so the buffer is free once this returns.
       if (!__all_sync(0xFFFFFFFFu, wait(&B.full[s], ph))) break;
       tc_fence_after();
-      // A pair's tile past N (odd N/128) is not decoded: its stage holds only
-      // this CTA's half of X, and its rows of the product are never stored.
-      if (!kPair || i < n_valid) {
-        const uint8_t* st = smem + s * plan.stage_bytes;
-        const uint8_t* pl = st + row * 64;
-        const uint32_t swz = uint32_t(row >> 1) & 3u;
-        uint4 a[kChunksPerThread], b[kChunksPerThread], g[kChunksPerThread];
+      const uint8_t* st = smem + s * plan.stage_bytes;
+      const uint8_t* pl = st + row * 64;
+      const uint32_t swz = uint32_t(row >> 1) & 3u;
+      uint4 a[kChunksPerThread], b[kChunksPerThread], g[kChunksPerThread];
 #pragma unroll
-        for (int cc = 0; cc < kChunksPerThread; ++cc) {
-          const uint32_t off = ((uint32_t(h * kChunksPerThread + cc) ^ swz) << 4);
-          a[cc] = *reinterpret_cast<const uint4*>(pl + off);
-          b[cc] = *reinterpret_cast<const uint4*>(pl + 8192 + off);
-          g[cc] = *reinterpret_cast<const uint4*>(pl + 16384 + off);
-        }
-        const uint32_t eb = st[plan.eb_off + row];
-        const uint32_t E2 = (eb << 7) * 0x00010001u;
+      for (int cc = 0; cc < kChunksPerThread; ++cc) {
+        const uint32_t off = ((uint32_t(h * kChunksPerThread + cc) ^ swz) << 4);
+        a[cc] = *reinterpret_cast<const uint4*>(pl + off);
+        b[cc] = *reinterpret_cast<const uint4*>(pl + 8192 + off);
+        g[cc] = *reinterpret_cast<const uint4*>(pl + 16384 + off);
+      }
+      const uint32_t eb = st[plan.eb_off + row];
+      const uint32_t E2 = (eb << 7) * 0x00010001u;
 
 #pragma unroll
-        for (int cc = 0; cc < kChunksPerThread; ++cc) {
-          const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
-          uint32_t w[16];
-          decode8(a[cc].x, b[cc].x, g[cc].x, E2, w + 0);
-          decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
-          decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
-          decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
-          uint32_t mk = cur.mask[cc];
-          while (mk) {
-            const int src = __ffs(mk) - 1;
-            mk &= mk - 1;
-            const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
-            if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
-          }
-          if (cur.o1 - cur.o0 > 32) {
-            // Rare: more than 32 exceptions in the unit; walk the rest in batches.
-            for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
-              uint32_t e2 = kInvalidEnt;
-              if (bst + lane < cur.o1) {
-                const uint32_t v = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
-                e2 = (v >> 30) ? kInvalidEnt : v;
-              }
-              const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
-              uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
-              while (mk2) {
-                const int src = __ffs(mk2) - 1;
-                mk2 &= mk2 - 1;
-                const uint32_t e = __shfl_sync(0xFFFFFFFFu, e2, src);
-                if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
-              }
+      for (int cc = 0; cc < kChunksPerThread; ++cc) {
+        const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
+        uint32_t w[16];
+        decode8(a[cc].x, b[cc].x, g[cc].x, E2, w + 0);
+        decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
+        decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
+        decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
+        uint32_t mk = cur.mask[cc];
+        while (mk) {
+          const int src = __ffs(mk) - 1;
+          mk &= mk - 1;
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
+          if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+        }
+        if (cur.o1 - cur.o0 > 32) {
+          // Rare: more than 32 exceptions in the unit; walk the rest in batches.
+          for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
+            uint32_t e2 = kInvalidEnt;
+            if (bst + lane < cur.o1) {
+              const uint32_t v = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
+              e2 = (v >> 30) ? kInvalidEnt : v;
+            }
+            const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
+            uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
+            while (mk2) {
+              const int src = __ffs(mk2) - 1;
+              mk2 &= mk2 - 1;
+              const uint32_t e = __shfl_sync(0xFFFFFFFFu, e2, src);
+              if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
             }
           }
-          tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
         }
+        tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
       }
       if (i + kDecGroups < n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
       tmem_st_wait();
       tc_fence_before();
-      arrive_leader(&B.a_full[s]);
+      // This thread's reads of the stage (generic proxy) come before the copy
+      // (async proxy) that refills it once the MMA has committed. Without the
+      // fence, a refill issued soon after the reads was seen to land under
+      // them in about 1 % of launches.
+      fence_proxy_async_smem();
+      mbar_arrive(&B.a_full[s]);
       for (int k = 0; k < kDecGroups; ++k)
         if (++s == S) {
           s = 0;
@@ -722,16 +631,11 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const int c_first = unit_owner(int64_t(t) * KB, U, G);
       const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
       const int nsplit = c_last - c_first + 1;
-      // This CTA's output tile (in a pair: its half of the worker tile), and
-      // whether it lies inside N (the pair's second tile may not).
-      const int tout = kPair ? 2 * t + rank : t;
-      const bool tvalid = tout < P.tiles;
       // Partial slots are laid out [chunk][row][16] floats: each thread's 16
       // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
-      // Worker cc's slots are those of its CTA (of the CTA of the same rank).
       auto slot_of = [&](int cc) {
         const int ft = int(unit_begin(cc, U, G) / KB);
-        return 2 * (kPair ? 2 * cc + rank : cc) + (t == ft ? 0 : 1);
+        return 2 * cc + (t == ft ? 0 : 1);
       };
       // The CTA's final segment ends the kernel. When its tile has one other
       // piece and that piece is already done (it was the first piece its CTA
@@ -740,17 +644,17 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // here without writing a partial or taking a counter round trip.
       const int me = c - c_first;
       int pref = 0;
-      if (!kPair && !P.defer && seg_end == ue && nsplit == 2 && nchunks == 1) {
+      if (!P.defer && seg_end == ue && nsplit == 2 && nchunks == 1) {
         if (et == 0) {
           int done = 0;
           const uint64_t t0 = globaltimer_ns();
           for (;;) {
-            if (ld_acquire_gpu(&P.counters[tout]) == nsplit - 1) {
+            if (ld_acquire_gpu(&P.counters[t]) == nsplit - 1) {
               done = 1;
               break;
             }
             if (mbar_try_wait(&B.acc_full[cur], cur_ph)) {
-              done = ld_acquire_gpu(&P.counters[tout]) == nsplit - 1;
+              done = ld_acquire_gpu(&P.counters[t]) == nsplit - 1;
               break;
             }
             if (*abort_flag || globaltimer_ns() - t0 > lim) break;  // the wait below reports it
@@ -778,12 +682,6 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // One decision for the 128 epilogue threads, which meet at named barriers below.
       if (named_bar_any(kEpiBar, 128, !wait(&B.acc_full[cur], cur_ph))) break;
       tc_fence_after();
-      if (kPair && !tvalid) {
-        // Rows past N: nothing to store; only hand the accumulator back.
-        tc_fence_before();
-        arrive_leader(&B.acc_empty[cur]);
-        continue;
-      }
       // Issuer k wrote accumulator (cur, k) iff the segment holds a unit i
       // (counted from the CTA's first unit) with i % issuers == k.
       const int ia = int(seg_begin - ub), nseg = int(seg_end - seg_begin);
@@ -815,12 +713,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
               v[x] = acc;
             }
           }
-          if (kArgmax) argmax_chunk(v, tout, mc);
-          else store_chunk(v, tout, mc);
+          if (kArgmax) argmax_chunk(v, t, mc);
+          else store_chunk(v, t, mc);
         }
         tc_fence_before();
-        arrive_leader(&B.acc_empty[cur]);
-        if (pref && et == 0) P.counters[tout] = 0;  // every other contributor has already counted
+        mbar_arrive(&B.acc_empty[cur]);
+        if (pref && et == 0) P.counters[t] = 0;  // every other contributor has already counted
       } else {
         // In the final segment every stage of the ring has been consumed (the
         // segment's MMAs completed), so the other pieces' partials can be
@@ -829,21 +727,22 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         // piece is already counted, the tile is finished here without writing
         // this piece or taking the counter round trip.
         //
-        // At large M (P.defer) a piece only goes to its partial slot and the
-        // sum is left to splitk_reduce_kernel, which spreads it over every SM:
-        // a split tile's partial is Mpad x 128 fp32 (up to 128 KB), and one
-        // CTA summing up to four of them alone takes longer than its main loop.
+        // With P.defer a piece only goes to its partial slot and the sum is
+        // left to splitk_reduce_kernel, which spreads it over every SM: at
+        // large M a split tile's partial is Mpad x 128 fp32 (up to 128 KB), and
+        // one CTA summing three or more of them alone takes longer than its
+        // main loop.
         const uint32_t ring_bytes = uint32_t(S) * plan.stage_bytes;
         const int cb_max = int(ring_bytes / (uint32_t(nsplit - 1) * 8192u));  // chunks per gather batch
         const bool gather = !P.defer && seg_end == ue && cb_max >= 1;
         int fast = 0;
         if (gather) {
-          if (et == 0) *fast_flag = ld_acquire_gpu(&P.counters[tout]) == nsplit - 1;
+          if (et == 0) *fast_flag = ld_acquire_gpu(&P.counters[t]) == nsplit - 1;
           named_bar_sync(kEpiBar, 128);
           fast = *fast_flag;
         }
         if (!fast) {
-          const int slot = 2 * cta + (t == first_tile ? 0 : 1);
+          const int slot = 2 * c + (t == first_tile ? 0 : 1);
           float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
           for (int mc = 0; mc < nchunks; ++mc) {
             float v[16];
@@ -854,14 +753,14 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           }
         }
         tc_fence_before();
-        arrive_leader(&B.acc_empty[cur]);
+        mbar_arrive(&B.acc_empty[cur]);
         if (!fast && !P.defer) {
           // The barrier orders every epilogue thread's partial stores before
           // the single release-acquire increment; the last contributor's
           // readers are ordered after that increment by the second barrier.
           named_bar_sync(kEpiBar, 128);
           if (et == 0) {
-            const int old = atomic_add_acq_rel_gpu(&P.counters[tout], 1);
+            const int old = atomic_add_acq_rel_gpu(&P.counters[t], 1);
             *last_flag = (old == nsplit - 1) ? 1 : 0;
           }
           named_bar_sync(kEpiBar, 128);
@@ -871,9 +770,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         for (int mc0 = 0; last && mc0 < nchunks;) {
           const int nb = gather ? (nchunks - mc0 < cb_max ? nchunks - mc0 : cb_max) : nchunks;
           if (gather) {
-            if (mc0 > 0) named_bar_sync(kEpiBar, 128);  // the previous batch has been read
+            if (mc0 > 0) {
+              // The previous batch has been read (generic proxy) by every
+              // thread before the next bulk copies (async proxy) overwrite it.
+              fence_proxy_async_smem();
+              named_bar_sync(kEpiBar, 128);
+            }
             if (et == 0) {
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               mbar_arrive_expect_tx(B.gather, uint32_t(nsplit - 1) * uint32_t(nb) * 8192u);
               int j = 0;
               for (int sp = 0; sp < nsplit; ++sp) {
@@ -916,12 +819,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
 #pragma unroll
               for (int x = 0; x < 16; ++x) r[x] += q[x];
             }
-            if (kArgmax) argmax_chunk(r, tout, mc);
-            else store_chunk(r, tout, mc);
+            if (kArgmax) argmax_chunk(r, t, mc);
+            else store_chunk(r, t, mc);
           }
           mc0 += nb;
         }
-        if (last && et == 0) P.counters[tout] = 0;
+        if (last && et == 0) P.counters[t] = 0;
         named_bar_sync(kEpiBar, 128);
       }
     }
@@ -930,33 +833,24 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   }
 
   __syncthreads();
-  // A pair's CTAs leave together: the first CTA's MMAs read the second's
-  // shared and tensor memory, and the second arrives on the first's barriers.
-  if constexpr (kPair) cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
-    if constexpr (kPair) tmem_dealloc_pair(tmem_base, C::kTmemCols);
-    else tmem_dealloc(tmem_base, C::kTmemCols);
+    tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
 // Sum of the split tiles' partials (large M): block (t, mc) adds, for output
 // tile t and tokens mc*16 .. mc*16+15, the partial slots of the CTAs that
-// hold pieces of t, in CTA order (the same order as the in-kernel fixup, so
-// the result does not depend on the path), and writes Y. Unsplit tiles were
+// hold pieces of t, in CTA order (the same order as the in-kernel sum, so the
+// result does not depend on the path), and writes Y. Unsplit tiles were
 // written by the GEMM.
-// With CTA pairs the schedule's workers are pairs and its tiles tile pairs:
-// output tile t is half t % 2 of worker tile t / 2, and its pieces sit in the
-// slots of the CTAs of rank t % 2.
 __global__ void __launch_bounds__(128) splitk_reduce_kernel(const float* __restrict__ parts, float* __restrict__ Y,
-                                                            int M, int Mpad, int N, int KB, int64_t U, int G,
-                                                            int pair) {
+                                                            int M, int Mpad, int N, int KB, int64_t U, int G) {
   grid_dep_wait();
   grid_dep_launch();
   const int t = blockIdx.x, mc = blockIdx.y, row = threadIdx.x;
-  const int wt = pair ? t >> 1 : t, rank = pair ? t & 1 : 0;
-  const int c_first = unit_owner(int64_t(wt) * KB, U, G);
-  const int c_last = unit_owner((int64_t(wt) + 1) * KB - 1, U, G);
+  const int c_first = unit_owner(int64_t(t) * KB, U, G);
+  const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
   if (c_first == c_last) return;
   float r[16];
 #pragma unroll
@@ -971,7 +865,7 @@ __global__ void __launch_bounds__(128) splitk_reduce_kernel(const float* __restr
       const int cc = c0 + j;
       if (cc <= c_last) {
         const int ft = int(unit_begin(cc, U, G) / KB);
-        const int slot = 2 * (pair ? 2 * cc + rank : cc) + (wt == ft ? 0 : 1);
+        const int slot = 2 * cc + (t == ft ? 0 : 1);
         const float4* src =
             reinterpret_cast<const float4*>(parts + size_t(slot) * Mpad * 128) + (size_t(mc) * 128 + row) * 4;
 #pragma unroll
@@ -998,23 +892,7 @@ __global__ void __launch_bounds__(128) splitk_reduce_kernel(const float* __restr
   }
 }
 
-// Pairs the device can run at once with this configuration (0 if none or
-// the query fails), cached per device and configuration.
-template <typename Kern>
-static int max_pairs(Kern kern, const cudaLaunchConfig_t& cfg, int dev, int* cache) {
-  if (dev < 0 || dev >= 64) return 0;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
-    }
-    cache[dev] = n > 0 ? n : -1;
-  }
-  return cache[dev] > 0 ? cache[dev] : 0;
-}
-
-template <bool kW12, bool kArgmax, bool kPair>
+template <bool kW12, bool kArgmax>
 static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensorMap& a0, const CUtensorMap& a1,
                        const CUtensorMap& a2, const CUtensorMap& x, cudaStream_t stream) {
   GemmParams P = P0;
@@ -1025,15 +903,15 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
   const int issuers = nacc * 2 * sh.Mpad <= 256 ? 2 : 1;
   const int a_col0 = (nacc * issuers * sh.Mpad + 63) & ~63;
   int stages = kMaxStages;
-  while (stages > 2 && (smem_plan<kW12, kPair>(sh.Mpad, stages).total > uint32_t(smem_max) ||
+  while (stages > 2 && (smem_plan<kW12>(sh.Mpad, stages).total > uint32_t(smem_max) ||
                         (kW12 && a_col0 + stages * kAColsPerBuf > 512)))
     --stages;
   if (kW12 && a_col0 + stages * kAColsPerBuf > 512) return W12_ERR_UNSUPPORTED;
-  const SmemPlan plan = smem_plan<kW12, kPair>(sh.Mpad, stages);
+  const SmemPlan plan = smem_plan<kW12>(sh.Mpad, stages);
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
   P.issuers = issuers;
-  auto kern = gemm_kernel<kW12, kArgmax, kPair>;
+  auto kern = gemm_kernel<kW12, kArgmax>;
   static bool attr_set[64] = {false};  // per device; setting it twice is harmless
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
@@ -1043,49 +921,23 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(P.grid));
   cfg.blockDim = dim3(unsigned(Cfg<kW12>::kThreads));
   cfg.dynamicSmemBytes = plan.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  int nattr = 0;
-  if (kPair) {
-    attr[nattr].id = cudaLaunchAttributeClusterDimension;
-    attr[nattr].val.clusterDim.x = 2;
-    attr[nattr].val.clusterDim.y = 1;
-    attr[nattr].val.clusterDim.z = 1;
-    ++nattr;
-  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = nattr;
-  if (kPair) {
-    // One pair per two SMs that can hold it; the workspace was sized for at
-    // most half the SMs' worth of pairs.
-    static int pair_cache[64] = {0};
-    cfg.gridDim = dim3(2);
-    const int np = max_pairs(kern, cfg, dev, pair_cache);
-    if (np <= 0) return W12_ERR_UNSUPPORTED;
-    P.grid = int(P.units < int64_t(np) ? P.units : int64_t(np));
-    if (P.grid > sh.pgrid) P.grid = sh.pgrid;
-    // The CTA's exception window spans its units' blocks plus the other
-    // CTA's tiles between them (at most 2 * units + 2 * KB + 1 offsets).
-    const int64_t per = (P.units + P.grid - 1) / P.grid;
-    if (kW12 && 2 * per + 2 * int64_t(P.KB) + 1 > kOffCap) return W12_ERR_UNSUPPORTED;
-  }
-  cfg.gridDim = dim3(unsigned(kPair ? 2 * P.grid : P.grid));
-  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
-  cfg.numAttrs = nattr + (overlap_enabled() ? 1 : 0);
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
   int st = cuda_status(cudaLaunchKernelEx(&cfg, kern, a0, a1, a2, x, P));
   if (st || !P.defer) return st;
-  cudaLaunchConfig_t rcfg = {};
+  cudaLaunchConfig_t rcfg = cfg;
   rcfg.gridDim = dim3(unsigned(P.tiles), unsigned(P.Mpad / 16));
   rcfg.blockDim = dim3(128);
   rcfg.dynamicSmemBytes = 0;
-  rcfg.stream = stream;
-  rcfg.attrs = attr + nattr;
-  rcfg.numAttrs = overlap_enabled() ? 1 : 0;
   return cuda_status(cudaLaunchKernelEx(&rcfg, splitk_reduce_kernel, static_cast<const float*>(P.parts), P.Y, P.M,
-                                        P.Mpad, P.N, P.KB, P.units, P.grid, kPair ? 1 : 0));
+                                        P.Mpad, P.N, P.KB, P.units, P.grid));
 }
 
 int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, const w12_weights* W,
@@ -1105,7 +957,7 @@ int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, c
     if (!Wbf16 || !aligned(Wbf16, 16)) return W12_ERR_ARG;
   }
   if (!device_supported()) return W12_ERR_UNSUPPORTED;
-  const bool single_fits = !w12_mode || (sh.units + sh.grid - 1) / sh.grid + 1 <= kOffCap;
+  if (w12_mode && (sh.units + sh.grid - 1) / sh.grid + 1 > kOffCap) return W12_ERR_SHAPE;
   const WsLayout L = ws_layout(sh, 0);
   if (ws_bytes < L.total) return W12_ERR_WORKSPACE;
 
@@ -1116,7 +968,6 @@ int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, c
   P.K = sh.K;
   P.KB = sh.KB;
   P.tiles = sh.tiles;
-  P.wtiles = sh.tiles;
   P.grid = sh.grid;
   P.units = sh.units;
   P.ebase = w12_mode ? W->ebase : nullptr;
@@ -1133,14 +984,15 @@ int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, c
   P.limit_ns = wait_limit_ns();
   // At large M a split tile's partial is Mpad x 128 fp32 (up to 128 KB), and
   // the last contributor summing three or more of them alone takes longer
-  // than the whole main loop; those launches leave the sum to a second
-  // kernel. The fused head keeps the in-kernel sum (its CTAs split at most
-  // two tiles).
-  // Only where some tile is split three or more ways (a CTA's range shorter
-  // than a tile): with two pieces the in-kernel sum reads one partial.
+  // than its whole main loop: such launches (some tile split three or more
+  // ways, i.e. a CTA's range shorter than a tile) leave the sum to a second
+  // kernel. Two-piece splits and the fused head keep the in-kernel sum.
   P.defer = (!argmax_mode && sh.Mpad >= kDeferMinMpad && sh.units < int64_t(sh.KB) * sh.grid) ? 1 : 0;
 
-  CUtensorMap t0, t1, t2;
+  CUtensorMap tx, t0, t1, t2;
+  if (!encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(X), uint64_t(K), uint64_t(M),
+                      uint64_t(K) * 2, 64, uint32_t(sh.Mpad), CU_TENSOR_MAP_SWIZZLE_128B))
+    return W12_ERR_CUDA;
   if (w12_mode) {
     const uint64_t half = uint64_t(K) / 2;
     if (!encode_tmap_2d(&t0, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p0, half, uint64_t(N), half, 64, 128,
@@ -1150,37 +1002,14 @@ int launch_gemm(bool w12_mode, bool argmax_mode, const uint16_t* X, int64_t M, c
         !encode_tmap_2d(&t2, CU_TENSOR_MAP_DATA_TYPE_UINT8, W->p2, half, uint64_t(N), half, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_64B))
       return W12_ERR_CUDA;
-  } else {
-    if (argmax_mode) return W12_ERR_UNSUPPORTED;
-    if (!encode_tmap_2d(&t0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(Wbf16), uint64_t(K),
-                        uint64_t(N), uint64_t(K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-      return W12_ERR_CUDA;
-    t1 = t2 = t0;
+    return argmax_mode ? launch_impl<true, true>(sh, P, t0, t1, t2, tx, stream)
+                       : launch_impl<true, false>(sh, P, t0, t1, t2, tx, stream);
   }
-  // X boxes: all Mpad token rows, or half of them per CTA of a pair.
-  auto x_map = [&](CUtensorMap* tx, int rows) {
-    return encode_tmap_2d(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(X), uint64_t(K), uint64_t(M),
-                          uint64_t(K) * 2, 64, uint32_t(rows), CU_TENSOR_MAP_SWIZZLE_128B);
-  };
-  CUtensorMap tx;
-  if (sh.Mpad >= kPairMinMpad) {
-    // CTA pairs: the schedule runs over 256-row tile pairs (the last one half
-    // empty when N/128 is odd). Falls back to single CTAs if the device cannot
-    // co-schedule pairs or the exception window would not fit.
-    GemmParams Q = P;
-    Q.wtiles = (sh.tiles + 1) / 2;
-    Q.units = int64_t(Q.wtiles) * sh.KB;
-    if (!x_map(&tx, sh.Mpad / 2)) return W12_ERR_CUDA;
-    const int r = !w12_mode    ? launch_impl<false, false, true>(sh, Q, t0, t1, t2, tx, stream)
-                  : argmax_mode ? launch_impl<true, true, true>(sh, Q, t0, t1, t2, tx, stream)
-                                : launch_impl<true, false, true>(sh, Q, t0, t1, t2, tx, stream);
-    if (r != W12_ERR_UNSUPPORTED) return r;
-  }
-  if (!single_fits) return W12_ERR_SHAPE;
-  if (!x_map(&tx, sh.Mpad)) return W12_ERR_CUDA;
-  return !w12_mode    ? launch_impl<false, false, false>(sh, P, t0, t1, t2, tx, stream)
-         : argmax_mode ? launch_impl<true, true, false>(sh, P, t0, t1, t2, tx, stream)
-                       : launch_impl<true, false, false>(sh, P, t0, t1, t2, tx, stream);
+  if (!encode_tmap_2d(&t0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(Wbf16), uint64_t(K),
+                      uint64_t(N), uint64_t(K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return W12_ERR_CUDA;
+  if (argmax_mode) return W12_ERR_UNSUPPORTED;
+  return launch_impl<false, false>(sh, P, t0, t0, t0, tx, stream);
 }
 
 }  // namespace w12

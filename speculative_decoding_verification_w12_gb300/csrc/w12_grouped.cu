@@ -726,6 +726,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       if (i + kDecGroups < n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
       tmem_st_wait();
       tc_fence_before();
+      // This thread's reads of the stage (generic proxy) come before the copy
+      // (async proxy) that refills it once the MMA has committed.
+      fence_proxy_async_smem();
       mbar_arrive(&B.a_full[s]);
       for (int k = 0; k < kDecGroups; ++k)
         if (++s == S) {
@@ -1025,9 +1028,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         for (int mc0 = 0; last && mc0 < nchunks;) {
           const int nb = gather ? (nchunks - mc0 < cb_max ? nchunks - mc0 : cb_max) : nchunks;
           if (gather) {
-            if (mc0 > 0) named_bar_sync(kEpiBar, 128);  // the previous batch has been read
+            if (mc0 > 0) {
+              // The previous batch has been read (generic proxy) by every
+              // thread before the next bulk copies (async proxy) overwrite it.
+              fence_proxy_async_smem();
+              named_bar_sync(kEpiBar, 128);
+            }
             if (et == 0) {
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               mbar_arrive_expect_tx(B.gather, uint32_t(nsplit - 1) * uint32_t(nb) * 8192u);
               int j = 0;
               for (int sp = 0; sp < nsplit; ++sp) {

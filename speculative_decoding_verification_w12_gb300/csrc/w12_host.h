@@ -51,7 +51,6 @@ inline int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 // Stream-K schedule shared by the GEMM launcher and its workspace sizing.
 struct GemmShape {
   int M, Mpad, N, K, KB, tiles, grid;
-  int pgrid;  // upper bound on CTA pairs when the GEMM runs on pairs (half the SMs)
   int64_t units;
 };
 int gemm_shape(int64_t M, int64_t N, int64_t K, GemmShape* s);

@@ -74,8 +74,7 @@ def test_split_k_shapes(N, K):
 
 @pytest.mark.parametrize("M", [16, 128])
 def test_exception_heavy_weights(M):
-    """Dense exceptions: zero groups, >32 exceptions per unit, specials (M=128
-    runs on CTA pairs, whose exception window spans both tiles of a pair)."""
+    """Dense exceptions: zero groups, >32 exceptions per unit, specials."""
     g = S.rng(5)
     N, K = 512, 1024
     W = S.weights_bf16(N, K, seed=6)
@@ -184,10 +183,10 @@ def test_batched_layer_shapes_sampled_columns(M, name, N, K):
 
 @pytest.mark.parametrize("M,N,K", [(64, 1152, 1280), (200, 1152, 1280), (256, 128, 4096), (96, 640, 4096),
                                    (128, 25600, 128), (80, 3200, 2048)])
-def test_pair_shapes(M, N, K):
-    """M >= 49 runs on CTA pairs (two 128-row tiles per MMA): odd tile counts
-    (the last pair's second tile lies past N), a single tile, deep and wide
-    shapes, ragged M; W12 and the bf16 kernel against the oracle."""
+def test_large_m_shapes(M, N, K):
+    """Large M: odd tile counts, a single tile, deep and wide shapes, ragged M
+    (tiles split three or more ways at M >= 113 are summed by the second
+    kernel); W12 and the bf16 kernel against the oracle."""
     W = S.weights_bf16(N, K, seed=M + N)
     X = S.activations_bf16(M, K, seed=K + 1)
     Y64 = O.gemm(X, O.pack(W))
