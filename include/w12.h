@@ -268,9 +268,13 @@ int w12_state_select(const void* states, int B, int T, int64_t row_bytes, const 
  * prefix_len[b] + T > max_kv_len; the request is computed with its prefix
  * clamped into range), W12_ERR_TIMEOUT (a bounded wait gave up; outputs
  * unspecified). Returns W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_WORKSPACE,
- * W12_ERR_UNSUPPORTED or W12_ERR_CUDA. The workspace (no zero-fill needed) is
- * at least w12_tree_attention_ws_bytes(...) bytes, which is 0 for a shape the
- * call rejects. */
+ * W12_ERR_UNSUPPORTED or W12_ERR_CUDA. The workspace is at least
+ * w12_tree_attention_ws_bytes(...) bytes, which is 0 for a shape the call
+ * rejects. It holds the key splits' partial results and one arrival count per
+ * (request, kv head, row tile): zero-fill it before its first use; a call
+ * that ends with dev_status W12_OK leaves the counts at zero, so the same
+ * workspace serves the next call. After any error status, zero it again.
+ * Calls that share one workspace must be ordered on one stream. */
 size_t w12_tree_attention_ws_bytes(int B, int T, int Hq, int Hkv, int64_t max_kv_len);
 
 int w12_tree_attention(const uint16_t* Q, const uint16_t* K_cache, const uint16_t* V_cache, int B, int T, int Hq,

@@ -254,6 +254,11 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+// Acquire-release fence at GPU scope: this thread's earlier memory operations
+// are ordered before its later ones for every thread of the GPU (lighter than
+// the sequentially consistent __threadfence).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Load with acquire semantics at GPU scope (pairs with the release half of
 // atomic_add_acq_rel_gpu in other CTAs).
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {

@@ -377,7 +377,13 @@ class TreeAttention:
         nbytes = lib().w12_tree_attention_ws_bytes(B, T, Hq, Hkv, self.max_kv_len)
         if nbytes == 0:
             raise W12Error(2, "w12_tree_attention_ws_bytes")
-        self.ws = torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+        # Zero-filled once: the kernel's per-item arrival counts start at zero
+        # and a W12_OK call leaves them there.
+        self.ws = torch.zeros(int(nbytes), dtype=torch.uint8, device=device)
+
+    def reset(self):
+        """Zero the workspace again (needed after a call that ended with an error status)."""
+        self.ws.zero_()
 
     def run(self, Q: torch.Tensor, K_cache: torch.Tensor, V_cache: torch.Tensor, prefix_len: torch.Tensor,
             parents: torch.Tensor, scale: float | None = None, out: torch.Tensor | None = None,

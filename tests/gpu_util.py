@@ -53,10 +53,14 @@ def status_value(st):
 
 
 # Tree attention vs the float64 oracle: P rounded to bf16 for the P.V product
-# (relative error <= 2^-9 per weight) and O rounded to bf16 (<= 2^-9 relative):
-# about 1.6e-3 rms relative in all; an element can be off by 2^-8 of itself.
+# (relative error <= 2^-9 per weight) and O rounded to bf16 (<= 2^-9 of the
+# element): about 1.6e-3 rms relative in all. Per element the error is bounded
+# by a small fraction of the output's rms (the P rounding, spread over many
+# keys) plus 2^-8 of the element itself (the O rounding, and the P rounding in
+# rows with few keys, where |O| can reach max |V|, far above the rms).
 ATTN_REL_FRO = 4e-3
 ATTN_MAX_ABS_OVER_RMS = 3e-2
+ATTN_ELEM_REL = 2.0 ** -8
 
 
 def assert_attn_close(O_bits: np.ndarray, O64: np.ndarray, what=""):
@@ -64,8 +68,11 @@ def assert_attn_close(O_bits: np.ndarray, O64: np.ndarray, what=""):
     err = O - O64
     rel = np.linalg.norm(err) / max(np.linalg.norm(O64), 1e-300)
     rms = np.sqrt(np.mean(O64 ** 2))
+    bound = ATTN_MAX_ABS_OVER_RMS * rms + ATTN_ELEM_REL * np.abs(O64)
     mx = np.abs(err).max()
     assert np.isfinite(O).all(), f"{what}: non-finite output"
     assert rel <= ATTN_REL_FRO, f"{what}: rel Frobenius {rel:.3e}"
-    assert mx <= ATTN_MAX_ABS_OVER_RMS * rms, f"{what}: max abs {mx:.3e} vs rms {rms:.3e}"
+    worst = np.unravel_index(np.argmax(np.abs(err) - bound), err.shape)
+    assert (np.abs(err) <= bound).all(), \
+        f"{what}: |err| {abs(err[worst]):.3e} at {worst} (O {O64[worst]:.4f}) above {bound[worst]:.3e} (rms {rms:.3e})"
     return rel, mx / rms

@@ -136,3 +136,36 @@ def test_argument_errors():
         w12.tree_attention(Q, K, K, i, p)
     assert e.value.code == 2
     assert w12.lib().w12_tree_attention_ws_bytes(1, 129, 2, 1, 1000) == 0     # T > 128
+
+
+def test_workspace_reused_across_calls():
+    """One workspace over several calls with split keys: the per-item arrival
+    counts return to zero after each call, so every call merges its own splits."""
+    B, T, Hq, Hkv = 2, 16, 5, 1
+    prefix = np.array([50, 3000], dtype=np.int32)
+    S_max = 3100
+    parents = _trees(B, T, "tree", seed=4)
+    att = w12.TreeAttention(B, T, Hq, Hkv, S_max)
+    for call in range(3):
+        Q, K, V = S.attention_inputs_bf16(B, T, S_max, Hq, Hkv, 128, seed=40 + call)
+        st = new_status()
+        out = att.run(to_dev_bf16(Q), to_dev_bf16(K), to_dev_bf16(V), to_dev_i32(prefix), to_dev_i32(parents), 0.1,
+                      status=st)
+        assert status_value(st) == 0
+        assert_attn_close(bits_of(out), O.tree_attention(Q, K, V, prefix, parents, 0.1), f"call {call}")
+
+
+def test_runs_that_span_several_items():
+    """200 (request, kv head) items of 5 key blocks over one CTA per SM: a
+    CTA's run takes the tail of one item, whole items and the head of the
+    next; uneven prefixes leave some segments with no keys of their request."""
+    B, T, Hq, Hkv, max_len = 25, 16, 8, 8, 600
+    g = np.random.default_rng(17)
+    prefix = g.integers(0, max_len - T + 1, size=B).astype(np.int32)
+    prefix[:3] = [0, max_len - T, 1]
+    Q, K, V = S.attention_inputs_bf16(B, T, max_len, Hq, Hkv, 128, seed=31)
+    parents = _trees(B, T, "tree", seed=8)
+    st = new_status()
+    out = _run(Q, K, V, prefix, parents, 0.11, max_len=max_len, status=st)
+    assert status_value(st) == 0
+    assert_attn_close(out, O.tree_attention(Q, K, V, prefix, parents, 0.11), "multi-item runs")
