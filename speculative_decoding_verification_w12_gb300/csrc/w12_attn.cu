@@ -86,14 +86,17 @@ constexpr uint32_t kTmemCols = 512;
 // and the O accumulators of the two key halves.
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColOA = 256, kColOB = 384;
 constexpr float kRescale = 8.0f;                // log2 growth of the maximum that triggers a rescale
+constexpr int kEarlyBlocks = 1;                 // K/V blocks copied before the setup barrier
+constexpr int kMergeBatch = 1;                  // partials whose loads a merge step keeps in flight
 
 struct AttnParams {
   const uint16_t* Q;          // [B, T, Hq, 128]
   uint16_t* O;                // [B, T, Hq, 128]
   const int32_t* prefix_len;  // [B]
   const int32_t* parents;     // [B, T]
-  float4* part_o;             // [grid, 2 slots, 32 chunks of 4 dims, 128 rows]: partial O
+  uint4* part_o;              // [grid, 2 slots, 16 chunks of 8 dims, 128 rows]: partial O / (l sc), fp16
   float2* part_ml;            // [grid, 2 slots, 128 rows]: (m, l) of the partial
+  float* part_sc;             // [grid, 2 slots, 2 halves, 128 rows]: scale sc of the half row
   int32_t* cnt;               // [items]: key blocks of the item done (zero between calls)
   int32_t* status;
   int64_t U;                  // B x Hkv x nkb (request, kv head, key block) units
@@ -139,6 +142,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// The same for fp16, and back.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+  return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t word_sel(const uint32_t (&a)[4], int i) {
   return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : i == 3 ? a[3] : 0u;
 }
@@ -159,7 +176,8 @@ __device__ __forceinline__ void parent_row(const int32_t* pb, int T, int (&pr)[4
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = lane + 32 * k;
-    pr[k] = i < T ? __ldg(pb + i) : -1;
+    pr[k] = -1;
+    if (32 * k < T && i < T) pr[k] = __ldg(pb + i);
   }
 }
 
@@ -191,12 +209,21 @@ __device__ __forceinline__ void tree_ancestors(const int (&pr)[4], int t, int T,
     const int jj = j >= 0 ? j : 0;
 #pragma unroll
     for (int w = 0; w < 4; ++w) anc[w] |= (j >= 0 && (jj >> 5) == w) ? 1u << (jj & 31) : 0u;
-    const int p0 = __shfl_sync(0xFFFFFFFFu, pr[0], jj & 31);
-    const int p1 = __shfl_sync(0xFFFFFFFFu, pr[1], jj & 31);
-    const int p2 = __shfl_sync(0xFFFFFFFFu, pr[2], jj & 31);
-    const int p3 = __shfl_sync(0xFFFFFFFFu, pr[3], jj & 31);
+    // Only the words that hold nodes < T are exchanged (T is uniform).
     const int w = jj >> 5;
-    const int pj = w == 0 ? p0 : w == 1 ? p1 : w == 2 ? p2 : p3;
+    int pj = __shfl_sync(0xFFFFFFFFu, pr[0], jj & 31);
+    if (T > 32) {
+      const int p1 = __shfl_sync(0xFFFFFFFFu, pr[1], jj & 31);
+      pj = w == 1 ? p1 : pj;
+    }
+    if (T > 64) {
+      const int p2 = __shfl_sync(0xFFFFFFFFu, pr[2], jj & 31);
+      pj = w == 2 ? p2 : pj;
+    }
+    if (T > 96) {
+      const int p3 = __shfl_sync(0xFFFFFFFFu, pr[3], jj & 31);
+      pj = w == 3 ? p3 : pj;
+    }
     j = j >= 0 ? pj : -1;
   }
 }
@@ -397,40 +424,84 @@ __device__ __forceinline__ void store_row(const AttnParams& P, int b, int g, int
   }
 }
 
+// A partial result of this thread's half row: (M, den) and o as
+// u = o / (den sc) in fp16, sc the largest |o / den| of the half row (so
+// |u| <= 1 and u keeps 11 significant bits relative to the row's largest
+// value); chunk-major, so a warp's stores of one chunk cover 32 consecutive
+// rows.
+__device__ __forceinline__ void store_partial(const AttnParams& P, size_t sb, int r, int h, float M, float den,
+                                              const float (&o)[64]) {
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 64; ++k) amax = fmaxf(amax, fabsf(o[k]));
+  amax *= inv;
+  const float sc = amax > 0.f ? amax : 1.f;
+  const float f = inv / sc;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 w;
+    w.x = pack_f16x2(o[8 * c] * f, o[8 * c + 1] * f);
+    w.y = pack_f16x2(o[8 * c + 2] * f, o[8 * c + 3] * f);
+    w.z = pack_f16x2(o[8 * c + 4] * f, o[8 * c + 5] * f);
+    w.w = pack_f16x2(o[8 * c + 6] * f, o[8 * c + 7] * f);
+    P.part_o[(sb * 16 + 8 * h + c) * 128 + r] = w;
+  }
+  P.part_sc[(sb * 2 + h) * 128 + r] = sc;
+  if (h == 0) P.part_ml[sb * 128 + r] = make_float2(M, den);
+}
+
 // Merge of an item's partial results by the segment that finished last: it
 // folds every partial of the item into (M, den, o), O = sum_s 2^(m_s - M) O_s /
-// sum_s 2^(m_s - M) l_s. With `own` the caller's (M, den, o) already hold this
-// CTA's part and its slot is skipped; otherwise they start empty and its slot
-// is read like the others. Partials are read through L2 (ld.cg) after the
-// acquire that made them visible; each CTA's 17 loads are in flight together.
+// sum_s 2^(m_s - M) l_s, with O_s = l_s sc_s u_s. With `own` the caller's
+// (M, den, o) already hold this CTA's part and its slot is skipped; otherwise
+// they start empty and its slot is read like the others. Partials are read
+// through L2 (ld.cg) after the acquire that made them visible, kMergeBatch
+// CTAs' at a time with all their loads in flight together; an empty partial
+// (m = -inf, l = 0) adds nothing.
 __device__ void merge_item(const AttnParams& P, const Seg& sg, int r, int h, float M, float den, float (&o)[64],
                            bool own) {
   const int64_t x0 = int64_t(sg.item / P.ntile) * P.nkb;
   const int k0 = run_of(P, x0), k1 = run_of(P, x0 + P.nkb - 1);
-  for (int k = k0; k <= k1; ++k) {
-    const int cc = k * P.ntile + sg.tile;
-    if (own && cc == int(blockIdx.x)) continue;
-    const int64_t st = run_start(P, k);
-    const int slot = (st >= x0) ? 0 : 1;
-    const size_t sb = size_t(cc) * 2 + slot;
-    const float2 ml = __ldcg(&P.part_ml[sb * 128 + r]);
-    float4 q[16];
+  for (int k = k0; k <= k1; k += kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float scv[kMergeBatch];
+    uint4 u[kMergeBatch][8];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) q[k] = __ldcg(&P.part_o[(sb * 32 + 16 * h + k) * 128 + r]);
-    // No branch on m before the loads are used, so all 17 are in flight at
-    // once; an empty partial (m = -inf) has o = 0 and l = 0 and adds nothing.
-    const float Mn = fmaxf(M, ml.x);
-    const float a = M == Mn ? 1.f : fast_exp2(M - Mn);  // 0 while M = -inf
-    const float w = ml.x == Mn ? 1.f : fast_exp2(ml.x - Mn);
+    for (int e = 0; e < kMergeBatch; ++e) {
+      const int kk = k + e;
+      const int cc = kk * P.ntile + sg.tile;
+      ml[e] = make_float2(-INFINITY, 0.f);
+      scv[e] = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      o[4 * k] = o[4 * k] * a + w * q[k].x;
-      o[4 * k + 1] = o[4 * k + 1] * a + w * q[k].y;
-      o[4 * k + 2] = o[4 * k + 2] * a + w * q[k].z;
-      o[4 * k + 3] = o[4 * k + 3] * a + w * q[k].w;
+      for (int c = 0; c < 8; ++c) u[e][c] = make_uint4(0, 0, 0, 0);
+      if (kk <= k1 && !(own && cc == int(blockIdx.x))) {
+        const size_t sb = size_t(cc) * 2 + (run_start(P, kk) >= x0 ? 0 : 1);
+        ml[e] = __ldcg(&P.part_ml[sb * 128 + r]);
+        scv[e] = __ldcg(&P.part_sc[(sb * 2 + h) * 128 + r]);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) u[e][c] = __ldcg(&P.part_o[(sb * 16 + 8 * h + c) * 128 + r]);
+      }
     }
-    den = den * a + w * ml.y;
-    M = Mn;
+#pragma unroll
+    for (int e = 0; e < kMergeBatch; ++e) {
+      const float Mn = fmaxf(M, ml[e].x);
+      const float a = M == Mn ? 1.f : fast_exp2(M - Mn);  // 0 while M = -inf
+      const float w = ml[e].x == Mn ? 1.f : fast_exp2(ml[e].x - Mn);
+      const float f = w * ml[e].y * scv[e];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t ww[4] = {u[e][c].x, u[e][c].y, u[e][c].z, u[e][c].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 v = unpack_f16x2(ww[q]);
+          o[8 * c + 2 * q] = o[8 * c + 2 * q] * a + f * v.x;
+          o[8 * c + 2 * q + 1] = o[8 * c + 2 * q + 1] * a + f * v.y;
+        }
+      }
+      den = den * a + w * ml[e].y;
+      M = Mn;
+    }
   }
   const int rr = sg.tile * 128 + r;
   if (rr < P.G * P.T) {
@@ -466,10 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Everything below reads what the previous kernel on the stream wrote.
   grid_dep_wait();
   Seg first;
-  {
-    int64_t pos = run0;
-    next_seg(P, pos, run1, run0, first);  // run1 > run0: every CTA has at least one unit
-  }
+  int64_t pos_first = run0;              // where the run continues after the first segment
+  next_seg(P, pos_first, run1, run0, first);  // run1 > run0: every CTA has at least one unit
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -488,12 +557,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(seg_ready, 256);  // every softmax thread
     *abort_flag = 0;
     fence_barrier_init();
-    // The first K and V blocks do not depend on Q: their copies start now,
-    // under the Q load and the setup barrier.
+    // The first K and V block do not depend on Q: their copies start now,
+    // under the Q load and the setup barrier (the rest of the ring after it,
+    // so that Q and the first block are not queued behind them).
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     const uint64_t pol = policy_evict_first();
-    for (int i = 0; i < min(kStages, first.n); ++i) {
+    for (int i = 0; i < min(kEarlyBlocks, first.n); ++i) {
       const int key0 = (first.j0 + i) * kKeys;
       uint8_t* ks = smem + kKOff + uint32_t(i) * kTile;
       uint8_t* vs = smem + kVOff + uint32_t(i) * kTile;
@@ -565,11 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* ring = smem + (isK ? kKOff : kVOff);
       const uint64_t pol = policy_evict_first();
       int issued = 0;
-      int skip = min(kStages, first.n);  // issued during setup
+      int skip = min(kEarlyBlocks, first.n);  // issued during setup
       bool ok = true;
-      int64_t pos = run0;
-      Seg sg;
-      while (ok && next_seg(P, pos, run1, run0, sg)) {
+      int64_t pos = pos_first;
+      Seg sg = first;
+      for (bool more = true; ok && more; more = next_seg(P, pos, run1, run0, sg)) {
         for (int i = 0; i < sg.n; ++i) {
           if (skip > 0) {
             --skip;
@@ -616,9 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = idesc_bf16(128, 128) | (1u << 16);  // B (V) MN-major
       int base = 0, si = 0;
       bool ok = true;
-      int64_t pos = run0;
-      Seg sg;
-      while (next_seg(P, pos, run1, run0, sg)) {
+      int64_t pos = pos_first;
+      Seg sg = first;
+      for (bool more = true; more; more = next_seg(P, pos, run1, run0, sg)) {
         if (si > 0 && !wait(seg_ready, uint32_t(si - 1) & 1u)) ok = false;
         for (int j = 0; ok && j < sg.n; ++j) {
           const int gj = base + j;
@@ -691,9 +761,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Rg = P.G * P.T;
     float2* xch = reinterpret_cast<float2*>(smem + kQOff);  // the Q area, once the segment's MMAs are done
     int base = 0, si = 0;
-    int64_t pos = run0;
-    Seg sg;
-    bool more = next_seg(P, pos, run1, run0, sg);
+    int64_t pos = pos_first;
+    Seg sg = first;
+    bool more = true;
     uint32_t anc[4] = {anc_first[0], anc_first[1], anc_first[2], anc_first[3]};  // this row's ancestor set
     while (more) {
       Seg nx;
@@ -802,11 +872,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 64; ++k) o[k] = 0.f;
       }
       tc_fence_before();
-      // The next segment's request length, parent row and Q are loaded
-      // between the two halves of this segment's stores, so that their
-      // latency passes under the stores. A partial result goes to this CTA's
-      // slot as (M, den) and o, chunk-major (a warp's stores of one chunk cover
-      // 32 consecutive rows).
+      // The next segment's request length and parent row are loaded before
+      // this segment's stores (a partial result to this CTA's slot), its Q
+      // right after them, so that their latency passes under the stores.
       constexpr int kQIter = 128 * 16 / 256;
       uint4 qv[kQIter];
       int pr[4];
@@ -814,19 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         seg_keys(P, nx);
         parent_row(P.parents + size_t(nx.b) * T, T, pr);
       }
-      const size_t sb = size_t(blockIdx.x) * 2 + sg.slot;
       if (!sg.whole) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          P.part_o[(sb * 32 + 16 * h + k) * 128 + r] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-        if (h == 0) P.part_ml[sb * 128 + r] = make_float2(sg.n > 0 && warp_live ? M : -INFINITY, den);
+        store_partial(P, size_t(blockIdx.x) * 2 + sg.slot, r, h, sg.n > 0 && warp_live ? M : -INFINITY, den, o);
       } else if (valid) {
         store_row(P, sg.b, sg.g, hh, t, h, o, den);
-      }
-      if (!sg.whole) {
-#pragma unroll
-        for (int k = 8; k < 16; ++k)
-          P.part_o[(sb * 32 + 16 * h + k) * 128 + r] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
       }
       if (has_next) {
         load_q_regs<256>(P, qv, nx.b, nx.g, nx.tile, threadIdx.x - 128);
@@ -959,12 +1018,13 @@ static bool has_partials(const AttnPlan& p) {
   return false;
 }
 
-static size_t part_o_bytes(const AttnPlan& p) { return size_t(p.grid) * 2 * 128 * kD * sizeof(float); }
+static size_t part_o_bytes(const AttnPlan& p) { return size_t(p.grid) * 2 * 128 * kD * 2; }
 static size_t part_ml_bytes(const AttnPlan& p) { return size_t(p.grid) * 2 * 128 * sizeof(float2); }
+static size_t part_sc_bytes(const AttnPlan& p) { return size_t(p.grid) * 2 * 2 * 128 * sizeof(float); }
 
 static size_t ws_bytes_of(const AttnPlan& p) {
   if (!has_partials(p)) return 256;
-  return part_o_bytes(p) + part_ml_bytes(p) + size_t(p.items) * sizeof(int32_t) + 256;
+  return part_o_bytes(p) + part_ml_bytes(p) + part_sc_bytes(p) + size_t(p.items) * sizeof(int32_t) + 256;
 }
 
 }  // namespace attn_impl
@@ -1000,9 +1060,11 @@ int w12_tree_attention(const uint16_t* Q, const uint16_t* K_cache, const uint16_
   P.prefix_len = prefix_len;
   P.parents = parents;
   if (parts) {
-    P.part_o = static_cast<float4*>(ws);
-    P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + part_o_bytes(pl));
-    P.cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + part_o_bytes(pl) + part_ml_bytes(pl));
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    P.part_o = reinterpret_cast<uint4*>(w);
+    P.part_ml = reinterpret_cast<float2*>(w + part_o_bytes(pl));
+    P.part_sc = reinterpret_cast<float*>(w + part_o_bytes(pl) + part_ml_bytes(pl));
+    P.cnt = reinterpret_cast<int32_t*>(w + part_o_bytes(pl) + part_ml_bytes(pl) + part_sc_bytes(pl));
   }
   P.status = dev_status;
   P.B = B;
