@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint64_t lim = P.limit_ns;
@@ -936,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

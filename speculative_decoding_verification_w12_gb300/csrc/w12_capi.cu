@@ -241,11 +241,11 @@ __global__ void selftest_timeout_kernel(int32_t* status, uint64_t limit_ns) {
     mbar_init(&bar, 1);
     fence_barrier_init();
   }
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     if (!mbar_wait(&bar, 0, limit_ns)) set_status(status, W12_ERR_TIMEOUT);
   }
-  __syncthreads();
+  cta_sync();
 }
 
 }  // namespace w12

@@ -254,6 +254,16 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+// Barrier of the whole CTA that is safe after warp-divergent code. __syncthreads
+// is an aligned barrier: every thread of a warp must reach it together. Where
+// one lane of a warp runs a role (a TMA producer, an MMA issuer) while the
+// others skip ahead, the warp first reconverges (__syncwarp), so that no lane
+// is counted at the barrier before its warp's other lanes are done.
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
 // Acquire-release fence at GPU scope: this thread's earlier memory operations
 // are ordered before its later ones for every thread of the GPU (lighter than
 // the sequentially consistent __threadfence).

@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // TMEM columns: accumulators [0, NACC*issuers*Mpad) (buffer b, issuer k at
@@ -1091,7 +1091,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     if (gather_pending >= 0) mbar_wait(B.gather, uint32_t(gather_pending), drain_limit_ns(lim));
   }
 
-  __syncthreads();
+  cta_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);

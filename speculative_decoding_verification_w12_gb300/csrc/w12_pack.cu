@@ -83,11 +83,11 @@ __global__ void __launch_bounds__(128) pack_block_kernel(const uint16_t* __restr
     if (lane >= o) incl += y;
   }
   if (lane == 31) warp_tot[wid] = incl;
-  __syncthreads();
+  cta_sync();
   int before = 0;
   for (int w = 0; w < wid; ++w) before += warp_tot[w];
   if (r == 0) block_tot = warp_tot[0] + warp_tot[1] + warp_tot[2] + warp_tot[3];
-  __syncthreads();
+  cta_sync();
   const int excl = before + incl - cnt;
 
   if (!kWrite) {
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(1024) exclusive_scan_kernel(uint32_t* data, in
     if (lane >= o) incl += y;
   }
   if (lane == 31) warp_sum[wid] = incl;
-  __syncthreads();
+  cta_sync();
   uint64_t before = 0;
   for (int w = 0; w < wid; ++w) before += warp_sum[w];
   uint64_t run = before + incl - local;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(1024) exclusive_scan_kernel(uint32_t* data, in
     data[i] = static_cast<uint32_t>(run);
     run += c;
   }
-  __syncthreads();
+  cta_sync();
   if (t == blockDim.x - 1) {
     uint64_t tot = 0;
     for (int w = 0; w < 32; ++w) tot += warp_sum[w];

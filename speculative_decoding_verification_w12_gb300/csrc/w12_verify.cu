@@ -50,7 +50,7 @@ __device__ __forceinline__ void block_argmax(float& bv, int& bi) {
     sv[w] = bv;
     si[w] = bi;
   }
-  __syncthreads();
+  cta_sync();
   if (w == 0) {
     bv = lane < 8 ? sv[lane] : -INFINITY;
     bi = lane < 8 ? si[lane] : 0x7FFFFFFF;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(256) reduce_accept_kernel(
     const int old = atomicAdd(done, 1);
     is_last = old == M - 1;
   }
-  __syncthreads();
+  cta_sync();
   if (!is_last) return;
   __threadfence();
   if (threadIdx.x == 0) *done = 0;
