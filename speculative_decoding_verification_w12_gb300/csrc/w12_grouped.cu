@@ -226,7 +226,7 @@ struct Bars {
   uint64_t* gather;
 };
 
-template <bool kW12, bool kArgmax, bool kMulti>
+template <bool kW12, bool kArgmax, int kMode>
 __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps TM, const __grid_constant__ GemmParams P) {
   using C = Cfg<kW12>;
@@ -263,7 +263,14 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   const int c = blockIdx.x;
   const int G = P.grid;
   const int n_units = cta_units(P, c);          // this CTA's units over all phases
-  constexpr bool single = !kMulti;  // one problem, one phase: problem 0 everywhere
+  // kMode 0: one problem, one phase (problem 0 everywhere); 1: several
+  // problems; 2: several problems with a SwiGLU link. The link's code (its
+  // flag polling and act blocks) is compiled only into mode 2, and the
+  // bookkeeping of several problems only into modes 1 and 2: the hot loops of
+  // every role stay small (instruction cache) and within registers.
+  constexpr bool kMulti = kMode != 0;
+  constexpr bool kGlu = kMode == 2;
+  constexpr bool single = !kMulti;
   const uint64_t lim = P.limit_ns;
 
   if (threadIdx.x == 0) {
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
       }
       grid_dep_wait();
-      const int32_t epoch = kMulti && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
+      const int32_t epoch = kGlu && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           mbar_arrive_expect_tx(&B.full[s], tx);
           load_w(x, st, &B.full[s]);
         }
-        if (kMulti && x.p == P.glu_to && !gave_up) {
+        if (kGlu && x.p == P.glu_to && !gave_up) {
           // X of this problem is written by this launch: wait until its
           // k-block is ready (bounded), then make it visible to the copy. If
           // the wait gives up, the copies are still issued (of stale data) so
@@ -515,9 +522,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       uint8_t* uprob = smem + plan.uprob_off;
       // The CTA's range in each phase: its first unit and where the range
       // starts in the CTA's sequence.
+      // (Arrays indexed only by unrolled loop counters, so that they stay in
+      // registers.)
       int64_t fb[kMaxProb];
       int fs[kMaxProb + 1];
       fs[0] = 0;
+#pragma unroll
       for (int f = 0; f < kMaxProb; ++f) {
         const bool on = f < P.nphase;
         fb[f] = on ? pbegin(P, c, f) : 0;
@@ -531,8 +541,16 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           const int i = i0 + lane + 32 * j;
           if (i < n_units) {
             int f = 0;
-            while (f + 1 < P.nphase && i >= fs[f + 1]) ++f;
-            const int64_t u = fb[f] + (i - fs[f]);
+            int64_t fbf = fb[0];
+            int fsf = 0;
+#pragma unroll
+            for (int q2 = 1; q2 < kMaxProb; ++q2)
+              if (q2 < P.nphase && i >= fs[q2]) {
+                f = q2;
+                fbf = fb[q2];
+                fsf = fs[q2];
+              }
+            const int64_t u = fbf + (i - fsf);
             const int p = prob_of(P, f, u);
             const int64_t loc = u - P.pr[p].unit0;
             va[j] = P.pr[p].exc_off[loc];
@@ -796,7 +814,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     };
 
     grid_dep_wait();
-    const int32_t epoch = kMulti && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
+    const int32_t epoch = kGlu && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
     // Tile t of the SwiGLU source problem is complete in Y: the CTA that
     // completes the second tile of block j writes act block j and publishes it.
     auto glu_tile_done = [&](int t) {
@@ -841,38 +859,39 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     int iseq = 0;  // index of the segment's first unit in the CTA's sequence
     // Walk the CTA's segments (its runs of units of one tile) phase by phase;
     // only (phase, next unit, end of range) is carried between segments.
+    // Unit numbers fit in 32 bits (the host checks every phase's count).
     int fn = 0;
-    int64_t un = pbegin(P, c, 0), uen = pbegin(P, c + 1, 0);
+    int un = int(pbegin(P, c, 0)), uen = int(pbegin(P, c + 1, 0));
     bool more = un < uen;
     if constexpr (kMulti) {
       for (fn = 1; fn < P.nphase && !more; ++fn) {
-        un = pbegin(P, c, fn);
-        uen = pbegin(P, c + 1, fn);
+        un = int(pbegin(P, c, fn));
+        uen = int(pbegin(P, c + 1, fn));
         more = un < uen;
       }
       --fn;
       if (!more) fn = 0;
     }
-    const int64_t ub0 = un;
+    const int ub0 = un;
     while (more) {
       const int f = kMulti ? fn : 0;
       const int64_t Uf = P.phase_units[f];
       const int Gf = phase_ctas(P, f);
-      const int64_t ub = kMulti ? pbegin(P, c, f) : ub0, ue = uen;
+      const int ub = kMulti ? int(pbegin(P, c, f)) : ub0, ue = uen;
       const int pi = kMulti ? prob_of(P, f, un) : 0;
       const int KBp = P.pr[pi].KB;
-      const int64_t u0p = kMulti ? P.pr[pi].unit0 : 0;
-      const int t = int((un - u0p) / KBp);
-      const int64_t tile_u0 = u0p + int64_t(t) * KBp;
-      const int64_t seg_begin = un;
-      const int64_t seg_end = tile_u0 + KBp < ue ? tile_u0 + KBp : ue;
+      const int u0p = kMulti ? int(P.pr[pi].unit0) : 0;
+      const int t = (un - u0p) / KBp;
+      const int tile_u0 = u0p + t * KBp;
+      const int seg_begin = un;
+      const int seg_end = tile_u0 + KBp < ue ? tile_u0 + KBp : ue;
       un = seg_end;
       more = un < uen;
       if constexpr (kMulti) {
         if (!more) {
           for (++fn; fn < P.nphase && !more; ++fn) {
-            un = pbegin(P, c, fn);
-            uen = pbegin(P, c + 1, fn);
+            un = int(pbegin(P, c, fn));
+            uen = int(pbegin(P, c + 1, fn));
             more = un < uen;
           }
           --fn;
@@ -982,7 +1001,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&B.acc_empty[cur]);
         if (pref && et == 0) P.counters[gt] = 0;  // every other contributor has already counted
-        if (kMulti && pi == P.glu_from) glu_tile_done(t);
+        if (kGlu && pi == P.glu_from) glu_tile_done(t);
       } else {
         // In the final segment every stage of the ring has been consumed (the
         // segment's MMAs completed), so the other pieces' partials can be
@@ -1084,7 +1103,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
         if (last && et == 0) P.counters[gt] = 0;
         named_bar_sync(kEpiBar, 128);
-        if (kMulti && last && pi == P.glu_from) glu_tile_done(t);
+        if (kGlu && last && pi == P.glu_from) glu_tile_done(t);
       }
     }
     // Partials requested into shared memory must land before the CTA exits.
@@ -1096,7 +1115,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (kMulti && P.glu_to >= 0 && threadIdx.x == 0) {
+  if (kGlu && P.glu_to >= 0 && threadIdx.x == 0) {
     // The last CTA to finish moves the launch epoch on, so the next launch
     // on this workspace tells its ready flags from this one's.
     const int32_t e = *reinterpret_cast<volatile int32_t*>(P.epoch);
@@ -1107,7 +1126,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   }
 }
 
-template <bool kW12, bool kArgmax, bool kMulti>
+template <bool kW12, bool kArgmax, int kMode>
 static int launch_impl(int Mpad, GemmParams& P, const GemmMaps& TM, cudaStream_t stream) {
   // Deepest ring that fits next to the fixed carve-up.
   const int smem_max = 232448;
@@ -1124,7 +1143,7 @@ static int launch_impl(int Mpad, GemmParams& P, const GemmMaps& TM, cudaStream_t
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
   P.issuers = issuers;
-  auto kern = gemm_kernel<kW12, kArgmax, kMulti>;
+  auto kern = gemm_kernel<kW12, kArgmax, kMode>;
   static bool attr_set[64] = {false};  // per device; setting it twice is harmless
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
@@ -1256,6 +1275,9 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
   int64_t per_cta = 0;
   for (int f = 0; f < g->nphase; ++f) per_cta += (g->phase_units[f] + g->grid - 1) / g->grid;
   if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
+  // The kernel numbers a phase's units (problem offsets included) in 32 bits.
+  for (int f = 0; f < g->nphase; ++f)
+    if (g->phase_units[f] > (int64_t(1) << 30)) return W12_ERR_SHAPE;
   if (to >= 0) {
     g->glu_from = 0;
     g->glu_to = n - 1;
@@ -1334,8 +1356,15 @@ static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_
   P.epoch = reinterpret_cast<int32_t*>(wsb + g.epoch);
   P.status = dev_status;
   P.limit_ns = wait_limit_ns();
-  return w12_mode ? launch_impl<true, false, true>(g.Mpad, P, TM, stream)
-                  : launch_impl<false, false, true>(g.Mpad, P, TM, stream);
+  // One problem runs the single-problem form; a SwiGLU link the linked form.
+  if (link)
+    return w12_mode ? launch_impl<true, false, 2>(g.Mpad, P, TM, stream)
+                    : launch_impl<false, false, 2>(g.Mpad, P, TM, stream);
+  if (n == 1)
+    return w12_mode ? launch_impl<true, false, 0>(g.Mpad, P, TM, stream)
+                    : launch_impl<false, false, 0>(g.Mpad, P, TM, stream);
+  return w12_mode ? launch_impl<true, false, 1>(g.Mpad, P, TM, stream)
+                  : launch_impl<false, false, 1>(g.Mpad, P, TM, stream);
 }
 
 }  // namespace grouped_impl
