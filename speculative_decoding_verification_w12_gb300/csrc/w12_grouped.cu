@@ -63,6 +63,7 @@ struct ProbParams {
 
 struct GemmParams {
   int M, Mpad, grid, stages, issuers, nprob, nphase;
+  int cta0[kMaxProb + 1];             // partitioned form: CTAs [cta0[p], cta0[p+1]) take problem p
   int pfirst[kMaxProb];               // first problem of each phase (problems are ordered by phase)
   int64_t phase_units[kMaxProb];
   ProbParams pr[kMaxProb];
@@ -143,6 +144,18 @@ __device__ __forceinline__ bool cur_phase(const GemmParams& P, int c, int f, Cur
     }
   }
   return false;
+}
+
+// First unit (ub, within problem p) of a CTA running one problem.
+__device__ __forceinline__ void cur_single(const GemmParams& P, int p, int64_t ub, int n, Cur& x) {
+  x.f = 0;
+  x.p = p;
+  x.KB = P.pr[p].KB;
+  x.tiles = P.pr[p].tiles;
+  x.t = int(ub / x.KB);
+  x.kb = int(ub % x.KB);
+  x.left = n;
+  x.pos = 0;
 }
 
 // Next unit of the CTA's sequence.
@@ -260,17 +273,28 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int c = blockIdx.x;
-  const int G = P.grid;
-  const int n_units = cta_units(P, c);          // this CTA's units over all phases
   // kMode 0: one problem, one phase (problem 0 everywhere); 1: several
-  // problems; 2: several problems with a SwiGLU link. The link's code (its
-  // flag polling and act blocks) is compiled only into mode 2, and the
-  // bookkeeping of several problems only into modes 1 and 2: the hot loops of
-  // every role stay small (instruction cache) and within registers.
-  constexpr bool kMulti = kMode != 0;
+  // problems; 2: several problems with a SwiGLU link; 3: several independent
+  // problems, each CTA on one of them (partitioned: the CTAs are split over
+  // the problems in proportion to their units, and every CTA runs the
+  // one-problem code on its problem, place c among its G). The link's code
+  // (its flag polling and act blocks) is compiled only into mode 2, and the
+  // bookkeeping of several problems per CTA only into modes 1 and 2: the hot
+  // loops of every role stay small (instruction cache) and within registers.
+  constexpr bool kMulti = kMode == 1 || kMode == 2;
   constexpr bool kGlu = kMode == 2;
   constexpr bool single = !kMulti;
+  int pc = 0, c = blockIdx.x, G = P.grid;  // this CTA's problem (one-problem code) and place among its CTAs
+  if constexpr (kMode == 3) {
+    while (pc + 1 < P.nprob && c >= P.cta0[pc + 1]) ++pc;
+    c -= P.cta0[pc];
+    G = P.cta0[pc + 1] - P.cta0[pc];
+  }
+  // One-problem code: the problem's units, split evenly over Gc CTAs.
+  const int64_t Uc = single ? int64_t(P.pr[pc].KB) * P.pr[pc].tiles : 0;
+  const int Gc = single ? (Uc < G ? int(Uc) : G) : 0;
+  auto sbegin = [&](int cc) { return unit_begin(cc < Gc ? cc : Gc, Uc, Gc); };
+  const int n_units = single ? int(sbegin(c + 1) - sbegin(c)) : cta_units(P, c);  // this CTA's units
   const uint64_t lim = P.limit_ns;
 
   if (threadIdx.x == 0) {
@@ -348,7 +372,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint32_t txx = 2u * xbox;
       // Weight tile of the unit at cursor x into stage buffer st.
       auto load_w = [&](const Cur& x, uint8_t* st, uint64_t* bar) {
-        const int pp = single ? 0 : x.p;
+        const int pp = x.p;
         const CUtensorMap* m = TM.m[pp];
         if (kW12) {
           tma_load_2d_hint(st, &m[0], x.kb * 64, x.t * 128, bar, pol_w);
@@ -365,7 +389,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // anything else is read or written, only after that wait.
       const int prefill = n_units < S ? n_units : S;
       Cur x;
-      cur_phase(P, c, 0, x);
+      if (single)
+        cur_single(P, pc, sbegin(c), n_units, x);
+      else
+        cur_phase(P, c, 0, x);
       // One problem: plain (t, kb) counters, as cheap as possible per unit.
       auto step = [&](Cur& y) {
         if (kMulti) {
@@ -416,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           }
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-        const CUtensorMap* mx = &TM.m[single ? 0 : x.p][3];
+        const CUtensorMap* mx = &TM.m[x.p][3];
         mbar_arrive_expect_tx(&B.full_x[s], txx);
         tma_load_2d_hint(st + plan.x_off, mx, x.kb * 128, 0, &B.full_x[s], pol_x);
         tma_load_2d_hint(st + plan.x_off + xbox, mx, x.kb * 128 + 64, 0, &B.full_x[s], pol_x);
@@ -453,7 +480,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint64_t adesc0 = sdesc_k_sw128(st0);
       const uint32_t a_tmem0 = tmem_base + a_col0;
       Cur x;
-      cur_phase(P, c, 0, x);
+      if (single)
+        cur_single(P, pc, sbegin(c), n_units, x);
+      else
+        cur_phase(P, c, 0, x);
       int s = 0, accb = 0;
       uint32_t ph = 0, accph = 0;
       bool started = false;  // this issuer has written its accumulator in the current segment
@@ -581,9 +611,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     } else if (kW12) {
       uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
       uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
-      const int64_t ub = unit_begin(c, P.phase_units[0], G);
-      const uint32_t* exc_off = P.pr[0].exc_off;
-      const uint32_t* exc_ent = P.pr[0].exc_ent;
+      const int64_t ub = sbegin(c);
+      const uint32_t* exc_off = P.pr[pc].exc_off;
+      const uint32_t* exc_ent = P.pr[pc].exc_ent;
       // Every load of a batch is issued before the batch's first store, so the
       // window costs one memory round trip per batch rather than one per 32
       // values: the decoders cannot start before this warp arrives.
@@ -599,7 +629,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
       __syncwarp();
       const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
-      bool bad = e1 < e0 || int64_t(e1) > P.pr[0].n_exc;
+      bool bad = e1 < e0 || int64_t(e1) > P.pr[pc].n_exc;
       const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
       if (fits) {
         constexpr int kBatch = 16;  // entries per lane in flight
@@ -649,7 +679,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     };
     const uint8_t* uprob = smem + plan.uprob_off;
     auto prep = [&](int i, Exc& x) {
-      const ProbParams& pp = P.pr[single ? 0 : uprob[i]];
+      const ProbParams& pp = P.pr[single ? pc : uprob[i]];
       x.o0 = soff[i];
       x.o1 = single ? soff[i + 1] : sent[i];
       if (x.o1 < x.o0 || int64_t(x.o1) > pp.n_exc || x.o0 < e_base || x.o1 > e_end) {
@@ -725,7 +755,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             uint32_t e2 = kInvalidEnt;
             if (bst + lane < cur.o1) {
               const uint32_t v =
-                  in_smem ? sent[bst - e_base + lane] : __ldg(P.pr[single ? 0 : uprob[i]].exc_ent + bst + lane);
+                  in_smem ? sent[bst - e_base + lane] : __ldg(P.pr[single ? pc : uprob[i]].exc_ent + bst + lane);
               seen |= v;
               e2 = (v >> 30) ? kInvalidEnt : v;
             }
@@ -861,7 +891,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     // only (phase, next unit, end of range) is carried between segments.
     // Unit numbers fit in 32 bits (the host checks every phase's count).
     int fn = 0;
-    int un = int(pbegin(P, c, 0)), uen = int(pbegin(P, c + 1, 0));
+    int un = int(single ? sbegin(c) : pbegin(P, c, 0)), uen = int(single ? sbegin(c + 1) : pbegin(P, c + 1, 0));
     bool more = un < uen;
     if constexpr (kMulti) {
       for (fn = 1; fn < P.nphase && !more; ++fn) {
@@ -875,10 +905,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const int ub0 = un;
     while (more) {
       const int f = kMulti ? fn : 0;
-      const int64_t Uf = P.phase_units[f];
-      const int Gf = phase_ctas(P, f);
+      const int64_t Uf = single ? Uc : P.phase_units[f];
+      const int Gf = single ? Gc : phase_ctas(P, f);
       const int ub = kMulti ? int(pbegin(P, c, f)) : ub0, ue = uen;
-      const int pi = kMulti ? prob_of(P, f, un) : 0;
+      const int pi = kMulti ? prob_of(P, f, un) : pc;
       const int KBp = P.pr[pi].KB;
       const int u0p = kMulti ? int(P.pr[pi].unit0) : 0;
       const int t = (un - u0p) / KBp;
@@ -900,7 +930,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const bool final_seg = !more;  // the CTA's last segment: the ring is idle once it is accumulated
       const int ia = kMulti ? iseq : int(seg_begin - ub0), nseg = int(seg_end - seg_begin);
       if (kMulti) iseq += nseg;
-      const int gt = (kMulti ? P.pr[pi].tile0 : 0) + t;   // launch-wide tile number (counters)
+      const int gt = P.pr[pi].tile0 + t;   // launch-wide tile number (counters)
       const int cur = accb;
       const uint32_t cur_ph = accph;
       if (++accb == NACC) {
@@ -915,8 +945,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // CTA cc has two slots per phase: its first piece in the phase, and
       // its last.
       auto slot_of = [&](int cc) {
-        const int64_t u0 = pbegin(P, cc, f);
-        return 2 * (cc * P.nphase + f) + ((u0 >= tile_u0 && u0 < tile_u0 + KBp) ? 0 : 1);
+        const int64_t u0 = single ? sbegin(cc) : pbegin(P, cc, f);
+        const int cg = kMode == 3 ? P.cta0[pi] + cc : cc;  // launch-wide CTA
+        return 2 * (cg * P.nphase + f) + ((u0 >= tile_u0 && u0 < tile_u0 + KBp) ? 0 : 1);
       };
       // The CTA's final segment ends the kernel. When its tile has one other
       // piece and that piece is already done (it was the first piece its CTA
@@ -1019,7 +1050,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           fast = *fast_flag;
         }
         if (!fast) {
-          const int slot = 2 * (c * P.nphase + f) + (seg_begin == ub ? 0 : 1);
+          const int slot = 2 * (int(blockIdx.x) * P.nphase + f) + (seg_begin == ub ? 0 : 1);
           float4* my = reinterpret_cast<float4*>(P.parts + size_t(slot) * P.Mpad * 128);
           for (int mc = 0; mc < nchunks; ++mc) {
             float v[16];
@@ -1214,6 +1245,8 @@ static void set_problem(ProbParams& q, bool w12_mode, const w12_weights* W, int6
 // workspace carve-up.
 struct Grouped {
   int n, order[kMaxProb], phase[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks;
+  bool part;                   // partitioned: each CTA runs one problem
+  int cta0[kMaxProb + 1];      // partitioned: CTAs [cta0[j], cta0[j+1]) take launch problem j
   int64_t N[kMaxProb], K[kMaxProb], phase_units[kMaxProb];
   size_t counters, glu_cnt, glu_ready, epoch, parts, total;
 };
@@ -1274,6 +1307,34 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
   g->grid = int(maxu < sms ? maxu : sms);
   int64_t per_cta = 0;
   for (int f = 0; f < g->nphase; ++f) per_cta += (g->phase_units[f] + g->grid - 1) / g->grid;
+  // Several independent problems: the CTAs are split over the problems so
+  // that the largest per-CTA share of units is as small as it can be (one
+  // CTA at a time to the problem whose CTAs carry the most units each).
+  // Units weigh the same bytes in every problem.
+  g->part = !link && n >= 2 && g->grid >= n;
+  if (g->part) {
+    int64_t U[kMaxProb];
+    int cnt[kMaxProb];
+    for (int j = 0; j < n; ++j) {
+      U[j] = (g->N[g->order[j]] / kGroup) * (g->K[g->order[j]] / kGroup);
+      cnt[j] = 1;
+    }
+    for (int left = g->grid - n; left > 0; --left) {
+      int best = -1;
+      for (int j = 0; j < n; ++j)
+        if (cnt[j] < U[j] && (best < 0 || U[j] * cnt[best] > U[best] * cnt[j])) best = j;
+      if (best < 0) break;
+      ++cnt[best];
+    }
+    per_cta = 0;
+    g->cta0[0] = 0;
+    for (int j = 0; j < n; ++j) {
+      g->cta0[j + 1] = g->cta0[j] + cnt[j];
+      const int64_t q = (U[j] + cnt[j] - 1) / cnt[j];
+      per_cta = q > per_cta ? q : per_cta;
+    }
+    g->grid = g->cta0[n];
+  }
   if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
   // The kernel numbers a phase's units (problem offsets included) in 32 bits.
   for (int f = 0; f < g->nphase; ++f)
@@ -1356,13 +1417,18 @@ static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_
   P.epoch = reinterpret_cast<int32_t*>(wsb + g.epoch);
   P.status = dev_status;
   P.limit_ns = wait_limit_ns();
-  // One problem runs the single-problem form; a SwiGLU link the linked form.
+  for (int j = 0; j <= n; ++j) P.cta0[j] = g.part ? g.cta0[j] : 0;
+  // One problem runs the single-problem form; a SwiGLU link the linked form;
+  // several independent problems the partitioned form.
   if (link)
     return w12_mode ? launch_impl<true, false, 2>(g.Mpad, P, TM, stream)
                     : launch_impl<false, false, 2>(g.Mpad, P, TM, stream);
   if (n == 1)
     return w12_mode ? launch_impl<true, false, 0>(g.Mpad, P, TM, stream)
                     : launch_impl<false, false, 0>(g.Mpad, P, TM, stream);
+  if (g.part)
+    return w12_mode ? launch_impl<true, false, 3>(g.Mpad, P, TM, stream)
+                    : launch_impl<false, false, 3>(g.Mpad, P, TM, stream);
   return w12_mode ? launch_impl<true, false, 1>(g.Mpad, P, TM, stream)
                   : launch_impl<false, false, 1>(g.Mpad, P, TM, stream);
 }
