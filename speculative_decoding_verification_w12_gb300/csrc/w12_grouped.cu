@@ -11,7 +11,10 @@
 // and every CTA works through its share of each in turn; each down k-block
 // waits (bounded) for a per-block ready flag written by the CTA that completes
 // the block's two gate/up tiles. Flags carry a launch epoch, moved on by the
-// last CTA to finish, so one workspace serves consecutive launches.
+// last CTA to finish, so one workspace serves consecutive launches. A count of
+// the blocks written so far lets a CTA that finds every block ready stop
+// reading flags: a flag read is a round trip to L2 that the copy thread would
+// otherwise take once per down unit.
 //
 // The kernel body follows the single-GEMM kernel of this library (warp roles,
 // ring, TMEM buffers, stream-K fixup), generalised from one problem to a list
@@ -79,7 +82,7 @@ struct GemmParams {
   uint16_t* act;
   int32_t* glu_cnt;                   // per block: tiles completed (reset to 0 by the writer)
   int32_t* glu_ready;                 // per block: epoch + 1 once written
-  int32_t* epoch;                     // [0] launch epoch, [1] CTAs finished in this launch
+  int32_t* epoch;                     // [0] launch epoch, [1] CTAs finished, [2] act blocks written (this launch)
   int32_t* status;
   uint64_t limit_ns;
 };
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       uint32_t ph = 0;
       int issued = 0;
       bool gave_up = false;
+      bool all_ready = false;  // every act block is written: no more flags to read
       for (; issued < n_units; ++issued) {
         uint8_t* st = smem + s * plan.stage_bytes;
         if (issued >= prefill) {
@@ -423,23 +427,26 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           mbar_arrive_expect_tx(&B.full[s], tx);
           load_w(x, st, &B.full[s]);
         }
-        if (kGlu && x.p == P.glu_to && !gave_up) {
+        if (kGlu && x.p == P.glu_to && !gave_up && !all_ready) {
           // X of this problem is written by this launch: wait until its
           // k-block is ready (bounded), then make it visible to the copy. If
           // the wait gives up, the copies are still issued (of stale data) so
           // that every stage's byte count completes; the status word and the
           // abort flag already report the failure.
-          const int32_t* rdy = P.glu_ready + x.kb;
-          bool okr = ld_acquire_gpu(rdy) == epoch + 1;
-          const uint64_t t0 = globaltimer_ns();
-          while (!okr) {
-            if (*abort_flag || globaltimer_ns() - t0 > lim) {
-              fail(W12_ERR_TIMEOUT);
-              gave_up = true;
-              break;
+          all_ready = ld_acquire_gpu(P.epoch + 2) == P.glu_blocks;
+          if (!all_ready) {
+            const int32_t* rdy = P.glu_ready + x.kb;
+            bool okr = ld_acquire_gpu(rdy) == epoch + 1;
+            const uint64_t t0 = globaltimer_ns();
+            while (!okr) {
+              if (*abort_flag || globaltimer_ns() - t0 > lim) {
+                fail(W12_ERR_TIMEOUT);
+                gave_up = true;
+                break;
+              }
+              __nanosleep(100);  // back off: every SM may be polling the same few flags
+              okr = ld_acquire_gpu(rdy) == epoch + 1;
             }
-            __nanosleep(100);  // back off: every SM may be polling the same few flags
-            okr = ld_acquire_gpu(rdy) == epoch + 1;
           }
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
@@ -880,6 +887,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         if (et == 0) {
           P.glu_cnt[j] = 0;
           st_release_gpu(P.glu_ready + j, epoch + 1);
+          atomic_add_acq_rel_gpu(P.epoch + 2, 1);
         }
       }
     };
@@ -1152,6 +1160,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const int32_t e = *reinterpret_cast<volatile int32_t*>(P.epoch);
     if (atomic_add_acq_rel_gpu(P.epoch + 1, 1) == G - 1) {
       P.epoch[1] = 0;
+      P.epoch[2] = 0;
       st_release_gpu(P.epoch, e + 1);
     }
   }
@@ -1353,7 +1362,7 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
   g->counters = take(sizeof(int32_t) * size_t(g->tiles));
   g->glu_cnt = take(sizeof(int32_t) * size_t(g->glu_blocks > 0 ? g->glu_blocks : 1));
   g->glu_ready = take(sizeof(int32_t) * size_t(g->glu_blocks > 0 ? g->glu_blocks : 1));
-  g->epoch = take(sizeof(int32_t) * 2);
+  g->epoch = take(sizeof(int32_t) * 4);
   g->parts = take(sizeof(float) * size_t(2) * g->nphase * g->grid * g->Mpad * kGroup);
   g->total = off;
   return W12_OK;
