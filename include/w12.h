@@ -165,16 +165,18 @@ int w12_gemm_bf16_ref(const uint16_t* X, int64_t M, const uint16_t* W, int64_t N
 /* --- Grouped verify GEMMs in one launch -------------------------------- */
 /* The verify pass reads every target weight each step (SpecPilot digest,
  * summary); a dense layer has several such GEMMs at the same M. A grouped
- * launch runs up to 4 of them in one persistent kernel: their 128x128 units
- * are split evenly over the SMs as one stream (one ramp-up and one tail for
- * the group instead of one per GEMM). With a SwiGLU link, problem `to` takes
+ * launch runs up to 4 of them in one persistent kernel (one ramp-up and one
+ * tail for the group instead of one per GEMM): the SMs are split over the
+ * problems in proportion to their 128x128 units, and each problem's units are
+ * split evenly over its SMs. With a SwiGLU link, problem `to` takes
  * as X the gated activation of problem `from`'s output, computed inside the
  * launch: act[m, j] = bf16(silu(Y_from[m, j]) * Y_from[m, N_from/2 + j]),
  * silu(g) = g / (1 + exp(-g)), rounded to nearest even. The pages give no
  * MLP activation; this is the gated SiLU of dense decoder layers, with the
- * gate in the first half of the fused gate/up output. The source's units
- * run first, then the other problems', then the target's; each of the
- * target's k-blocks starts once that block of act is written.
+ * gate in the first half of the fused gate/up output. The launch then runs
+ * in three phases, the SMs split anew in each: the source, the other
+ * problems, the target; each of the target's k-blocks starts once that block
+ * of act is written.
  *
  * problems: X [M, K] bf16 row-major (16-byte aligned; unused for the link
  * target), weights (W for w12_gemm_grouped; Wbf16 with N, K for the bf16

@@ -50,13 +50,15 @@ constexpr int kScratchStride = 129;   // floats per column in the argmax transpo
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
 
 // One GEMM of a launch. A launch runs up to kMaxProb GEMMs (problems) that
-// share M, in up to kMaxProb phases: the units of each phase are split evenly
-// over the CTAs (stream-K over the phase's concatenated problems), and every
-// CTA works through its share of each phase in turn. The last phase holds
-// the problem whose X is produced inside the launch (the SwiGLU link below).
+// share M, in up to three phases (problems are ordered by phase). In every
+// phase the CTAs are split over the phase's problems in proportion to their
+// units; the CTAs of one problem share its units evenly (stream-K over the
+// problem), so each CTA runs one job per phase: a range of consecutive units
+// of one problem. The last phase holds the problem whose X is produced inside
+// the launch (the SwiGLU link below).
 struct ProbParams {
   int N, K, KB, tiles, phase, tile0;  // tile0: first of its tiles in the launch-wide tile numbering
-  int64_t unit0;                      // first unit of the problem in its phase's unit numbering
+  int cta0, cta1;                     // the problem's CTAs [cta0, cta1) in its phase
   const uint8_t* ebase;
   const uint32_t* exc_off;
   const uint32_t* exc_ent;
@@ -66,9 +68,6 @@ struct ProbParams {
 
 struct GemmParams {
   int M, Mpad, grid, stages, issuers, nprob, nphase;
-  int cta0[kMaxProb + 1];             // partitioned form: CTAs [cta0[p], cta0[p+1]) take problem p
-  int pfirst[kMaxProb];               // first problem of each phase (problems are ordered by phase)
-  int64_t phase_units[kMaxProb];
   ProbParams pr[kMaxProb];
   float* parts;                       // split-K partial slots: 2 per CTA per phase
   int32_t* counters;                  // one per tile of the launch
@@ -92,13 +91,20 @@ struct GemmMaps {
   CUtensorMap m[kMaxProb][4];
 };
 
-// Position of a unit in a CTA's sequence: phase f, problem p, the problem's
-// tile t and k-block kb, with the problem's KB and tile count cached; left =
-// units of the CTA still to come in this phase (this one included), pos =
-// this unit's place in the CTA's range of the phase. Single-thread loops
-// advance it per unit with 32-bit steps only.
+// A CTA's job in one phase: units [b, b + n) of problem p, whose U units are
+// shared by G CTAs, this one at place cl; s0 = index of the job's first unit
+// in the CTA's sequence. Exception entries of the job: positions [e0, e1) of
+// the CTA's staged window, entry g0 + (position - e0) of the problem's list.
+struct Job {
+  int p, f, cl, G, U, b, n, s0;
+  uint32_t e0, e1, g0, pad;
+};
+
+// Position of a unit in a CTA's sequence: job j (problem p), the problem's
+// tile t and k-block kb, with the problem's KB cached; left = units of the
+// job still to come (this one included), pos = this unit's place in the job.
 struct Cur {
-  int f, p, t, kb, KB, tiles, left, pos;
+  int j, p, t, kb, KB, left, pos;
 };
 
 __device__ __forceinline__ int64_t unit_begin(int c, int64_t U, int G) { return int64_t(c) * U / G; }
@@ -108,83 +114,30 @@ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int G) {
   return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
 }
 
-// A phase with fewer units than CTAs is shared by its first phase_units CTAs
-// only (one unit each), so that the CTAs holding pieces of one tile are
-// always consecutive; pbegin(c) is the first unit of CTA c in phase f (the
-// phase's unit count for CTAs past the sharing ones).
-__device__ __forceinline__ int phase_ctas(const GemmParams& P, int f) {
-  return P.phase_units[f] < P.grid ? int(P.phase_units[f]) : P.grid;
-}
-
-__device__ __forceinline__ int64_t pbegin(const GemmParams& P, int c, int f) {
-  const int Gf = phase_ctas(P, f);
-  return unit_begin(c < Gf ? c : Gf, P.phase_units[f], Gf);
-}
-
-// Problem of phase f that holds phase unit u.
-__device__ __forceinline__ int prob_of(const GemmParams& P, int f, int64_t u) {
-  int p = P.pfirst[f];
-  while (p + 1 < P.nprob && P.pr[p + 1].phase == f && u >= P.pr[p + 1].unit0) ++p;
-  return p;
-}
-
-// First unit of CTA c at or after phase f; false if it has none.
-__device__ __forceinline__ bool cur_phase(const GemmParams& P, int c, int f, Cur& x) {
-  for (; f < P.nphase; ++f) {
-    const int64_t ub = pbegin(P, c, f);
-    const int64_t ue = pbegin(P, c + 1, f);
-    if (ub < ue) {
-      x.f = f;
-      x.p = prob_of(P, f, ub);
-      x.KB = P.pr[x.p].KB;
-      x.tiles = P.pr[x.p].tiles;
-      const int64_t loc = ub - P.pr[x.p].unit0;
-      x.t = int(loc / x.KB);
-      x.kb = int(loc % x.KB);
-      x.left = int(ue - ub);
-      x.pos = 0;
-      return true;
-    }
-  }
-  return false;
-}
-
-// First unit (ub, within problem p) of a CTA running one problem.
-__device__ __forceinline__ void cur_single(const GemmParams& P, int p, int64_t ub, int n, Cur& x) {
-  x.f = 0;
+// Cursor at unit ub of problem p, n units to go in the job.
+__device__ __forceinline__ void cur_at(const GemmParams& P, int j, int p, int ub, int n, Cur& x) {
+  x.j = j;
   x.p = p;
   x.KB = P.pr[p].KB;
-  x.tiles = P.pr[p].tiles;
-  x.t = int(ub / x.KB);
-  x.kb = int(ub % x.KB);
+  x.t = ub / x.KB;
+  x.kb = ub % x.KB;
   x.left = n;
   x.pos = 0;
 }
 
-// Next unit of the CTA's sequence.
-__device__ __forceinline__ bool cur_next(const GemmParams& P, int c, Cur& x) {
+// Next unit of a job-table sequence (the next job's first unit after the
+// last unit of a job).
+__device__ __forceinline__ void cur_step(const GemmParams& P, const Job* J, int njobs, Cur& x) {
   if (--x.left > 0) {
     ++x.pos;
     if (++x.kb == x.KB) {
       x.kb = 0;
-      if (++x.t == x.tiles) {
-        x.t = 0;
-        ++x.p;
-        x.KB = P.pr[x.p].KB;
-        x.tiles = P.pr[x.p].tiles;
-      }
+      ++x.t;
     }
-    return true;
+  } else if (x.j + 1 < njobs) {
+    const int j = x.j + 1;
+    cur_at(P, j, J[j].p, J[j].b, J[j].n, x);
   }
-  return cur_phase(P, c, x.f + 1, x);
-}
-
-// Units of CTA c over all phases.
-__device__ __forceinline__ int cta_units(const GemmParams& P, int c) {
-  int n = 0;
-  for (int f = 0; f < P.nphase; ++f)
-    n += int(pbegin(P, c + 1, f) - pbegin(P, c, f));
-  return n;
 }
 
 template <bool kW12>
@@ -200,7 +153,7 @@ struct Cfg {
 // Shared memory carve-up (identical on host and device).
 struct SmemPlan {
   uint32_t stage_bytes, x_off, eb_off, stages;
-  uint32_t scratch_off, red_off, soff_off, sent_off, uprob_off, bar_off, misc_off, total;
+  uint32_t scratch_off, red_off, soff_off, sent_off, uprob_off, bar_off, misc_off, job_off, total;
 };
 
 template <bool kW12>
@@ -226,6 +179,8 @@ __host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
   off += 64 * 8;
   p.misc_off = off;
   off += 64;
+  p.job_off = off;
+  off += kMaxProb * sizeof(Job);
   p.total = off + 1024;  // slack for 1024-byte alignment of the base
   return p;
 }
@@ -276,28 +231,29 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // kMode 0: one problem, one phase (problem 0 everywhere); 1: several
-  // problems; 2: several problems with a SwiGLU link; 3: several independent
-  // problems, each CTA on one of them (partitioned: the CTAs are split over
-  // the problems in proportion to their units, and every CTA runs the
-  // one-problem code on its problem, place c among its G). The link's code
-  // (its flag polling and act blocks) is compiled only into mode 2, and the
-  // bookkeeping of several problems per CTA only into modes 1 and 2: the hot
-  // loops of every role stay small (instruction cache) and within registers.
-  constexpr bool kMulti = kMode == 1 || kMode == 2;
+  // kMode 0: one phase of independent problems, each CTA on one of them
+  // (with one problem, every CTA on it): the one-problem code, on problem pc
+  // at place c among its G CTAs. kMode 2: the phases of a SwiGLU link, one job
+  // per phase (gate/up; the other problems; down), read from the CTA's job
+  // table. The link's code (job table, flag polling, act blocks) is compiled
+  // only into mode 2: the hot loops of every role stay small (instruction
+  // cache) and within registers.
+  constexpr bool kMulti = kMode == 2;
   constexpr bool kGlu = kMode == 2;
   constexpr bool single = !kMulti;
-  int pc = 0, c = blockIdx.x, G = P.grid;  // this CTA's problem (one-problem code) and place among its CTAs
-  if constexpr (kMode == 3) {
-    while (pc + 1 < P.nprob && c >= P.cta0[pc + 1]) ++pc;
-    c -= P.cta0[pc];
-    G = P.cta0[pc + 1] - P.cta0[pc];
+  Job* J = reinterpret_cast<Job*>(smem + plan.job_off);
+  int pc = 0, c = blockIdx.x, G = P.grid;
+  if constexpr (single) {
+    while (pc + 1 < P.nprob && c >= P.pr[pc].cta1) ++pc;
+    c -= P.pr[pc].cta0;
+    G = P.pr[pc].cta1 - P.pr[pc].cta0;
   }
   // One-problem code: the problem's units, split evenly over Gc CTAs.
   const int64_t Uc = single ? int64_t(P.pr[pc].KB) * P.pr[pc].tiles : 0;
   const int Gc = single ? (Uc < G ? int(Uc) : G) : 0;
   auto sbegin = [&](int cc) { return unit_begin(cc < Gc ? cc : Gc, Uc, Gc); };
-  const int n_units = single ? int(sbegin(c + 1) - sbegin(c)) : cta_units(P, c);  // this CTA's units
+  int n_units = single ? int(sbegin(c + 1) - sbegin(c)) : 0;  // this CTA's units (job table: set below)
+  int njobs = 1;
   const uint64_t lim = P.limit_ns;
 
   if (threadIdx.x == 0) {
@@ -318,6 +274,22 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     mbar_init(B.gather, 1);
     *abort_flag = 0;
     *last_flag = 0;
+    if (kMulti) {
+      // Job table: this CTA's (nonempty) job in each phase, in phase order.
+      int nj = 0, s0 = 0;
+      for (int p = 0; p < P.nprob; ++p) {
+        const ProbParams& q = P.pr[p];
+        if (int(blockIdx.x) < q.cta0 || int(blockIdx.x) >= q.cta1) continue;
+        const int U = q.KB * q.tiles, Gp = q.cta1 - q.cta0, cl = int(blockIdx.x) - q.cta0;
+        const int b = int(unit_begin(cl, U, Gp)), e = int(unit_begin(cl + 1, U, Gp));
+        if (e <= b) continue;
+        J[nj] = Job{p, q.phase, cl, Gp, U, b, e - b, s0, 0u, 0u, 0u, 0u};
+        s0 += e - b;
+        ++nj;
+      }
+      misc[9] = uint32_t(nj);
+      misc[10] = uint32_t(s0);
+    }
     fence_barrier_init();
   }
   if (warp == 2) {
@@ -328,6 +300,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   cta_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (kMulti) {
+    njobs = int(misc[9]);
+    n_units = int(misc[10]);
+  }
   // TMEM columns: accumulators [0, NACC*issuers*Mpad) (buffer b, issuer k at
   // column (b*issuers + k)*Mpad), then one 64-column A buffer per stage.
   const int NISS = P.issuers;
@@ -393,13 +369,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const int prefill = n_units < S ? n_units : S;
       Cur x;
       if (single)
-        cur_single(P, pc, sbegin(c), n_units, x);
+        cur_at(P, 0, pc, int(sbegin(c)), n_units, x);
       else
-        cur_phase(P, c, 0, x);
+        cur_at(P, 0, njobs > 0 ? J[0].p : 0, njobs > 0 ? J[0].b : 0, njobs > 0 ? J[0].n : 0, x);
       // One problem: plain (t, kb) counters, as cheap as possible per unit.
       auto step = [&](Cur& y) {
         if (kMulti) {
-          cur_next(P, c, y);
+          cur_step(P, J, njobs, y);
         } else if (++y.kb == y.KB) {
           y.kb = 0;
           ++y.t;
@@ -488,9 +464,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const uint32_t a_tmem0 = tmem_base + a_col0;
       Cur x;
       if (single)
-        cur_single(P, pc, sbegin(c), n_units, x);
+        cur_at(P, 0, pc, int(sbegin(c)), n_units, x);
       else
-        cur_phase(P, c, 0, x);
+        cur_at(P, 0, njobs > 0 ? J[0].p : 0, njobs > 0 ? J[0].b : 0, njobs > 0 ? J[0].n : 0, x);
       int s = 0, accb = 0;
       uint32_t ph = 0, accph = 0;
       bool started = false;  // this issuer has written its accumulator in the current segment
@@ -535,7 +511,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           }
         }
         if (kMulti) {
-          cur_next(P, c, x);
+          cur_step(P, J, njobs, x);
         } else if (++x.kb == x.KB) {
           x.kb = 0;
         }
@@ -551,68 +527,72 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   } else if (warp == 3) {
     // ---------------------------------------------- exception metadata (W12)
     if (kW12 && !single) {
-      // Several problems: per unit i of the CTA's sequence, the start (soff)
-      // and end (sent) of its exception entries in its problem's CSR; the
-      // decoders read the entries themselves. Loads go 8 per lane at a time.
-      uint32_t* lo = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
-      uint32_t* hi = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
-      uint8_t* uprob = smem + plan.uprob_off;
-      // The CTA's range in each phase: its first unit and where the range
-      // starts in the CTA's sequence.
-      // (Arrays indexed only by unrolled loop counters, so that they stay in
-      // registers.)
-      int64_t fb[kMaxProb];
-      int fs[kMaxProb + 1];
-      fs[0] = 0;
-#pragma unroll
-      for (int f = 0; f < kMaxProb; ++f) {
-        const bool on = f < P.nphase;
-        fb[f] = on ? pbegin(P, c, f) : 0;
-        fs[f + 1] = fs[f] + (on ? int(pbegin(P, c + 1, f) - fb[f]) : 0);
-      }
+      // Job table: the offsets of a job's units and its entries are one window
+      // of its problem's lists. The offsets are rebased to positions in the
+      // CTA's staged window (soff: n_units + 1 values; unit i's entries are at
+      // positions soff[i] .. soff[i+1]) and ujob[i] names unit i's job. The
+      // entries go to sent when every window fits; otherwise the decoders read
+      // them from global memory.
+      uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
+      uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
+      uint8_t* ujob = smem + plan.uprob_off;
       bool bad = false;
-      for (int i0 = 0; i0 < n_units; i0 += 32 * 8) {
-        uint32_t va[8], vb[8];
+      uint32_t base = 0;
+      for (int j = 0; j < njobs; ++j) {
+        const ProbParams& q = P.pr[J[j].p];
+        const int b = J[j].b, n = J[j].n, s0 = J[j].s0;  // n_units + 1 <= kOffCap (host)
+        const uint32_t e0 = q.exc_off[b], e1 = q.exc_off[b + n];
+        const bool badj = e1 < e0 || int64_t(e1) > q.n_exc;
+        bad |= badj;
+        const uint32_t w = badj ? 0u : e1 - e0;
+        // Every load of a batch is issued before its first store.
+        for (int k0 = 0; k0 < n; k0 += 32 * 8) {
+          uint32_t v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + lane + 32 * j;
-          if (i < n_units) {
-            int f = 0;
-            int64_t fbf = fb[0];
-            int fsf = 0;
+          for (int jj = 0; jj < 8; ++jj)
+            if (k0 + lane + 32 * jj < n) v[jj] = q.exc_off[b + k0 + lane + 32 * jj];
 #pragma unroll
-            for (int q2 = 1; q2 < kMaxProb; ++q2)
-              if (q2 < P.nphase && i >= fs[q2]) {
-                f = q2;
-                fbf = fb[q2];
-                fsf = fs[q2];
-              }
-            const int64_t u = fbf + (i - fsf);
-            const int p = prob_of(P, f, u);
-            const int64_t loc = u - P.pr[p].unit0;
-            va[j] = P.pr[p].exc_off[loc];
-            vb[j] = P.pr[p].exc_off[loc + 1];
-            uprob[i] = uint8_t(p);
+          for (int jj = 0; jj < 8; ++jj) {
+            const int k = k0 + lane + 32 * jj;
+            if (k < n) {
+              soff[s0 + k] = v[jj] - e0 + base;  // checked against [e0, e1) of the job by the decoders
+              ujob[s0 + k] = uint8_t(j);
+            }
           }
         }
+        if (lane == 0) {
+          J[j].e0 = base;
+          J[j].e1 = base + w;
+          J[j].g0 = e0;
+        }
+        base += w;
+      }
+      if (lane == 0) soff[n_units] = base;
+      __syncwarp();  // lane 0's job fields, for every lane
+      const bool fits = base <= uint32_t(kEntCap);
+      if (fits) {
+        constexpr int kBatch = 16;  // entries per lane in flight
+        for (int j = 0; j < njobs; ++j) {
+          const uint32_t* src = P.pr[J[j].p].exc_ent + J[j].g0;
+          uint32_t* dst = sent + J[j].e0;
+          const uint32_t n = J[j].e1 - J[j].e0;
+          for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
+            uint32_t v[kBatch];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + lane + 32 * j;
-          if (i < n_units) {
-            lo[i] = va[j];
-            hi[i] = vb[j];
-            bad |= vb[j] < va[j];
+            for (int jj = 0; jj < kBatch; ++jj)
+              if (b0 + lane + 32 * jj < n) v[jj] = src[b0 + lane + 32 * jj];
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj)
+              if (b0 + lane + 32 * jj < n) dst[b0 + lane + 32 * jj] = v[jj];
           }
         }
       }
-      bad = __any_sync(0xFFFFFFFFu, bad);
-      __syncwarp();
       __syncwarp();
       if (lane == 0) {
         if (bad) set_status(P.status, W12_ERR_CORRUPT);
-        *ent_in_smem = 0;
+        *ent_in_smem = fits ? 1 : 0;
         *ent_base = 0;
-        *ent_end = 0xFFFFFFFFu;
+        *ent_end = base;
         mbar_arrive(B.exc_ready);
       }
     } else if (kW12) {
@@ -681,15 +661,29 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     // Exceptions of unit i that fall in this warp's rows: the lane-held entry
     // (first 32 of the unit) and one ballot mask per 32-value chunk. Prepared
     // one unit ahead so this bookkeeping overlaps the previous unit's stores.
+    // (o0, o1: the unit's entry positions.)
     struct Exc {
       uint32_t o0, o1, ent, mask[kChunksPerThread];
     };
-    const uint8_t* uprob = smem + plan.uprob_off;
+    const uint8_t* ujob = smem + plan.uprob_off;
+    // Where unit i's entries are read from when they are not staged: entry
+    // position o at gptr(i)[o].
+    auto gptr = [&](int i) -> const uint32_t* {
+      if (single) return P.pr[pc].exc_ent;
+      const Job& jb = J[ujob[i]];
+      return P.pr[jb.p].exc_ent + (int64_t(jb.g0) - int64_t(jb.e0));
+    };
     auto prep = [&](int i, Exc& x) {
-      const ProbParams& pp = P.pr[single ? pc : uprob[i]];
       x.o0 = soff[i];
-      x.o1 = single ? soff[i + 1] : sent[i];
-      if (x.o1 < x.o0 || int64_t(x.o1) > pp.n_exc || x.o0 < e_base || x.o1 > e_end) {
+      x.o1 = soff[i + 1];
+      bool badu;
+      if (single) {
+        badu = x.o1 < x.o0 || int64_t(x.o1) > P.pr[pc].n_exc || x.o0 < e_base || x.o1 > e_end;
+      } else {
+        const Job& jb = J[ujob[i]];
+        badu = x.o1 < x.o0 || x.o0 < jb.e0 || x.o1 > jb.e1;
+      }
+      if (badu) {
         if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
         x.o1 = x.o0;
       }
@@ -701,7 +695,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         if (uint32_t(lane) < nex) {
           // An entry with a row field of 128 or more is corrupt: never applied,
           // reported once the loop ends.
-          const uint32_t v = in_smem ? sent[x.o0 - e_base + lane] : __ldg(pp.exc_ent + x.o0 + lane);
+          const uint32_t v = in_smem ? sent[x.o0 - e_base + lane] : __ldg(gptr(i) + x.o0 + lane);
           seen |= v;
           x.ent = (v >> 30) ? kInvalidEnt : v;
         }
@@ -762,7 +756,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
             uint32_t e2 = kInvalidEnt;
             if (bst + lane < cur.o1) {
               const uint32_t v =
-                  in_smem ? sent[bst - e_base + lane] : __ldg(P.pr[single ? pc : uprob[i]].exc_ent + bst + lane);
+                  in_smem ? sent[bst - e_base + lane] : __ldg(gptr(i) + bst + lane);
               seen |= v;
               e2 = (v >> 30) ? kInvalidEnt : v;
             }
@@ -867,18 +861,18 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       if (*glu_flag) {
         const int64_t Nh = pg.N / 2;
         const int64_t col = int64_t(j) * 128 + et;
-        // 16 rows per batch, every load of a batch issued before its first
-        // use: one L2 round trip per 16 rows.
-        for (int m0 = 0; m0 < P.M; m0 += 16) {
-          float g[16], u[16];
+        // 8 rows per batch, every load of a batch issued before its first
+        // use: one L2 round trip per 8 rows.
+        for (int m0 = 0; m0 < P.M; m0 += 8) {
+          float g[8], u[8];
 #pragma unroll
-          for (int r = 0; r < 16; ++r) {
+          for (int r = 0; r < 8; ++r) {
             const int m = m0 + r < P.M ? m0 + r : P.M - 1;
             g[r] = __ldcg(pg.Y + int64_t(m) * pg.N + col);
             u[r] = __ldcg(pg.Y + int64_t(m) * pg.N + Nh + col);
           }
 #pragma unroll
-          for (int r = 0; r < 16; ++r)
+          for (int r = 0; r < 8; ++r)
             if (m0 + r < P.M) P.act[int64_t(m0 + r) * Nh + col] = f32_to_bf16_rne(g[r] / (1.0f + expf(-g[r])) * u[r]);
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -894,50 +888,45 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     int accb = 0;
     uint32_t accph = 0;
     int gather_pending = -1;  // phase of a gather of partials that was given up on
-    int iseq = 0;  // index of the segment's first unit in the CTA's sequence
-    // Walk the CTA's segments (its runs of units of one tile) phase by phase;
-    // only (phase, next unit, end of range) is carried between segments.
-    // Unit numbers fit in 32 bits (the host checks every phase's count).
-    int fn = 0;
-    int un = int(single ? sbegin(c) : pbegin(P, c, 0)), uen = int(single ? sbegin(c + 1) : pbegin(P, c + 1, 0));
-    bool more = un < uen;
-    if constexpr (kMulti) {
-      for (fn = 1; fn < P.nphase && !more; ++fn) {
-        un = int(pbegin(P, c, fn));
-        uen = int(pbegin(P, c + 1, fn));
-        more = un < uen;
+    // Walk the CTA's segments (its runs of units of one tile) job by job;
+    // only the job and (next unit, end of the job's range) are carried
+    // between segments. Unit numbers fit in 32 bits (the host checks every
+    // problem's count).
+    int jn = 0, un = 0, uen = 0;
+    const int ub_single = single ? int(sbegin(c)) : 0;
+    bool more;
+    if (single) {
+      un = ub_single;
+      uen = int(sbegin(c + 1));
+      more = un < uen;
+    } else {
+      more = njobs > 0;
+      if (more) {
+        un = J[0].b;
+        uen = un + J[0].n;
       }
-      --fn;
-      if (!more) fn = 0;
     }
-    const int ub0 = un;
     while (more) {
-      const int f = kMulti ? fn : 0;
-      const int64_t Uf = single ? Uc : P.phase_units[f];
-      const int Gf = single ? Gc : phase_ctas(P, f);
-      const int ub = kMulti ? int(pbegin(P, c, f)) : ub0, ue = uen;
-      const int pi = kMulti ? prob_of(P, f, un) : pc;
+      // This segment's job (the cursor may move on to the next job below).
+      const int f = single ? 0 : J[jn].f, cl = single ? c : J[jn].cl, Gf = single ? Gc : J[jn].G;
+      const int ub = single ? ub_single : J[jn].b, ue = uen, ia0 = single ? 0 : J[jn].s0;
+      const int64_t Uf = single ? Uc : J[jn].U;
+      const int pi = single ? pc : J[jn].p;
       const int KBp = P.pr[pi].KB;
-      const int u0p = kMulti ? int(P.pr[pi].unit0) : 0;
-      const int t = (un - u0p) / KBp;
-      const int tile_u0 = u0p + t * KBp;
+      const int t = un / KBp;
+      const int tile_u0 = t * KBp;
       const int seg_begin = un;
       const int seg_end = tile_u0 + KBp < ue ? tile_u0 + KBp : ue;
       un = seg_end;
       more = un < uen;
-      if constexpr (kMulti) {
-        if (!more) {
-          for (++fn; fn < P.nphase && !more; ++fn) {
-            un = int(pbegin(P, c, fn));
-            uen = int(pbegin(P, c + 1, fn));
-            more = un < uen;
-          }
-          --fn;
-        }
+      if (kMulti && !more && jn + 1 < njobs) {
+        ++jn;
+        un = J[jn].b;
+        uen = un + J[jn].n;
+        more = true;
       }
       const bool final_seg = !more;  // the CTA's last segment: the ring is idle once it is accumulated
-      const int ia = kMulti ? iseq : int(seg_begin - ub0), nseg = int(seg_end - seg_begin);
-      if (kMulti) iseq += nseg;
+      const int ia = ia0 + (seg_begin - ub), nseg = seg_end - seg_begin;
       const int gt = P.pr[pi].tile0 + t;   // launch-wide tile number (counters)
       const int cur = accb;
       const uint32_t cur_ph = accph;
@@ -953,8 +942,8 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // CTA cc has two slots per phase: its first piece in the phase, and
       // its last.
       auto slot_of = [&](int cc) {
-        const int64_t u0 = single ? sbegin(cc) : pbegin(P, cc, f);
-        const int cg = kMode == 3 ? P.cta0[pi] + cc : cc;  // launch-wide CTA
+        const int64_t u0 = unit_begin(cc < Gf ? cc : Gf, Uf, Gf);
+        const int cg = P.pr[pi].cta0 + cc;  // launch-wide CTA
         return 2 * (cg * P.nphase + f) + ((u0 >= tile_u0 && u0 < tile_u0 + KBp) ? 0 : 1);
       };
       // The CTA's final segment ends the kernel. When its tile has one other
@@ -962,7 +951,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // processed, so it usually is), its partial is fetched while this
       // segment's last units are still in flight, and the tile is finished
       // here without writing a partial or taking a counter round trip.
-      const int me = c - c_first;
+      const int me = cl - c_first;
       int pref = 0;
       // (Any phase's last segment qualifies: the prefetch goes to the
       // epilogue's own transpose buffer, not to the ring.)
@@ -1254,8 +1243,7 @@ static void set_problem(ProbParams& q, bool w12_mode, const w12_weights* W, int6
 // workspace carve-up.
 struct Grouped {
   int n, order[kMaxProb], phase[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks;
-  bool part;                   // partitioned: each CTA runs one problem
-  int cta0[kMaxProb + 1];      // partitioned: CTAs [cta0[j], cta0[j+1]) take launch problem j
+  int cta0[kMaxProb], cta1[kMaxProb];  // launch problem j runs on CTAs [cta0[j], cta1[j]) of its phase
   int64_t N[kMaxProb], K[kMaxProb], phase_units[kMaxProb];
   size_t counters, glu_cnt, glu_ready, epoch, parts, total;
 };
@@ -1283,11 +1271,10 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
     if (g->N[link->from] % (2 * kGroup) || g->K[link->to] != g->N[link->from] / 2) return W12_ERR_SHAPE;
     to = link->to;
   }
-  // Phases. Independent problems form one phase: their units are split over
-  // the CTAs as one stream, so a tile is cut only where a CTA's range ends.
-  // With a SwiGLU link the source forms the first phase, the other problems
-  // the second (the activation blocks complete while the CTAs work on them)
-  // and the target the last.
+  // Phases. Independent problems form one phase. With a SwiGLU link the
+  // source forms the first phase, the other problems the second (the
+  // activation blocks complete while the CTAs work on them) and the target
+  // the last.
   const int from = link ? link->from : -1;
   int k = 0;
   if (from >= 0) {
@@ -1304,50 +1291,57 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
     g->order[k] = to;
     g->phase[k++] = g->nphase++;
   }
-  int64_t maxu = 0;
+  int64_t maxu = 0, U[kMaxProb];
   for (int j = 0; j < n; ++j) {
     const int i = g->order[j];
-    g->phase_units[g->phase[j]] += (g->N[i] / kGroup) * (g->K[i] / kGroup);
+    U[j] = (g->N[i] / kGroup) * (g->K[i] / kGroup);
+    g->phase_units[g->phase[j]] += U[j];
     g->tiles += int(g->N[i] / kGroup);
+    // The kernel numbers a problem's units in 32 bits.
+    if (U[j] > (int64_t(1) << 30)) return W12_ERR_SHAPE;
   }
   for (int f = 0; f < g->nphase; ++f) maxu = g->phase_units[f] > maxu ? g->phase_units[f] : maxu;
   int sms = device_sm_count();
   if (sms <= 0) sms = 256;  // sizing without a device: an upper bound
-  g->grid = int(maxu < sms ? maxu : sms);
+  // One CTA per SM at most: a CTA of the SwiGLU link may wait on work of any
+  // other CTA, so all of them must be resident together.
+  const int grid = int(maxu < sms ? maxu : sms);
+  // Each phase splits the CTAs over its problems so that the largest
+  // per-CTA share of units is as small as it can be: one CTA at a time to
+  // the problem whose CTAs carry the most units each (units weigh the same
+  // bytes in every problem), never more CTAs than units.
   int64_t per_cta = 0;
-  for (int f = 0; f < g->nphase; ++f) per_cta += (g->phase_units[f] + g->grid - 1) / g->grid;
-  // Several independent problems: the CTAs are split over the problems so
-  // that the largest per-CTA share of units is as small as it can be (one
-  // CTA at a time to the problem whose CTAs carry the most units each).
-  // Units weigh the same bytes in every problem.
-  g->part = !link && n >= 2 && g->grid >= n;
-  if (g->part) {
-    int64_t U[kMaxProb];
+  g->grid = 0;
+  for (int f = 0; f < g->nphase; ++f) {
+    int j0 = -1, j1 = -1;
+    for (int j = 0; j < n; ++j)
+      if (g->phase[j] == f) {
+        if (j0 < 0) j0 = j;
+        j1 = j + 1;
+      }
+    if (grid < j1 - j0) return W12_ERR_UNSUPPORTED;
     int cnt[kMaxProb];
-    for (int j = 0; j < n; ++j) {
-      U[j] = (g->N[g->order[j]] / kGroup) * (g->K[g->order[j]] / kGroup);
-      cnt[j] = 1;
-    }
-    for (int left = g->grid - n; left > 0; --left) {
+    for (int j = j0; j < j1; ++j) cnt[j] = 1;
+    for (int left = grid - (j1 - j0); left > 0; --left) {
       int best = -1;
-      for (int j = 0; j < n; ++j)
+      for (int j = j0; j < j1; ++j)
         if (cnt[j] < U[j] && (best < 0 || U[j] * cnt[best] > U[best] * cnt[j])) best = j;
       if (best < 0) break;
       ++cnt[best];
     }
-    per_cta = 0;
-    g->cta0[0] = 0;
-    for (int j = 0; j < n; ++j) {
-      g->cta0[j + 1] = g->cta0[j] + cnt[j];
+    int at = 0;
+    int64_t most = 0;
+    for (int j = j0; j < j1; ++j) {
+      g->cta0[j] = at;
+      at += cnt[j];
+      g->cta1[j] = at;
       const int64_t q = (U[j] + cnt[j] - 1) / cnt[j];
-      per_cta = q > per_cta ? q : per_cta;
+      most = q > most ? q : most;
     }
-    g->grid = g->cta0[n];
+    per_cta += most;
+    g->grid = at > g->grid ? at : g->grid;
   }
   if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
-  // The kernel numbers a phase's units (problem offsets included) in 32 bits.
-  for (int f = 0; f < g->nphase; ++f)
-    if (g->phase_units[f] > (int64_t(1) << 30)) return W12_ERR_SHAPE;
   if (to >= 0) {
     g->glu_from = 0;
     g->glu_to = n - 1;
@@ -1394,20 +1388,17 @@ static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_
   P.grid = g.grid;
   P.nprob = n;
   P.nphase = g.nphase;
-  for (int f = 0; f < g.nphase; ++f) P.phase_units[f] = g.phase_units[f];
-  for (int j = n - 1; j >= 0; --j) P.pfirst[g.phase[j]] = j;
   GemmMaps TM;
   memset(&TM, 0, sizeof(TM));
   int tile0 = 0;
-  int64_t unit0[kMaxProb] = {0, 0, 0, 0};
   for (int j = 0; j < n; ++j) {
     const int i = g.order[j];
     const bool is_to = link && i == link->to;
     ProbParams& q = P.pr[j];
     set_problem(q, w12_mode, probs[i].W, g.N[i], g.K[i], probs[i].Y);
     q.phase = g.phase[j];
-    q.unit0 = unit0[q.phase];
-    unit0[q.phase] += int64_t(q.tiles) * q.KB;
+    q.cta0 = g.cta0[j];
+    q.cta1 = g.cta1[j];
     q.tile0 = tile0;
     tile0 += q.tiles;
     const uint16_t* X = is_to ? link->act : probs[i].X;
@@ -1426,20 +1417,13 @@ static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_
   P.epoch = reinterpret_cast<int32_t*>(wsb + g.epoch);
   P.status = dev_status;
   P.limit_ns = wait_limit_ns();
-  for (int j = 0; j <= n; ++j) P.cta0[j] = g.part ? g.cta0[j] : 0;
-  // One problem runs the single-problem form; a SwiGLU link the linked form;
-  // several independent problems the partitioned form.
+  // Independent problems run the one-problem form (each CTA on one problem);
+  // a SwiGLU link the job-table form.
   if (link)
     return w12_mode ? launch_impl<true, false, 2>(g.Mpad, P, TM, stream)
                     : launch_impl<false, false, 2>(g.Mpad, P, TM, stream);
-  if (n == 1)
-    return w12_mode ? launch_impl<true, false, 0>(g.Mpad, P, TM, stream)
-                    : launch_impl<false, false, 0>(g.Mpad, P, TM, stream);
-  if (g.part)
-    return w12_mode ? launch_impl<true, false, 3>(g.Mpad, P, TM, stream)
-                    : launch_impl<false, false, 3>(g.Mpad, P, TM, stream);
-  return w12_mode ? launch_impl<true, false, 1>(g.Mpad, P, TM, stream)
-                  : launch_impl<false, false, 1>(g.Mpad, P, TM, stream);
+  return w12_mode ? launch_impl<true, false, 0>(g.Mpad, P, TM, stream)
+                  : launch_impl<false, false, 0>(g.Mpad, P, TM, stream);
 }
 
 }  // namespace grouped_impl
