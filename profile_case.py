@@ -5,6 +5,8 @@
 --op w12 | bf16 | head (fused LM head + greedy accept); --shape one of the
 27B-class layer GEMMs (qkv, o, gate_up, down) or head (5120 -> 151936).
 --op step replays the benchmarked verify step (layer + fused head) at M = 16.
+--op layer runs the layer's four W12 GEMMs as one grouped launch (--swiglu:
+gate_up -> SwiGLU -> down inside the launch).
 --op attn runs the tree-masked verify attention (40 q / 8 kv heads x 128) for
 --B requests x --T-node random trees over a --P-token prefix.
 Prints the mean CUDA-event time per launch.
@@ -26,7 +28,8 @@ SHAPES = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (34816, 5120), "dow
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head", "attn", "step"])
+    ap.add_argument("--op", default="w12", choices=["w12", "bf16", "head", "attn", "step", "layer"])
+    ap.add_argument("--swiglu", action="store_true")
     ap.add_argument("--B", type=int, default=4)
     ap.add_argument("--T", type=int, default=64)
     ap.add_argument("--P", type=int, default=8192)
@@ -44,6 +47,8 @@ def main():
         return attn(a, dev)
     if a.op == "step":
         return step(a, dev, d)
+    if a.op == "layer":
+        return layer(a, dev, d)
     Wb = d(S.weights_bf16(N, K))
     X = d(S.activations_bf16(a.M, K))
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -73,6 +78,30 @@ def main():
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
     print(f"{a.op} {a.shape} M={a.M}: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/launch")
+
+
+def layer(a, dev, d):
+    """The 27B-class layer's four W12 GEMMs (qkv, o, gate_up, down) in one grouped launch at M = --M."""
+    names = ("qkv", "o", "gate_up", "down")
+    packs = [w12.pack(d(S.weights_bf16(*SHAPES[n], seed=S.SEED_WEIGHTS + i))) for i, n in enumerate(names)]
+    Xs = [d(S.activations_bf16(a.M, SHAPES[n][1], tag=i)) for i, n in enumerate(names)]
+    torch.cuda.empty_cache()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if a.swiglu:
+        items = [(Xs[0], packs[0], None), (Xs[1], packs[1], None), (Xs[2], packs[2], None), (None, packs[3], None)]
+        g = w12.Grouped(items, a.M, swiglu=(2, 3), status=st)
+    else:
+        g = w12.Grouped([(Xs[i], packs[i], None) for i in range(4)], a.M, status=st)
+    g.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.iters):
+        g.run()
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    print(f"layer M={a.M}{' swiglu' if a.swiglu else ''}: {e0.elapsed_time(e1) / a.iters * 1e3:.1f} us/launch")
 
 
 def step(a, dev, d):
