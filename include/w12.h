@@ -342,6 +342,18 @@ int w12_selftest_timeout(int32_t* dev_status, int limit_us, void* stream);
  * default 2000000. Values below 1 are rejected. */
 int w12_set_wait_limit_us(int64_t limit_us);
 
+/* Copy `bytes` bytes from src to dst on `stream` with a kernel rather than a
+ * copy-engine transfer, for the host path of a step (inputs in, results out).
+ * dst and src are device memory or page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister; the device reads and writes it in place through unified
+ * addressing), both 16-byte aligned, not overlapping. With launch overlap on
+ * (below) the next kernel on the stream may start while the copy runs (a GEMM
+ * then requests its first weight tiles meanwhile), and the copy itself waits
+ * for the previous kernel before it reads or writes. bytes == 0 launches
+ * nothing. Errors: W12_ERR_ARG (null, misaligned or overlapping pointers, or
+ * memory the device cannot address), W12_ERR_UNSUPPORTED, W12_ERR_CUDA. */
+int w12_copy(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Launch overlap (programmatic dependent launch), on by default: a GEMM or
  * verify launch may start while the previous kernel on its stream is still
  * running. Before that kernel completes it only reads the packed weights

@@ -248,6 +248,54 @@ __global__ void selftest_timeout_kernel(int32_t* status, uint64_t limit_ns) {
   cta_sync();
 }
 
+// ---------------------------------------------------------------------------
+// Copy kernel for the host path of a step: inputs from page-locked host memory
+// into device buffers, results back. As a kernel (not a copy-engine transfer)
+// it takes part in launch overlap: it lets the next kernel on the stream start
+// at once (a GEMM then requests its first weight tiles while the inputs are
+// still arriving) and waits for the previous kernel before it reads or writes.
+// ---------------------------------------------------------------------------
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyBlocks = 16;  // few CTAs: the next GEMM needs whole SMs for its own CTAs
+
+__global__ void __launch_bounds__(kCopyThreads) copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                            int64_t n16, uint8_t* __restrict__ dtail,
+                                                            const uint8_t* __restrict__ stail, int tail) {
+  grid_dep_launch();
+  grid_dep_wait();
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  // Four 16-byte loads in flight per thread before the stores. Loads skip
+  // the caches (the source may be host memory the CPU rewrote since the last
+  // launch) and stores write through (the destination may be host memory).
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldcv(src + i), b = __ldcv(src + i + stride), c = __ldcv(src + i + 2 * stride),
+                d = __ldcv(src + i + 3 * stride);
+    __stwt(dst + i, a);
+    __stwt(dst + i + stride, b);
+    __stwt(dst + i + 2 * stride, c);
+    __stwt(dst + i + 3 * stride, d);
+  }
+  for (; i < n16; i += stride) __stwt(dst + i, __ldcv(src + i));
+  if (blockIdx.x == 0 && int(threadIdx.x) < tail) {
+    const uint8_t v = *reinterpret_cast<const volatile uint8_t*>(stail + threadIdx.x);
+    *reinterpret_cast<volatile uint8_t*>(dtail + threadIdx.x) = v;
+  }
+}
+
+// Device address of p (device, managed or page-locked host memory), or null.
+static const void* device_address(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
 }  // namespace w12
 
 using namespace w12;
@@ -288,6 +336,34 @@ int w12_selftest_timeout(int32_t* dev_status, int limit_us, void* stream) {
   selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_status,
                                                                            uint64_t(limit_us) * 1000ull);
   return cuda_status(cudaGetLastError());
+}
+
+int w12_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (!dst || !src || !aligned(dst, 16) || !aligned(src, 16)) return W12_ERR_ARG;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  if (bytes > 0 && s0 < d0 + bytes && d0 < s0 + bytes) return W12_ERR_ARG;  // overlapping
+  if (!device_supported()) return W12_ERR_UNSUPPORTED;
+  if (bytes == 0) return W12_OK;
+  void* dd = const_cast<void*>(device_address(dst));
+  const void* sd = device_address(src);
+  if (!dd || !sd) return W12_ERR_ARG;
+  const int64_t n16 = int64_t(bytes / 16);
+  const int tail = int(bytes % 16);
+  int64_t blocks = (n16 + kCopyThreads - 1) / kCopyThreads;
+  blocks = blocks < 1 ? 1 : (blocks > kCopyBlocks ? kCopyBlocks : blocks);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(unsigned(kCopyThreads));
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_enabled() ? 1 : 0;
+  uint8_t* dt = static_cast<uint8_t*>(dd) + n16 * 16;
+  const uint8_t* st = static_cast<const uint8_t*>(sd) + n16 * 16;
+  return cuda_status(cudaLaunchKernelEx(&cfg, copy_kernel, static_cast<uint4*>(dd), static_cast<const uint4*>(sd),
+                                        n16, dt, st, tail));
 }
 
 size_t w12_gemm_ws_bytes(int64_t M, int64_t N, int64_t K) {

@@ -12,8 +12,11 @@ argument checks), which otherwise dominates the short layer GEMMs at M = 16.
 Inputs (activations X, hidden states H, draft block) live in one device
 buffer mirrored by one pinned host buffer, and the results (accept_len,
 bonus, argmax) in one device buffer mirrored by one pinned host buffer, so
-the host path is one graph: a single host-to-device copy, the step, and a
-single device-to-host copy.
+the host path is one graph: a copy kernel that reads the pinned inputs, the
+step, and a copy kernel that writes the results to pinned memory (kernels,
+not copy-engine transfers, so that the step's first GEMM starts requesting
+its weights while the inputs arrive, and the result copy follows the last
+kernel without a separate transfer's start-up).
 """
 from __future__ import annotations
 
@@ -55,6 +58,7 @@ class VerifyStep:
         self._out_dev = torch.zeros(2 * B + M, dtype=torch.int32, device=self.dev)
         self._out_host = torch.zeros(2 * B + M, dtype=torch.int32).pin_memory()
         self.accept_len, self.bonus, self.argmax = self._out_dev[:B], self._out_dev[B:2 * B], self._out_dev[2 * B:]
+        self._results_host = (self._out_host[:B], self._out_host[B:2 * B], self._out_host[2 * B:])
         # All layer GEMMs in one launch (up to 4 per launch).
         self.groups = ([w12.Grouped([(x, w, y) for x, w, y in zip(self.X[i:i + 4], layers[i:i + 4], self.Y[i:i + 4])],
                                     M, status=self.status) for i in range(0, len(layers), 4)]
@@ -108,13 +112,15 @@ class VerifyStep:
 
     def capture_host(self):
         """Record copy-in, step and copy-out into one CUDA graph."""
+        w12.copy(self._in_dev, self._in_host)
         self.run()
+        w12.copy(self._out_host, self._out_dev)
         torch.cuda.synchronize(self.dev)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self._in_dev.copy_(self._in_host, non_blocking=True)
+            w12.copy(self._in_dev, self._in_host)
             self.run()
-            self._out_host.copy_(self._out_dev, non_blocking=True)
+            w12.copy(self._out_host, self._out_dev)
         torch.cuda.synchronize(self.dev)
         self.graph_host = g
         return self
@@ -138,9 +144,7 @@ class VerifyStep:
         if self.graph_host is None:
             self.capture_host()
         self.graph_host.replay()
-        B = self.B
-        h = self._out_host
-        return h[:B], h[B:2 * B], h[2 * B:]
+        return self._results_host
 
     def h2d_bytes(self) -> int:
         return self._in_host.numel()

@@ -26,7 +26,7 @@ EXPORTS = [
     "w12_verify_greedy_fused", "w12_verify_tree", "w12_verify_tree_fused", "w12_selftest_timeout",
     "w12_set_wait_limit_us", "w12_set_overlap", "w12_gemm_noalloc", "w12_gemm_grouped_ws_bytes",
     "w12_gemm_grouped", "w12_gemm_grouped_bf16_ref", "w12_kv_commit", "w12_state_select",
-    "w12_tree_attention_ws_bytes", "w12_tree_attention",
+    "w12_tree_attention_ws_bytes", "w12_tree_attention", "w12_copy",
 ]
 
 
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "w12_selftest_timeout": (i32, [vp, i32, vp]),
             "w12_set_wait_limit_us": (i32, [i64]),
             "w12_set_overlap": (i32, [i32]),
+            "w12_copy": (i32, [vp, vp, sz, vp]),
             "w12_gemm_noalloc": (i32, [vp, i64, ctypes.POINTER(_Weights), vp, vp, vp]),
             "w12_gemm_grouped_ws_bytes": (sz, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu)]),
             "w12_gemm_grouped": (i32, [ctypes.POINTER(_Problem), i32, i64, ctypes.POINTER(_Swiglu), vp, sz, vp, vp]),
@@ -496,6 +497,18 @@ def selftest_timeout(limit_us: int, status: torch.Tensor, stream=None):
 
 def set_wait_limit_us(limit_us: int):
     _check(lib().w12_set_wait_limit_us(int(limit_us)), "w12_set_wait_limit_us")
+
+
+def copy(dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """dst <- src bytes with the library's copy kernel (w12_copy). Each tensor is
+    contiguous, on the device or in pinned host memory, 16-byte aligned; the
+    byte counts must match."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy: tensors must be contiguous")
+    nb = dst.numel() * dst.element_size()
+    if nb != src.numel() * src.element_size():
+        raise ValueError("copy: byte counts differ")
+    _check(lib().w12_copy(dst.data_ptr(), src.data_ptr(), nb, _stream(stream)), "w12_copy")
 
 
 def set_overlap(enable: bool):
