@@ -1,0 +1,182 @@
+// Decode warps of the W12 GEMM kernels (the single-GEMM kernel and the grouped
+// one share this code): the loop that restores each unit's 128 x 128 bf16
+// weights from the three 4-bit planes in a shared-memory stage, patches the
+// unit's exception entries in, and stores the result as the MMA's A operand
+// in tensor memory.
+//
+// A unit's row r (one thread's W row) is 128 values: 64 bytes in each plane
+// (`planes` at stage + r * 64 in 8 KB planes, 128-byte swizzle in 16-byte
+// chunks), the group's exponent base in the stage's ebase bytes. Exception
+// entry e (row << 23 | col << 16 | bits16, row and col within the unit) sets
+// value (row, col) to its 16 stored bits; an entry with a row field >= 128
+// (bits 31..30 set) is corrupt: never applied, and reported by the caller
+// from the OR of the entries read. Entries of a unit are read from the
+// staged window in shared memory when it fits, else from global memory.
+#pragma once
+
+#include "w12_dev.cuh"
+
+namespace w12 {
+
+#ifndef W12_DEC_GROUPS
+#define W12_DEC_GROUPS 2
+#endif
+#ifndef W12_DEC_SPLIT
+#define W12_DEC_SPLIT 1
+#endif
+static_assert(W12_DEC_GROUPS >= 1 && W12_DEC_GROUPS <= 3, "decode groups: 1..3");
+static_assert(W12_DEC_SPLIT == 1 || W12_DEC_SPLIT == 2 || W12_DEC_SPLIT == 4, "decode split: 1, 2 or 4");
+constexpr int kDecGroups = W12_DEC_GROUPS;       // decode groups: group g takes units g, g + kDecGroups, ...
+constexpr int kDecSplit = W12_DEC_SPLIT;         // warps sharing one unit row
+constexpr int kChunksPerThread = 4 / kDecSplit;  // 32-value chunks each decode thread restores per unit
+constexpr int kAColsPerBuf = 64;                 // 128 K values = 64 TMEM columns of bf16 pairs
+constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
+
+// What the decode loop needs from its kernel.
+struct DecodeCtx {
+  const uint8_t* smem;       // stage 0 (stages stage_bytes apart)
+  uint32_t stage_bytes;
+  uint32_t eb_off;           // the stage's ebase bytes (one per row)
+  int S;                     // ring stages
+  int n_units;               // units of this CTA
+  uint64_t* full;            // [S] weight bytes of a stage landed
+  uint64_t* a_full;          // [S] decoded A of a stage stored (128 * kDecSplit arrivals)
+  uint32_t a_tmem;           // TMEM address of A buffer 0 at this warp's lane quarter
+  const uint32_t* soff;      // per unit: first entry position (n_units + 1 values)
+  const uint32_t* sent;      // staged entries (when in_smem)
+  uint32_t e_base;           // position of sent[0]
+  bool in_smem;
+  int32_t* status;
+};
+
+// The decode warp's loop. dw = warp index among the decode warps. wait(bar,
+// parity) is the kernel's bounded wait (false: give up); bad(i, o0, o1) says
+// whether unit i's entry positions [o0, o1) fail a consistency check (then the
+// unit is decoded without exceptions and W12_ERR_CORRUPT is set); gptr(i)
+// gives the pointer p with entry position o of unit i at p[o] when entries are
+// not staged. Returns the OR of the entries read.
+template <class Wait, class Bad, class Gptr>
+__device__ __forceinline__ uint32_t decode_units(const DecodeCtx& c, int dw, Wait&& wait, Bad&& bad, Gptr&& gptr) {
+  const int lane = threadIdx.x & 31;
+  const int q = (threadIdx.x >> 5) & 3;       // TMEM lane quarter of this warp
+  const int grp = (dw >> 2) / kDecSplit;      // decode group
+  const int h = (dw >> 2) % kDecSplit;        // slice of the unit row (kChunksPerThread chunks of 32 values)
+  const int row = q * 32 + lane;              // W row within the unit
+  const uint32_t tm_a = c.a_tmem + (uint32_t(q * 32) << 16);
+  uint32_t seen = 0;
+
+  // Exceptions of unit i that fall in this warp's rows: the lane-held entry
+  // (first 32 of the unit) and one ballot mask per 32-value chunk. Prepared
+  // one unit ahead so this bookkeeping overlaps the previous unit's stores.
+  struct Exc {
+    uint32_t o0, o1, ent, mask[kChunksPerThread];
+  };
+  auto prep = [&](int i, Exc& x) {
+    x.o0 = c.soff[i];
+    x.o1 = c.soff[i + 1];
+    if (bad(i, x.o0, x.o1)) {
+      if (lane == 0) set_status(c.status, W12_ERR_CORRUPT);
+      x.o1 = x.o0;
+    }
+    const uint32_t nex = x.o1 - x.o0;
+    x.ent = kInvalidEnt;
+#pragma unroll
+    for (int cc = 0; cc < kChunksPerThread; ++cc) x.mask[cc] = 0;
+    if (nex > 0) {
+      if (uint32_t(lane) < nex) {
+        const uint32_t v = c.in_smem ? c.sent[x.o0 - c.e_base + lane] : __ldg(gptr(i) + x.o0 + lane);
+        seen |= v;
+        x.ent = (v >> 30) ? kInvalidEnt : v;
+      }
+      const bool mine = x.ent != kInvalidEnt && ((x.ent >> 28) & 3u) == uint32_t(q);
+      const uint32_t ch = (x.ent >> 21) & 3u;
+#pragma unroll
+      for (int cc = 0; cc < kChunksPerThread; ++cc)
+        x.mask[cc] = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(h * kChunksPerThread + cc));
+    }
+  };
+  Exc cur;
+  if (grp < c.n_units) prep(grp, cur);
+
+  int s = 0;
+  uint32_t ph = 0;
+  for (int k = 0; k < grp; ++k)
+    if (++s == c.S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  for (int i = grp; i < c.n_units; i += kDecGroups) {
+    // Stage s's copies can only have landed after the MMA that last read
+    // its TMEM A buffer committed, so the buffer is free once this returns.
+    // One decision per warp: the loop uses warp-collective instructions.
+    if (!__all_sync(0xFFFFFFFFu, wait(&c.full[s], ph))) break;
+    tc_fence_after();
+    const uint8_t* st = c.smem + s * c.stage_bytes;
+    const uint8_t* pl = st + row * 64;
+    const uint32_t swz = uint32_t(row >> 1) & 3u;
+    uint4 a[kChunksPerThread], b[kChunksPerThread], g[kChunksPerThread];
+#pragma unroll
+    for (int cc = 0; cc < kChunksPerThread; ++cc) {
+      const uint32_t off = ((uint32_t(h * kChunksPerThread + cc) ^ swz) << 4);
+      a[cc] = *reinterpret_cast<const uint4*>(pl + off);
+      b[cc] = *reinterpret_cast<const uint4*>(pl + 8192 + off);
+      g[cc] = *reinterpret_cast<const uint4*>(pl + 16384 + off);
+    }
+    const uint32_t eb = st[c.eb_off + row];
+    const uint32_t E2 = (eb << 7) * 0x00010001u;
+
+#pragma unroll
+    for (int cc = 0; cc < kChunksPerThread; ++cc) {
+      const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
+      uint32_t w[16];
+      decode8(a[cc].x, b[cc].x, g[cc].x, E2, w + 0);
+      decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
+      decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
+      decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
+      uint32_t mk = cur.mask[cc];
+      while (mk) {
+        const int src = __ffs(mk) - 1;
+        mk &= mk - 1;
+        const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
+        if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+      }
+      if (cur.o1 - cur.o0 > 32) {
+        // Rare: more than 32 exceptions in the unit; walk the rest in batches.
+        for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
+          uint32_t e2 = kInvalidEnt;
+          if (bst + lane < cur.o1) {
+            const uint32_t v = c.in_smem ? c.sent[bst - c.e_base + lane] : __ldg(gptr(i) + bst + lane);
+            seen |= v;
+            e2 = (v >> 30) ? kInvalidEnt : v;
+          }
+          const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
+          uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
+          while (mk2) {
+            const int src = __ffs(mk2) - 1;
+            mk2 &= mk2 - 1;
+            const uint32_t e = __shfl_sync(0xFFFFFFFFu, e2, src);
+            if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+          }
+        }
+      }
+      tmem_st16(tm_a + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
+    }
+    if (i + kDecGroups < c.n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
+    tmem_st_wait();
+    tc_fence_before();
+    // This thread's reads of the stage (generic proxy) come before the copy
+    // (async proxy) that refills it once the MMA has committed. Without the
+    // fence, a refill issued soon after the reads was seen to land under
+    // them in about 1 % of launches.
+    fence_proxy_async_smem();
+    mbar_arrive(&c.a_full[s]);
+    for (int k = 0; k < kDecGroups; ++k)
+      if (++s == c.S) {
+        s = 0;
+        ph ^= 1u;
+      }
+  }
+  return seen;
+}
+
+}  // namespace w12

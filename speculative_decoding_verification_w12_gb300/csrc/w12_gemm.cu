@@ -25,6 +25,7 @@
 // The BF16 baseline uses the same skeleton with A loaded by TMA into smem.
 // In argmax mode (fused LM head) the epilogue reduces each 128-row vocab
 // tile to a per-row (max, index) pair instead of writing logits.
+#include "w12_decode.cuh"
 #include "w12_dev.cuh"
 #include "w12_host.h"
 
@@ -34,22 +35,9 @@ namespace w12 {
 // serves one TMEM lane quarter (32 rows); the W12_DEC_SPLIT warps of a
 // quarter in a group split the unit's 4 chunks of 32 values; groups take
 // units in turn (unit i goes to group i % W12_DEC_GROUPS).
-#ifndef W12_DEC_GROUPS
-#define W12_DEC_GROUPS 2
-#endif
-#ifndef W12_DEC_SPLIT
-#define W12_DEC_SPLIT 1
-#endif
-static_assert(W12_DEC_GROUPS >= 1 && W12_DEC_GROUPS <= 3, "decode groups: 1..3");
-static_assert(W12_DEC_SPLIT == 1 || W12_DEC_SPLIT == 2 || W12_DEC_SPLIT == 4, "decode split: 1, 2 or 4");
-constexpr int kDecGroups = W12_DEC_GROUPS;
-constexpr int kDecSplit = W12_DEC_SPLIT;
-constexpr int kChunksPerThread = 4 / kDecSplit;  // 32-value chunks each decode thread restores per unit
 constexpr int kMaxStages = 8;         // smem ring depth limit (one TMEM A buffer per stage)
-constexpr int kAColsPerBuf = 64;      // 128 K values = 64 columns of bf16 pairs
 constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
 constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
-constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
 constexpr int kDeferMinMpad = 128;    // from this many padded rows, split tiles may be summed by a second kernel
 
 struct GemmParams {
@@ -430,131 +418,30 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     }
   } else if (kW12 && warp >= 4 && warp < 4 + C::kDecWarps) {
     // --------------------------------------------------------------- decode
-    const int dw = warp - 4;
-    const int q = warp & 3;          // TMEM lane quarter of this warp
-    const int grp = (dw >> 2) / kDecSplit;  // decode group: units grp, grp + kDecGroups, ...
-    const int h = (dw >> 2) % kDecSplit;    // slice of the unit row (kChunksPerThread chunks of 32 values)
-    const int row = q * 32 + lane;   // W row within the unit
-    const uint32_t tm_lane = uint32_t(q * 32) << 16;
-    const uint32_t* soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
-    const uint32_t* sent = reinterpret_cast<const uint32_t*>(smem + plan.sent_off);
-    // Waits are taken as one decision per warp: the loop below uses
-    // warp-collective instructions (shuffles, ballots, tcgen05.st).
-    bool ok = __all_sync(0xFFFFFFFFu, wait(B.exc_ready, 0));
-    const bool in_smem = ok && *ent_in_smem;
-    const uint32_t e_base = *ent_base;
-    const uint32_t e_end = *ent_end;
-    const int n_units = int(ue - ub);
-
-    // Exceptions of unit i that fall in this warp's rows: the lane-held entry
-    // (first 32 of the unit) and one ballot mask per 32-value chunk. Prepared
-    // one unit ahead so this bookkeeping overlaps the previous unit's stores.
-    struct Exc {
-      uint32_t o0, o1, ent, mask[kChunksPerThread];
-    };
-    auto prep = [&](int i, Exc& x) {
-      x.o0 = soff[i];
-      x.o1 = soff[i + 1];
-      if (x.o1 < x.o0 || int64_t(x.o1) > P.n_exc || x.o0 < e_base || x.o1 > e_end) {
-        if (lane == 0) set_status(P.status, W12_ERR_CORRUPT);
-        x.o1 = x.o0;
-      }
-      const uint32_t nex = x.o1 - x.o0;
-      x.ent = kInvalidEnt;
-#pragma unroll
-      for (int cc = 0; cc < kChunksPerThread; ++cc) x.mask[cc] = 0;
-      if (nex > 0) {
-        if (uint32_t(lane) < nex) {
-          // An entry with a row field of 128 or more is corrupt: it is never
-          // applied (warp 3 reports it).
-          const uint32_t v = in_smem ? sent[x.o0 - e_base + lane] : __ldg(P.exc_ent + x.o0 + lane);
-          x.ent = (v >> 30) ? kInvalidEnt : v;
-        }
-        const bool mine = x.ent != kInvalidEnt && ((x.ent >> 28) & 3u) == uint32_t(q);
-        const uint32_t ch = (x.ent >> 21) & 3u;
-#pragma unroll
-        for (int cc = 0; cc < kChunksPerThread; ++cc)
-          x.mask[cc] = __ballot_sync(0xFFFFFFFFu, mine && ch == uint32_t(h * kChunksPerThread + cc));
-      }
-    };
-    Exc cur;
-    if (ok && grp < n_units) prep(grp, cur);
-
-    int s = 0;
-    uint32_t ph = 0;
-    for (int k = 0; k < grp; ++k)
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
-    for (int i = grp; i < n_units && ok; i += kDecGroups) {
-      // Stage s's copies can only have landed after the MMA that last read
-      // its TMEM A buffer committed, so the buffer is free once this returns.
-      if (!__all_sync(0xFFFFFFFFu, wait(&B.full[s], ph))) break;
-      tc_fence_after();
-      const uint8_t* st = smem + s * plan.stage_bytes;
-      const uint8_t* pl = st + row * 64;
-      const uint32_t swz = uint32_t(row >> 1) & 3u;
-      uint4 a[kChunksPerThread], b[kChunksPerThread], g[kChunksPerThread];
-#pragma unroll
-      for (int cc = 0; cc < kChunksPerThread; ++cc) {
-        const uint32_t off = ((uint32_t(h * kChunksPerThread + cc) ^ swz) << 4);
-        a[cc] = *reinterpret_cast<const uint4*>(pl + off);
-        b[cc] = *reinterpret_cast<const uint4*>(pl + 8192 + off);
-        g[cc] = *reinterpret_cast<const uint4*>(pl + 16384 + off);
-      }
-      const uint32_t eb = st[plan.eb_off + row];
-      const uint32_t E2 = (eb << 7) * 0x00010001u;
-
-#pragma unroll
-      for (int cc = 0; cc < kChunksPerThread; ++cc) {
-        const uint32_t lc = uint32_t(h * kChunksPerThread + cc);  // 16-byte plane chunk = 32 values
-        uint32_t w[16];
-        decode8(a[cc].x, b[cc].x, g[cc].x, E2, w + 0);
-        decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
-        decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
-        decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
-        uint32_t mk = cur.mask[cc];
-        while (mk) {
-          const int src = __ffs(mk) - 1;
-          mk &= mk - 1;
-          const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
-          if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
-        }
-        if (cur.o1 - cur.o0 > 32) {
-          // Rare: more than 32 exceptions in the unit; walk the rest in batches.
-          for (uint32_t bst = cur.o0 + 32; bst < cur.o1; bst += 32) {
-            uint32_t e2 = kInvalidEnt;
-            if (bst + lane < cur.o1) {
-              const uint32_t v = in_smem ? sent[bst - e_base + lane] : __ldg(P.exc_ent + bst + lane);
-              e2 = (v >> 30) ? kInvalidEnt : v;
-            }
-            const bool mine2 = e2 != kInvalidEnt && ((e2 >> 28) & 3u) == uint32_t(q) && ((e2 >> 21) & 3u) == lc;
-            uint32_t mk2 = __ballot_sync(0xFFFFFFFFu, mine2);
-            while (mk2) {
-              const int src = __ffs(mk2) - 1;
-              mk2 &= mk2 - 1;
-              const uint32_t e = __shfl_sync(0xFFFFFFFFu, e2, src);
-              if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
-            }
-          }
-        }
-        tmem_st16(tmem_base + tm_lane + a_col0 + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
-      }
-      if (i + kDecGroups < n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
-      tmem_st_wait();
-      tc_fence_before();
-      // This thread's reads of the stage (generic proxy) come before the copy
-      // (async proxy) that refills it once the MMA has committed. Without the
-      // fence, a refill issued soon after the reads was seen to land under
-      // them in about 1 % of launches.
-      fence_proxy_async_smem();
-      mbar_arrive(&B.a_full[s]);
-      for (int k = 0; k < kDecGroups; ++k)
-        if (++s == S) {
-          s = 0;
-          ph ^= 1u;
-        }
+    // One decision per warp: the decode loop uses warp-collective instructions.
+    if (__all_sync(0xFFFFFFFFu, wait(B.exc_ready, 0))) {
+      DecodeCtx d;
+      d.smem = smem;
+      d.stage_bytes = plan.stage_bytes;
+      d.eb_off = plan.eb_off;
+      d.S = S;
+      d.n_units = int(ue - ub);
+      d.full = B.full;
+      d.a_full = B.a_full;
+      d.a_tmem = tmem_base + a_col0;
+      d.soff = reinterpret_cast<const uint32_t*>(smem + plan.soff_off);
+      d.sent = reinterpret_cast<const uint32_t*>(smem + plan.sent_off);
+      d.e_base = *ent_base;
+      d.in_smem = *ent_in_smem;
+      d.status = P.status;
+      const uint32_t e_end = *ent_end;
+      // (Corrupt entries are reported by warp 3, which reads the whole window.)
+      decode_units(
+          d, warp - 4, wait,
+          [&](int, uint32_t o0, uint32_t o1) {
+            return o1 < o0 || int64_t(o1) > P.n_exc || o0 < d.e_base || o1 > e_end;
+          },
+          [&](int) { return P.exc_ent; });
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------- epilogue
