@@ -15,6 +15,7 @@
 #pragma once
 
 #include "w12_dev.cuh"
+#include "w12_host.h"
 
 namespace w12 {
 
@@ -31,6 +32,55 @@ constexpr int kDecSplit = W12_DEC_SPLIT;         // warps sharing one unit row
 constexpr int kChunksPerThread = 4 / kDecSplit;  // 32-value chunks each decode thread restores per unit
 constexpr int kAColsPerBuf = 64;                 // 128 K values = 64 TMEM columns of bf16 pairs
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
+
+// A CTA's exception window over units [ub, ub + n) of one problem, staged by
+// one warp (all 32 lanes): the n + 1 offsets exc_off[ub ..] into soff (n + 1
+// <= kOffCap, which the host checks), and the entries they span,
+// exc_ent[e0 .. e1), into sent when they fit (kEntCap). Every load of a batch
+// is issued before the batch's first store, so the window costs one memory
+// round trip per batch rather than one per 32 values (the decoders cannot
+// start before it is done). bad: the window's ends are inconsistent (e1 < e0
+// or past n_exc).
+struct ExcWindow {
+  uint32_t e0, e1;
+  bool bad, fits;
+};
+
+__device__ __forceinline__ ExcWindow stage_window(const uint32_t* exc_off, const uint32_t* exc_ent, int64_t n_exc,
+                                                  int64_t ub, int n, uint32_t* soff, uint32_t* sent) {
+  const int lane = threadIdx.x & 31;
+  const int nwin = n + 1;
+  {
+    uint32_t v[kOffCap / 32];
+#pragma unroll
+    for (int j = 0; j < kOffCap / 32; ++j)
+      if (lane + 32 * j < nwin) v[j] = exc_off[ub + lane + 32 * j];
+#pragma unroll
+    for (int j = 0; j < kOffCap / 32; ++j)
+      if (lane + 32 * j < nwin) soff[lane + 32 * j] = v[j];
+  }
+  __syncwarp();
+  ExcWindow w;
+  w.e0 = soff[0];
+  w.e1 = soff[nwin - 1];
+  w.bad = w.e1 < w.e0 || int64_t(w.e1) > n_exc;
+  w.fits = !w.bad && (w.e1 - w.e0) <= uint32_t(kEntCap);
+  if (w.fits) {
+    constexpr int kBatch = 16;  // entries per lane in flight
+    const uint32_t cnt = w.e1 - w.e0;
+    for (uint32_t b0 = 0; b0 < cnt; b0 += 32 * kBatch) {
+      uint32_t v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (b0 + lane + 32 * j < cnt) v[j] = exc_ent[w.e0 + b0 + lane + 32 * j];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (b0 + lane + 32 * j < cnt) sent[b0 + lane + 32 * j] = v[j];
+    }
+  }
+  __syncwarp();
+  return w;
+}
 
 // What the decode loop needs from its kernel.
 struct DecodeCtx {

@@ -359,62 +359,16 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
   } else if (warp == 3) {
     // ---------------------------------------------- exception metadata (W12)
     if (kW12) {
-      uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
-      uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
-      // Every load of a batch is issued before the batch's first store, so the
-      // window costs one memory round trip per batch rather than one per 32
-      // values: the decoders cannot start before this warp arrives.
-      const int nwin = int(ue - ub) + 1;  // host guarantees nwin <= kOffCap
-      {
-        uint32_t v[kOffCap / 32];
-#pragma unroll
-        for (int j = 0; j < kOffCap / 32; ++j)
-          if (lane + 32 * j < nwin) v[j] = P.exc_off[ub + lane + 32 * j];
-#pragma unroll
-        for (int j = 0; j < kOffCap / 32; ++j)
-          if (lane + 32 * j < nwin) soff[lane + 32 * j] = v[j];
-      }
-      __syncwarp();
-      const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
-      bool bad = e1 < e0 || int64_t(e1) > P.n_exc;
-      const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
-      constexpr int kBatch = 16;  // entries per lane in flight
-      uint32_t seen = 0;          // OR of the entries' top bits (a row field >= 128 is corrupt)
-      if (fits) {
-        const uint32_t n = e1 - e0;
-        for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
-          uint32_t v[kBatch];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j)
-            if (b0 + lane + 32 * j < n) v[j] = P.exc_ent[e0 + b0 + lane + 32 * j];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j)
-            if (b0 + lane + 32 * j < n) {
-              sent[b0 + lane + 32 * j] = v[j];
-              seen |= v[j];
-            }
-        }
-      }
-      __syncwarp();
+      const ExcWindow w = stage_window(P.exc_off, P.exc_ent, P.n_exc, ub, int(ue - ub),
+                                       reinterpret_cast<uint32_t*>(smem + plan.soff_off),
+                                       reinterpret_cast<uint32_t*>(smem + plan.sent_off));
       if (lane == 0) {
-        if (bad) set_status(P.status, W12_ERR_CORRUPT);
-        *ent_in_smem = fits ? 1 : 0;
-        *ent_base = e0;
-        *ent_end = bad ? e0 : e1;
+        if (w.bad) set_status(P.status, W12_ERR_CORRUPT);
+        *ent_in_smem = w.fits ? 1 : 0;
+        *ent_base = w.e0;
+        *ent_end = w.bad ? w.e0 : w.e1;
         mbar_arrive(B.exc_ready);
       }
-      if (!bad && !fits) {
-        // Entries left in global memory: scanned here, off the decoders' path.
-        const uint32_t n = e1 - e0;
-        for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
-          uint32_t v[kBatch];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) v[j] = (b0 + lane + 32 * j < n) ? __ldg(P.exc_ent + e0 + b0 + lane + 32 * j) : 0u;
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) seen |= v[j];
-        }
-      }
-      if (__any_sync(0xFFFFFFFFu, (seen >> 30) != 0) && lane == 0) set_status(P.status, W12_ERR_CORRUPT);
     }
   } else if (kW12 && warp >= 4 && warp < 4 + C::kDecWarps) {
     // --------------------------------------------------------------- decode
@@ -435,13 +389,15 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       d.in_smem = *ent_in_smem;
       d.status = P.status;
       const uint32_t e_end = *ent_end;
-      // (Corrupt entries are reported by warp 3, which reads the whole window.)
-      decode_units(
+      const uint32_t seen = decode_units(
           d, warp - 4, wait,
           [&](int, uint32_t o0, uint32_t o1) {
             return o1 < o0 || int64_t(o1) > P.n_exc || o0 < d.e_base || o1 > e_end;
           },
           [&](int) { return P.exc_ent; });
+      // Every entry of the window is read by a decode warp: a corrupt one
+      // (row field >= 128) shows in the OR.
+      if ((seen >> 30) != 0) set_status(P.status, W12_ERR_CORRUPT);
     }
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------- epilogue

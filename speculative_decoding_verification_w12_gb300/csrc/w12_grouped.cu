@@ -584,47 +584,14 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         mbar_arrive(B.exc_ready);
       }
     } else if (kW12) {
-      uint32_t* soff = reinterpret_cast<uint32_t*>(smem + plan.soff_off);
-      uint32_t* sent = reinterpret_cast<uint32_t*>(smem + plan.sent_off);
-      const int64_t ub = sbegin(c);
-      const uint32_t* exc_off = P.pr[pc].exc_off;
-      const uint32_t* exc_ent = P.pr[pc].exc_ent;
-      // Every load of a batch is issued before the batch's first store, so the
-      // window costs one memory round trip per batch rather than one per 32
-      // values: the decoders cannot start before this warp arrives.
-      const int nwin = n_units + 1;  // host guarantees nwin <= kOffCap
-      {
-        uint32_t v[kOffCap / 32];
-#pragma unroll
-        for (int j = 0; j < kOffCap / 32; ++j)
-          if (lane + 32 * j < nwin) v[j] = exc_off[ub + lane + 32 * j];
-#pragma unroll
-        for (int j = 0; j < kOffCap / 32; ++j)
-          if (lane + 32 * j < nwin) soff[lane + 32 * j] = v[j];
-      }
-      __syncwarp();
-      const uint32_t e0 = soff[0], e1 = soff[nwin - 1];
-      bool bad = e1 < e0 || int64_t(e1) > P.pr[pc].n_exc;
-      const bool fits = !bad && (e1 - e0) <= uint32_t(kEntCap);
-      if (fits) {
-        constexpr int kBatch = 16;  // entries per lane in flight
-        const uint32_t n = e1 - e0;
-        for (uint32_t b0 = 0; b0 < n; b0 += 32 * kBatch) {
-          uint32_t v[kBatch];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j)
-            if (b0 + lane + 32 * j < n) v[j] = exc_ent[e0 + b0 + lane + 32 * j];
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j)
-            if (b0 + lane + 32 * j < n) sent[b0 + lane + 32 * j] = v[j];
-        }
-      }
-      __syncwarp();
+      const ExcWindow w = stage_window(P.pr[pc].exc_off, P.pr[pc].exc_ent, P.pr[pc].n_exc, sbegin(c), n_units,
+                                       reinterpret_cast<uint32_t*>(smem + plan.soff_off),
+                                       reinterpret_cast<uint32_t*>(smem + plan.sent_off));
       if (lane == 0) {
-        if (bad) set_status(P.status, W12_ERR_CORRUPT);
-        *ent_in_smem = fits ? 1 : 0;
-        *ent_base = e0;
-        *ent_end = bad ? e0 : e1;
+        if (w.bad) set_status(P.status, W12_ERR_CORRUPT);
+        *ent_in_smem = w.fits ? 1 : 0;
+        *ent_base = w.e0;
+        *ent_end = w.bad ? w.e0 : w.e1;
         mbar_arrive(B.exc_ready);
       }
     }
