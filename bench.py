@@ -49,7 +49,7 @@ def profiled_traffic():
     import hashlib
     prof = os.path.join(ROOT, "profiles", "fused_head_m16.md")
     srcs = [os.path.join(ROOT, "speculative_decoding_verification_w12_gb300", "csrc", f)
-            for f in ("w12_gemm.cu", "w12_dev.cuh")]
+            for f in ("w12_gemm.cu", "w12_decode.cuh", "w12_dev.cuh")]
     if not os.path.exists(prof) or not all(os.path.exists(f) for f in srcs):
         return None
     fields = {}
