@@ -150,3 +150,50 @@ def test_grouped_exception_heavy(zero_frac):
     assert status_value(st) == 0
     for i, (X, W) in enumerate(zip(Xs, Ws)):
         assert_gemm_close(Ys[i].cpu().numpy(), O.gemm(X, O.pack(W)), f"problem {i}, zeros {zero_frac}")
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_grouped_swiglu_four_problems_small(M):
+    """Two independent problems between gate_up and down, all small: the
+    phases have fewer units than CTAs (so some CTAs sit a phase out), and the
+    middle phase splits its CTAs over two problems. Every output against the
+    oracle (stage-isolated as above), over repeated launches."""
+    Nh = 256
+    shapes = [(256, 128), (2 * Nh, 384), (384, 256), (256, Nh)]   # other, gate_up, other, down
+    Ws, Xs = _problems(shapes, M, seed=13 * M)
+    pks = [w12.pack(to_dev_bf16(W)) for W in Ws]
+    st = new_status()
+    g = w12.Grouped([(to_dev_bf16(Xs[0]), pks[0], None), (to_dev_bf16(Xs[1]), pks[1], None),
+                     (to_dev_bf16(Xs[2]), pks[2], None), (None, pks[3], None)], M, swiglu=(1, 3), status=st)
+    for rep in range(2):
+        Ys = [Y.cpu().numpy() for Y in g.run()]
+        assert status_value(st) == 0
+        for i in (0, 1, 2):
+            assert_gemm_close(Ys[i], O.gemm(Xs[i], O.pack(Ws[i])), f"problem {i} rep {rep}")
+        act = bits_of(g.act)
+        _act_close(act, O.swiglu(Ys[1]))
+        assert_gemm_close(Ys[3], O.gemm(act, O.pack(Ws[3])), f"down rep {rep}")
+
+
+@pytest.mark.parametrize("zero_frac", [0.02, 0.3])
+def test_grouped_swiglu_exception_heavy(zero_frac):
+    """The SwiGLU-linked form with many exceptions: 2 % keeps every job's
+    entries in shared memory, 30 % overflows it, so the decoders read each
+    job's entries from its own problem's list in global memory."""
+    M, Nh = 16, 512
+    shapes = [(512, 256), (2 * Nh, 384), (384, Nh)]     # other, gate_up, down
+    Ws, Xs = _problems(shapes, M, seed=31)
+    g = np.random.default_rng(9)
+    for W in Ws:
+        W[g.random(W.shape) < zero_frac] = 0
+    pks = [w12.pack(to_dev_bf16(W)) for W in Ws]
+    st = new_status()
+    gr = w12.Grouped([(to_dev_bf16(Xs[0]), pks[0], None), (to_dev_bf16(Xs[1]), pks[1], None), (None, pks[2], None)],
+                     M, swiglu=(1, 2), status=st)
+    Y0, Ygu, Ydn = (Y.cpu().numpy() for Y in gr.run())
+    assert status_value(st) == 0
+    assert_gemm_close(Y0, O.gemm(Xs[0], O.pack(Ws[0])), f"other, zeros {zero_frac}")
+    assert_gemm_close(Ygu, O.gemm(Xs[1], O.pack(Ws[1])), f"gate_up, zeros {zero_frac}")
+    act = bits_of(gr.act)
+    _act_close(act, O.swiglu(Ygu))
+    assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), f"down, zeros {zero_frac}")
