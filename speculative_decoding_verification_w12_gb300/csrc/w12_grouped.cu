@@ -66,6 +66,12 @@ struct GemmParams {
   // (columns j*128 .. j*128+127) is written by the CTA that completes the
   // second of its two Y tiles (j and j + N/256).
   int glu_from, glu_to, glu_blocks;
+  // Pairs: the source phase gives CTA c < glu_blocks the two whole tiles c and
+  // c + glu_blocks (gate and up of act block c) instead of an even share of
+  // the source's units, so no source tile is split and each act block is
+  // written by the CTA that computed both of its tiles, at the end of its
+  // first phase rather than after the last of several pieces.
+  int glu_pairs;
   uint16_t* act;
   int32_t* glu_cnt;                   // per block: tiles completed (reset to 0 by the writer)
   int32_t* glu_ready;                 // per block: epoch + 1 once written
@@ -80,8 +86,8 @@ struct GemmMaps {
 };
 
 // A CTA's job in one phase: units [b, b + n) of problem p, whose U units are
-// shared by G CTAs, this one at place cl; s0 = index of the job's first unit
-// in the CTA's sequence. Exception entries of the job: positions [e0, e1) of
+// shared by G CTAs, this one at place cl (G = 0: whole tiles that no other
+// CTA shares); s0 = index of the job's first unit in the CTA's sequence. Exception entries of the job: positions [e0, e1) of
 // the CTA's staged window, entry g0 + (position - e0) of the problem's list.
 struct Job {
   int p, f, cl, G, U, b, n, s0;
@@ -168,7 +174,7 @@ __host__ __device__ inline SmemPlan smem_plan(int Mpad, int stages) {
   p.misc_off = off;
   off += 64;
   p.job_off = off;
-  off += kMaxProb * sizeof(Job);
+  off += (kMaxProb + 1) * sizeof(Job);
   p.total = off + 1024;  // slack for 1024-byte alignment of the base
   return p;
 }
@@ -267,6 +273,17 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       int nj = 0, s0 = 0;
       for (int p = 0; p < P.nprob; ++p) {
         const ProbParams& q = P.pr[p];
+        if (P.glu_pairs && p == P.glu_from) {
+          if (int(blockIdx.x) < P.glu_blocks) {
+            for (int h = 0; h < 2; ++h) {
+              const int t = int(blockIdx.x) + h * P.glu_blocks;
+              J[nj] = Job{p, q.phase, 0, 0, q.KB * q.tiles, t * q.KB, q.KB, s0, 0u, 0u, 0u, 0u};
+              s0 += q.KB;
+              ++nj;
+            }
+          }
+          continue;
+        }
         if (int(blockIdx.x) < q.cta0 || int(blockIdx.x) >= q.cta1) continue;
         const int U = q.KB * q.tiles, Gp = q.cta1 - q.cta0, cl = int(blockIdx.x) - q.cta0;
         const int b = int(unit_begin(cl, U, Gp)), e = int(unit_begin(cl + 1, U, Gp));
@@ -780,8 +797,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         accb = 0;
         accph ^= 1u;
       }
-      const int c_first = unit_owner(tile_u0, Uf, Gf);
-      const int c_last = unit_owner(tile_u0 + KBp - 1, Uf, Gf);
+      // (A whole-tile job, Gf = 0, holds the only piece of its tiles.)
+      const int c_first = Gf == 0 ? cl : unit_owner(tile_u0, Uf, Gf);
+      const int c_last = Gf == 0 ? cl : unit_owner(tile_u0 + KBp - 1, Uf, Gf);
       const int nsplit = c_last - c_first + 1;
       // Partial slots are laid out [chunk][row][16] floats: each thread's 16
       // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
@@ -1088,7 +1106,7 @@ static void set_problem(ProbParams& q, bool w12_mode, const w12_weights* W, int6
 // Grouped launch: problems in launch order with their phases, and the
 // workspace carve-up.
 struct Grouped {
-  int n, order[kMaxProb], phase[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks;
+  int n, order[kMaxProb], phase[kMaxProb], nphase, Mpad, grid, tiles, glu_from, glu_to, glu_blocks, glu_pairs;
   int cta0[kMaxProb], cta1[kMaxProb];  // launch problem j runs on CTAs [cta0[j], cta1[j]) of its phase
   int64_t N[kMaxProb], K[kMaxProb], phase_units[kMaxProb];
   size_t counters, glu_cnt, glu_ready, epoch, parts, total;
@@ -1187,12 +1205,26 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
     per_cta += most;
     g->grid = at > g->grid ? at : g->grid;
   }
-  if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
   if (to >= 0) {
     g->glu_from = 0;
     g->glu_to = n - 1;
     g->glu_blocks = int(g->N[link->from] / (2 * kGroup));
+    // Whole gate/up pairs for the source phase when they spread over the CTAs
+    // about as evenly as an even split would (at most 1.25 CTAs per pair):
+    // one pair per CTA, the rest of the CTAs start on the next phase.
+    const int pairs = g->glu_blocks;
+    if (pairs <= grid && 4 * grid <= 5 * pairs) {
+      g->glu_pairs = 1;
+      const int64_t src_kb = g->K[link->from] / kGroup;
+      int64_t most0 = 0;  // the even split's largest share, replaced by a pair's units
+      for (int j = 0; j < n; ++j)
+        if (g->phase[j] == 0) most0 = (U[j] + (g->cta1[j] - g->cta0[j]) - 1) / (g->cta1[j] - g->cta0[j]);
+      per_cta += 2 * src_kb - most0;
+      g->cta0[0] = 0;
+      g->cta1[0] = pairs;
+    }
   }
+  if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -1257,6 +1289,7 @@ static int launch_grouped(bool w12_mode, const w12_problem* probs, int n, int64_
   P.glu_from = g.glu_from;
   P.glu_to = g.glu_to;
   P.glu_blocks = g.glu_blocks;
+  P.glu_pairs = g.glu_pairs;
   P.act = link ? link->act : nullptr;
   P.glu_cnt = reinterpret_cast<int32_t*>(wsb + g.glu_cnt);
   P.glu_ready = reinterpret_cast<int32_t*>(wsb + g.glu_ready);

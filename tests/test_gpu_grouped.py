@@ -197,3 +197,26 @@ def test_grouped_swiglu_exception_heavy(zero_frac):
     act = bits_of(gr.act)
     _act_close(act, O.swiglu(Ygu))
     assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), f"down, zeros {zero_frac}")
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_grouped_swiglu_whole_pairs(M):
+    """Enough gate/up pairs for the pair schedule (128 act blocks, at most 1.25
+    CTAs per pair on a 152-SM GPU): CTA c < 128 computes gate/up tiles c and
+    c + 128 whole, and the rest start on the middle phase. Every output against
+    the oracle (stage-isolated), over repeated launches."""
+    Nh = 128 * 128
+    shapes = [(256, 128), (2 * Nh, 128), (128, Nh)]     # other, gate_up, down
+    Ws, Xs = _problems(shapes, M, seed=17 * M)
+    pks = [w12.pack(to_dev_bf16(W)) for W in Ws]
+    st = new_status()
+    g = w12.Grouped([(to_dev_bf16(Xs[0]), pks[0], None), (to_dev_bf16(Xs[1]), pks[1], None), (None, pks[2], None)],
+                    M, swiglu=(1, 2), status=st)
+    for rep in range(2):
+        Y0, Ygu, Ydn = (Y.cpu().numpy() for Y in g.run())
+        assert status_value(st) == 0
+        assert_gemm_close(Y0, O.gemm(Xs[0], O.pack(Ws[0])), f"other rep {rep}")
+        assert_gemm_close(Ygu, O.gemm(Xs[1], O.pack(Ws[1])), f"gate_up rep {rep}")
+        act = bits_of(g.act)
+        _act_close(act, O.swiglu(Ygu))
+        assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), f"down rep {rep}")
