@@ -1170,60 +1170,91 @@ static int plan_grouped(const w12_problem* probs, int n, int64_t M, const w12_sw
   // One CTA per SM at most: a CTA of the SwiGLU link may wait on work of any
   // other CTA, so all of them must be resident together.
   const int grid = int(maxu < sms ? maxu : sms);
-  // Each phase splits the CTAs over its problems so that the largest
-  // per-CTA share of units is as small as it can be: one CTA at a time to
-  // the problem whose CTAs carry the most units each (units weigh the same
-  // bytes in every problem), never more CTAs than units.
-  int64_t per_cta = 0;
-  g->grid = 0;
-  for (int f = 0; f < g->nphase; ++f) {
-    int j0 = -1, j1 = -1;
-    for (int j = 0; j < n; ++j)
-      if (g->phase[j] == f) {
-        if (j0 < 0) j0 = j;
-        j1 = j + 1;
-      }
-    if (grid < j1 - j0) return W12_ERR_UNSUPPORTED;
-    int cnt[kMaxProb];
-    for (int j = j0; j < j1; ++j) cnt[j] = 1;
-    for (int left = grid - (j1 - j0); left > 0; --left) {
+  // CTAs [lo, hi) split over the problems of `sel` (a bit per launch problem)
+  // so that the largest per-CTA share of units is as small as it can be: one
+  // CTA at a time to the problem whose CTAs carry the most units each (units
+  // weigh the same bytes in every problem), never more CTAs than units.
+  // Returns that share, or -1 if there are fewer CTAs than problems.
+  auto split = [&](int lo, int hi, unsigned sel) -> int64_t {
+    int cnt[kMaxProb], np = 0;
+    for (int j = 0; j < n; ++j) {
+      cnt[j] = (sel >> j) & 1u;
+      np += cnt[j];
+    }
+    if (np == 0) return 0;
+    if (hi - lo < np) return -1;
+    for (int left = hi - lo - np; left > 0; --left) {
       int best = -1;
-      for (int j = j0; j < j1; ++j)
-        if (cnt[j] < U[j] && (best < 0 || U[j] * cnt[best] > U[best] * cnt[j])) best = j;
+      for (int j = 0; j < n; ++j)
+        if (((sel >> j) & 1u) && cnt[j] < U[j] && (best < 0 || U[j] * cnt[best] > U[best] * cnt[j])) best = j;
       if (best < 0) break;
       ++cnt[best];
     }
-    int at = 0;
+    int at = lo;
     int64_t most = 0;
-    for (int j = j0; j < j1; ++j) {
+    for (int j = 0; j < n; ++j) {
+      if (!((sel >> j) & 1u)) continue;
       g->cta0[j] = at;
       at += cnt[j];
       g->cta1[j] = at;
       const int64_t q = (U[j] + cnt[j] - 1) / cnt[j];
       most = q > most ? q : most;
     }
-    per_cta += most;
-    g->grid = at > g->grid ? at : g->grid;
+    return most;
+  };
+  unsigned in_phase[kMaxProb] = {0, 0, 0, 0};
+  for (int j = 0; j < n; ++j) in_phase[g->phase[j]] |= 1u << j;
+  int64_t most_of[kMaxProb] = {0, 0, 0, 0};
+  for (int f = 0; f < g->nphase; ++f) {
+    most_of[f] = split(0, grid, in_phase[f]);
+    if (most_of[f] < 0) return W12_ERR_UNSUPPORTED;
   }
+  g->grid = grid;
   if (to >= 0) {
     g->glu_from = 0;
     g->glu_to = n - 1;
     g->glu_blocks = int(g->N[link->from] / (2 * kGroup));
     // Whole gate/up pairs for the source phase when they spread over the CTAs
     // about as evenly as an even split would (at most 1.25 CTAs per pair):
-    // one pair per CTA, the rest of the CTAs start on the next phase.
+    // one pair per CTA. The CTAs without a pair then take the middle phase's
+    // problems that even out the first two phases best: each subset of them
+    // on the free CTAs and the rest on the paired ones, against the middle
+    // phase split over all CTAs, by the largest per-CTA load in units.
     const int pairs = g->glu_blocks;
     if (pairs <= grid && 4 * grid <= 5 * pairs) {
       g->glu_pairs = 1;
-      const int64_t src_kb = g->K[link->from] / kGroup;
-      int64_t most0 = 0;  // the even split's largest share, replaced by a pair's units
-      for (int j = 0; j < n; ++j)
-        if (g->phase[j] == 0) most0 = (U[j] + (g->cta1[j] - g->cta0[j]) - 1) / (g->cta1[j] - g->cta0[j]);
-      per_cta += 2 * src_kb - most0;
+      const int64_t pair_units = 2 * (g->K[link->from] / kGroup);
+      most_of[0] = pair_units;
       g->cta0[0] = 0;
       g->cta1[0] = pairs;
+      const unsigned mid = g->nphase == 3 ? in_phase[1] : 0u;
+      if (mid && grid > pairs) {
+        int64_t best_load = pair_units + most_of[1];  // the middle phase over all CTAs
+        unsigned best = ~0u;
+        for (unsigned sub = mid;; sub = (sub - 1) & mid) {  // every subset of the middle problems
+          const int64_t fr = split(pairs, grid, sub), pr = split(0, pairs, mid & ~sub);
+          if (fr >= 0 && pr >= 0) {
+            const int64_t load = fr > pair_units + pr ? fr : pair_units + pr;
+            if (load < best_load) {
+              best_load = load;
+              best = sub;
+            }
+          }
+          if (sub == 0) break;
+        }
+        if (best != ~0u) {
+          const int64_t fr = split(pairs, grid, best), pr = split(0, pairs, mid & ~best);
+          most_of[1] = fr > pr ? fr : pr;
+        } else {
+          most_of[1] = split(0, grid, mid);
+        }
+      }
     }
   }
+  int64_t per_cta = 0;
+  for (int f = 0; f < g->nphase; ++f) per_cta += most_of[f];
+  g->grid = 0;  // CTAs past every problem's range (all capped at their units) are not launched
+  for (int j = 0; j < n; ++j) g->grid = g->cta1[j] > g->grid ? g->cta1[j] : g->grid;
   if (w12_mode && per_cta + 1 > kOffCap) return W12_ERR_SHAPE;
   size_t off = 0;
   auto take = [&](size_t bytes) {
