@@ -711,8 +711,41 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     const int32_t epoch = kGlu && P.glu_to >= 0 ? ld_acquire_gpu(P.epoch) : 0;
     // Tile t of the SwiGLU source problem is complete in Y: the CTA that
     // completes the second tile of block j writes act block j and publishes it.
-    auto glu_tile_done = [&](int t) {
+    // This thread's column of act block j from both halves in Y: 8 rows per
+    // batch, every load of a batch issued before its first use (one L2 round
+    // trip per 8 rows).
+    auto act_from_y = [&](int j) {
       const ProbParams& pg = P.pr[P.glu_from];
+      const int64_t Nh = pg.N / 2;
+      const int64_t col = int64_t(j) * 128 + et;
+      for (int m0 = 0; m0 < P.M; m0 += 8) {
+        float g[8], u[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int m = m0 + r < P.M ? m0 + r : P.M - 1;
+          g[r] = __ldcg(pg.Y + int64_t(m) * pg.N + col);
+          u[r] = __ldcg(pg.Y + int64_t(m) * pg.N + Nh + col);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (m0 + r < P.M) P.act[int64_t(m0 + r) * Nh + col] = f32_to_bf16_rne(g[r] / (1.0f + expf(-g[r])) * u[r]);
+      }
+    };
+    // Pairs: tile t >= glu_blocks completes act block j = t - glu_blocks, whose
+    // gate tile this CTA computed earlier. Each thread reads only the column it
+    // stored itself in both tiles, so no barrier or count comes first; one
+    // barrier orders every thread's act stores before the publication.
+    auto glu_pair_done = [&](int j) {
+      act_from_y(j);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __threadfence();
+      named_bar_sync(kEpiBar, 128);
+      if (et == 0) {
+        st_release_gpu(P.glu_ready + j, epoch + 1);
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(P.epoch + 2) : "memory");
+      }
+    };
+    auto glu_tile_done = [&](int t) {
       const int j = t < P.glu_blocks ? t : t - P.glu_blocks;
       named_bar_sync(kEpiBar, 128);  // every thread's Y stores of the tile are issued
       if (et == 0) {
@@ -722,22 +755,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       }
       named_bar_sync(kEpiBar, 128);
       if (*glu_flag) {
-        const int64_t Nh = pg.N / 2;
-        const int64_t col = int64_t(j) * 128 + et;
-        // 8 rows per batch, every load of a batch issued before its first
-        // use: one L2 round trip per 8 rows.
-        for (int m0 = 0; m0 < P.M; m0 += 8) {
-          float g[8], u[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const int m = m0 + r < P.M ? m0 + r : P.M - 1;
-            g[r] = __ldcg(pg.Y + int64_t(m) * pg.N + col);
-            u[r] = __ldcg(pg.Y + int64_t(m) * pg.N + Nh + col);
-          }
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-            if (m0 + r < P.M) P.act[int64_t(m0 + r) * Nh + col] = f32_to_bf16_rne(g[r] / (1.0f + expf(-g[r])) * u[r]);
-        }
+        act_from_y(j);
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
         named_bar_sync(kEpiBar, 128);
@@ -893,7 +911,10 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&B.acc_empty[cur]);
         if (pref && et == 0) P.counters[gt] = 0;  // every other contributor has already counted
-        if (kGlu && pi == P.glu_from) glu_tile_done(t);
+        if (kGlu && pi == P.glu_from) {
+          if (!P.glu_pairs) glu_tile_done(t);
+          else if (t >= P.glu_blocks) glu_pair_done(t - P.glu_blocks);
+        }
       } else {
         // In the final segment every stage of the ring has been consumed (the
         // segment's MMAs completed), so the other pieces' partials can be
@@ -995,7 +1016,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         }
         if (last && et == 0) P.counters[gt] = 0;
         named_bar_sync(kEpiBar, 128);
-        if (kGlu && last && pi == P.glu_from) glu_tile_done(t);
+        if (kGlu && last && pi == P.glu_from && !P.glu_pairs) glu_tile_done(t);  // (pairs never split a tile)
       }
     }
     // Partials requested into shared memory must land before the CTA exits.
