@@ -12,11 +12,11 @@ argument checks), which otherwise dominates the short layer GEMMs at M = 16.
 Inputs (activations X, hidden states H, draft block) live in one device
 buffer mirrored by one pinned host buffer, and the results (accept_len,
 bonus, argmax) in one device buffer mirrored by one pinned host buffer, so
-the host path is one graph: a copy kernel that reads the pinned inputs, the
-step, and a copy kernel that writes the results to pinned memory (kernels,
-not copy-engine transfers, so that the step's first GEMM starts requesting
-its weights while the inputs arrive, and the result copy follows the last
-kernel without a separate transfer's start-up).
+the host path is one graph: a copy kernel that reads the pinned inputs (a
+kernel, not a copy-engine transfer, so that the step's first GEMM starts
+requesting its weights while the inputs arrive) and the step, whose accept
+kernel writes the results straight into the pinned host buffer (the device
+addresses page-locked memory in place).
 """
 from __future__ import annotations
 
@@ -76,8 +76,9 @@ class VerifyStep:
         """Kernel launches per step: the layer GEMMs, the fused head GEMM and its reduce/accept kernel."""
         return (len(self.groups) if self.groups is not None else len(self.layers)) + 2
 
-    def run(self):
-        """Enqueue one step on the current stream (eager libw12 calls)."""
+    def run(self, out=None):
+        """Enqueue one step on the current stream (eager libw12 calls). out:
+        (accept_len, bonus, argmax) to write instead of the device results."""
         if self.groups is not None:
             for g in self.groups:
                 g.run()
@@ -85,7 +86,7 @@ class VerifyStep:
             for x, w, y, ws in zip(self.X, self.layers, self.Y, self.ws):
                 w12.gemm(x, w, Y=y, ws=ws, status=self.status)
         w12.verify_greedy_fused(self.H, self.head, self.draft, self.T_rows, ws=self.hws, status=self.status,
-                                out=(self.accept_len, self.bonus, self.argmax))
+                                out=out if out is not None else (self.accept_len, self.bonus, self.argmax))
 
     def capture(self):
         """Record one step into a CUDA graph (after one eager warm-up call)."""
@@ -111,16 +112,15 @@ class VerifyStep:
         return self._X_host, self._H_host, self._draft_host
 
     def capture_host(self):
-        """Record copy-in, step and copy-out into one CUDA graph."""
+        """Record copy-in and the step into one CUDA graph; the accept kernel
+        writes its results straight into the pinned host buffer."""
         w12.copy(self._in_dev, self._in_host)
-        self.run()
-        w12.copy(self._out_host, self._out_dev)
+        self.run(out=self._results_host)
         torch.cuda.synchronize(self.dev)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             w12.copy(self._in_dev, self._in_host)
-            self.run()
-            w12.copy(self._out_host, self._out_dev)
+            self.run(out=self._results_host)
         torch.cuda.synchronize(self.dev)
         self.graph_host = g
         return self
