@@ -199,7 +199,7 @@ def test_grouped_swiglu_exception_heavy(zero_frac):
     assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), f"down, zeros {zero_frac}")
 
 
-@pytest.mark.parametrize("M", [16, 40])
+@pytest.mark.parametrize("M", [16, 40, 128, 256])
 def test_grouped_swiglu_whole_pairs(M):
     """Enough gate/up pairs for the pair schedule (128 act blocks, at most 1.25
     CTAs per pair on a 152-SM GPU): CTA c < 128 computes gate/up tiles c and
