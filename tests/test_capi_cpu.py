@@ -109,3 +109,42 @@ def test_tree_attention_without_gpu_is_unsupported(L):
     buf = (ctypes.c_uint8 * 4096)()
     a = (ctypes.addressof(buf) + 15) // 16 * 16
     assert L.w12_tree_attention(a, a, a, 1, 16, 10, 2, 128, 64, 64, a, a, 0.1, a, a, 4096, None, None) == 8
+
+
+def _grouped_ws(L, shapes, M, link=None):
+    """w12_gemm_grouped_ws_bytes for W12 problems of the given (N, K) (the
+    query reads only the shapes; the weight pointers are never followed)."""
+    ws = [w12._Weights(N=N, K=K) for N, K in shapes]
+    probs = (w12._Problem * len(shapes))()
+    for i, W in enumerate(ws):
+        probs[i].W = ctypes.cast(ctypes.pointer(W), ctypes.c_void_p).value
+        probs[i].N, probs[i].K = shapes[i]
+    sw = None if link is None else ctypes.pointer(w12._Swiglu(link[0], link[1], None))
+    return int(L.w12_gemm_grouped_ws_bytes(probs, len(shapes), M, sw))
+
+
+def test_grouped_plan_on_the_host(L):
+    """The grouped launch's host plan, without a device (sized for 256 SMs):
+    counters per tile, the link's per-block arrays and epoch, and two partial
+    slots of Mpad x 128 fp32 per CTA and phase, each rounded up to 256 bytes."""
+    layer = [(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)]
+    r256 = lambda b: -(-b // 256) * 256  # noqa: E731
+    tiles = sum(N // 128 for N, _ in layer)
+    grid = 256   # every phase has more units than CTAs
+    # Independent: one phase.
+    want = r256(4 * tiles) + 256 + 256 + 256 + r256(4 * 2 * 1 * grid * 16 * 128)
+    assert _grouped_ws(L, layer, 16) == want
+    # gate_up -> SwiGLU -> down: three phases, 136 act blocks.
+    blocks = 34816 // 256
+    want = r256(4 * tiles) + r256(4 * blocks) * 2 + 256 + r256(4 * 2 * 3 * grid * 16 * 128)
+    assert _grouped_ws(L, layer, 16, link=(2, 3)) == want
+    # Mpad follows M (rounded to 16).
+    assert _grouped_ws(L, layer, 33) == r256(4 * tiles) + 768 + r256(4 * 2 * grid * 48 * 128)
+    # Rejected plans: a link whose target's K is not half the source's N, too
+    # many problems, M out of range, and more units per CTA than the exception
+    # window holds (its offsets: units per CTA + 1 <= 1024).
+    assert _grouped_ws(L, layer, 16, link=(0, 1)) == 0
+    assert _grouped_ws(L, layer + [(128, 128)], 16) == 0
+    assert _grouped_ws(L, layer, 0) == 0 and _grouped_ws(L, layer, 257) == 0
+    assert _grouped_ws(L, [(2048 * 128, 128 * 128)], 16) == 0   # 2048 x 128 units: 1024 per CTA
+    assert _grouped_ws(L, [(2048 * 128, 127 * 128)], 16) > 0    # 2048 x 127 units: 1016 per CTA
