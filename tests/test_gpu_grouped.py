@@ -72,6 +72,15 @@ def test_grouped_swiglu_chain(M):
     act = bits_of(g.act)
     _act_close(act, O.swiglu(Ygu))
     assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), "down")
+    # The bf16 baseline of the same linked launch.
+    gb = w12.Grouped([(to_dev_bf16(Xs[0]), to_dev_bf16(Ws[0]), None), (to_dev_bf16(Xs[1]), to_dev_bf16(Ws[1]), None),
+                      (None, to_dev_bf16(Ws[2]), None)], M, swiglu=(1, 2), bf16=True, status=st)
+    Y0, Ygu, Ydn = (Y.cpu().numpy() for Y in gb.run())
+    assert status_value(st) == 0
+    assert_gemm_close(Ygu, O.gemm(Xs[1], O.pack(Ws[1])), "bf16 gate_up")
+    act = bits_of(gb.act)
+    _act_close(act, O.swiglu(Ygu))
+    assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), "bf16 down")
 
 
 def test_grouped_swiglu_new_inputs_each_call():
@@ -212,11 +221,14 @@ def test_grouped_swiglu_whole_pairs(M):
     st = new_status()
     g = w12.Grouped([(to_dev_bf16(Xs[0]), pks[0], None), (to_dev_bf16(Xs[1]), pks[1], None), (None, pks[2], None)],
                     M, swiglu=(1, 2), status=st)
+    gb = w12.Grouped([(to_dev_bf16(Xs[0]), to_dev_bf16(Ws[0]), None), (to_dev_bf16(Xs[1]), to_dev_bf16(Ws[1]), None),
+                      (None, to_dev_bf16(Ws[2]), None)], M, swiglu=(1, 2), bf16=True, status=st)
     for rep in range(2):
-        Y0, Ygu, Ydn = (Y.cpu().numpy() for Y in g.run())
-        assert status_value(st) == 0
-        assert_gemm_close(Y0, O.gemm(Xs[0], O.pack(Ws[0])), f"other rep {rep}")
-        assert_gemm_close(Ygu, O.gemm(Xs[1], O.pack(Ws[1])), f"gate_up rep {rep}")
-        act = bits_of(g.act)
-        _act_close(act, O.swiglu(Ygu))
-        assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), f"down rep {rep}")
+        for name, gr in (("w12", g), ("bf16", gb)):
+            Y0, Ygu, Ydn = (Y.cpu().numpy() for Y in gr.run())
+            assert status_value(st) == 0
+            assert_gemm_close(Y0, O.gemm(Xs[0], O.pack(Ws[0])), f"{name} other rep {rep}")
+            assert_gemm_close(Ygu, O.gemm(Xs[1], O.pack(Ws[1])), f"{name} gate_up rep {rep}")
+            act = bits_of(gr.act)
+            _act_close(act, O.swiglu(Ygu))
+            assert_gemm_close(Ydn, O.gemm(act, O.pack(Ws[2])), f"{name} down rep {rep}")
