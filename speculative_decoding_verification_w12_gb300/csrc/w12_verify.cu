@@ -199,8 +199,22 @@ __global__ void __launch_bounds__(256) reduce_accept_kernel(
   const int m = blockIdx.x;
   float bv = -INFINITY;
   int bi = 0x7FFFFFFF;
-  for (int p = threadIdx.x; p < nparts; p += blockDim.x)
-    better(bv, bi, pv[int64_t(p) * Mstride + m], pi[int64_t(p) * Mstride + m]);
+  // Eight partials per thread in flight before the comparisons: one L2 round
+  // trip per batch (1,187 partials per row over 256 threads for the 151,936
+  // vocabulary: one batch) instead of one per partial.
+  constexpr int kBatch = 8;
+  for (int p0 = threadIdx.x; p0 < nparts; p0 += kBatch * int(blockDim.x)) {
+    float vv[kBatch];
+    int32_t ii[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int p = p0 + j * int(blockDim.x);
+      vv[j] = p < nparts ? pv[int64_t(p) * Mstride + m] : -INFINITY;
+      ii[j] = p < nparts ? pi[int64_t(p) * Mstride + m] : 0x7FFFFFFF;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) better(bv, bi, vv[j], ii[j]);
+  }
   block_argmax(bv, bi);
   if (threadIdx.x == 0) {
     argmax_ws[m] = bi;
