@@ -474,8 +474,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const int c_first = unit_owner(int64_t(t) * KB, U, G);
       const int c_last = unit_owner((int64_t(t) + 1) * KB - 1, U, G);
       const int nsplit = c_last - c_first + 1;
-      // Partial slots are laid out [chunk][row][16] floats: each thread's 16
-      // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
+      // Partial slots are laid out [chunk][quarter][row][4] floats: the 16
+      // values a thread holds for a chunk are four 16-byte pieces 2 KB apart,
+      // so each warp-wide access covers 512 contiguous bytes (whole sectors).
       auto slot_of = [&](int cc) {
         const int ft = int(unit_begin(cc, U, G) / KB);
         return 2 * cc + (t == ft ? 0 : 1);
@@ -508,13 +509,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         pref = *pref_flag;
         if (pref) {
           const float4* s0 =
-              reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + 1 - me)) * P.Mpad * 128) + size_t(row) * 4;
+              reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + 1 - me)) * P.Mpad * 128) + row;
           // Parked in this thread's own column of the transpose buffer (free
           // until this segment's epilogue writes the same places).
           float* sc = scratch + row;
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const float4 f = __ldcg(s0 + x);
+            const float4 f = __ldcg(s0 + x * 128);
             sc[(4 * x) * kScratchStride] = f.x;
             sc[(4 * x + 1) * kScratchStride] = f.y;
             sc[(4 * x + 2) * kScratchStride] = f.z;
@@ -590,9 +591,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           for (int mc = 0; mc < nchunks; ++mc) {
             float v[16];
             load_acc(mc, v);
-            float4* dst = my + (size_t(mc) * 128 + row) * 4;
+            float4* dst = my + size_t(mc) * 512 + row;
 #pragma unroll
-            for (int x = 0; x < 4; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+            for (int x = 0; x < 4; ++x) dst[x * 128] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
           }
         }
         tc_fence_before();
@@ -650,12 +651,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
                 load_acc(mc, q);
               } else {
                 const float4* src =
-                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nb + b2) * 8192u) + row * 4
+                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nb + b2) * 8192u) + row
                            : reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128) +
-                                 (size_t(mc) * 128 + row) * 4;
+                                 size_t(mc) * 512 + row;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
-                  const float4 f = gather ? src[x] : __ldcg(src + x);
+                  const float4 f = gather ? src[x * 128] : __ldcg(src + x * 128);
                   q[4 * x] = f.x, q[4 * x + 1] = f.y, q[4 * x + 2] = f.z, q[4 * x + 3] = f.w;
                 }
               }
@@ -710,9 +711,9 @@ __global__ void __launch_bounds__(128) splitk_reduce_kernel(const float* __restr
         const int ft = int(unit_begin(cc, U, G) / KB);
         const int slot = 2 * cc + (t == ft ? 0 : 1);
         const float4* src =
-            reinterpret_cast<const float4*>(parts + size_t(slot) * Mpad * 128) + (size_t(mc) * 128 + row) * 4;
+            reinterpret_cast<const float4*>(parts + size_t(slot) * Mpad * 128) + size_t(mc) * 512 + row;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) f[j][x] = __ldcg(src + x);
+        for (int x = 0; x < 4; ++x) f[j][x] = __ldcg(src + x * 128);
       }
     }
 #pragma unroll
