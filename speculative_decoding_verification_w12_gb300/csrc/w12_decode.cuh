@@ -29,7 +29,6 @@ static_assert(W12_DEC_GROUPS >= 1 && W12_DEC_GROUPS <= 3, "decode groups: 1..3")
 static_assert(W12_DEC_SPLIT == 1 || W12_DEC_SPLIT == 2 || W12_DEC_SPLIT == 4, "decode split: 1, 2 or 4");
 constexpr int kDecGroups = W12_DEC_GROUPS;       // decode groups: group g takes units g, g + kDecGroups, ...
 constexpr int kDecSplit = W12_DEC_SPLIT;         // warps sharing one unit row
-constexpr int kChunksPerThread = 4 / kDecSplit;  // 32-value chunks each decode thread restores per unit
 constexpr int kAColsPerBuf = 64;                 // 128 K values = 64 TMEM columns of bf16 pairs
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
 
@@ -90,7 +89,7 @@ struct DecodeCtx {
   int S;                     // ring stages
   int n_units;               // units of this CTA
   uint64_t* full;            // [S] weight bytes of a stage landed
-  uint64_t* a_full;          // [S] decoded A of a stage stored (128 * kDecSplit arrivals)
+  uint64_t* a_full;          // [S] decoded A of a stage stored (128 * split width arrivals)
   uint32_t a_tmem;           // TMEM address of A buffer 0 at this warp's lane quarter
   const uint32_t* soff;      // per unit: first entry position (n_units + 1 values)
   const uint32_t* sent;      // staged entries (when in_smem)
@@ -105,12 +104,18 @@ struct DecodeCtx {
 // unit is decoded without exceptions and W12_ERR_CORRUPT is set); gptr(i)
 // gives the pointer p with entry position o of unit i at p[o] when entries are
 // not staged. Returns the OR of the entries read.
-template <class Wait, class Bad, class Gptr>
+//
+// kGroups x kSplitW sets how the 4 * kGroups * kSplitW decode warps share the
+// work (a_full counts 128 * kSplitW arrivals): more groups decode more units
+// at once, a wider split restores each unit sooner.
+template <int kGroups = kDecGroups, int kSplitW = kDecSplit, class Wait, class Bad, class Gptr>
 __device__ __forceinline__ uint32_t decode_units(const DecodeCtx& c, int dw, Wait&& wait, Bad&& bad, Gptr&& gptr) {
+  static_assert(kGroups >= 1 && (kSplitW == 1 || kSplitW == 2 || kSplitW == 4), "decode layout");
+  constexpr int kChunksPerThread = 4 / kSplitW;
   const int lane = threadIdx.x & 31;
   const int q = (threadIdx.x >> 5) & 3;       // TMEM lane quarter of this warp
-  const int grp = (dw >> 2) / kDecSplit;      // decode group
-  const int h = (dw >> 2) % kDecSplit;        // slice of the unit row (kChunksPerThread chunks of 32 values)
+  const int grp = (dw >> 2) / kSplitW;        // decode group
+  const int h = (dw >> 2) % kSplitW;          // slice of the unit row (kChunksPerThread chunks of 32 values)
   const int row = q * 32 + lane;              // W row within the unit
   const uint32_t tm_a = c.a_tmem + (uint32_t(q * 32) << 16);
   uint32_t seen = 0;
@@ -155,7 +160,7 @@ __device__ __forceinline__ uint32_t decode_units(const DecodeCtx& c, int dw, Wai
       s = 0;
       ph ^= 1u;
     }
-  for (int i = grp; i < c.n_units; i += kDecGroups) {
+  for (int i = grp; i < c.n_units; i += kGroups) {
     // Stage s's copies can only have landed after the MMA that last read
     // its TMEM A buffer committed, so the buffer is free once this returns.
     // One decision per warp: the loop uses warp-collective instructions.
@@ -211,7 +216,7 @@ __device__ __forceinline__ uint32_t decode_units(const DecodeCtx& c, int dw, Wai
       }
       tmem_st16(tm_a + uint32_t(s * kAColsPerBuf) + lc * 16u, w);
     }
-    if (i + kDecGroups < c.n_units) prep(i + kDecGroups, cur);  // overlaps the stores in flight
+    if (i + kGroups < c.n_units) prep(i + kGroups, cur);  // overlaps the stores in flight
     tmem_st_wait();
     tc_fence_before();
     // This thread's reads of the stage (generic proxy) come before the copy
@@ -220,7 +225,7 @@ __device__ __forceinline__ uint32_t decode_units(const DecodeCtx& c, int dw, Wai
     // them in about 1 % of launches.
     fence_proxy_async_smem();
     mbar_arrive(&c.a_full[s]);
-    for (int k = 0; k < kDecGroups; ++k)
+    for (int k = 0; k < kGroups; ++k)
       if (++s == c.S) {
         s = 0;
         ph ^= 1u;

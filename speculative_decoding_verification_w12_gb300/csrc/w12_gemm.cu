@@ -18,7 +18,8 @@
 //   decode warps (4 + 4*groups*split of them): each thread restores its
 //               row's share of the unit from the planes (LDS.128), patches
 //               exceptions in registers, and writes bf16 pairs into TMEM
-//               (tcgen05.st); decode groups take units in turn.
+//               (tcgen05.st); decode groups take units in turn (at large M
+//               one group of wider split restores each unit sooner).
 //   last 4 warps epilogue: tcgen05.ld of the accumulator; unsplit tiles write
 //               Y directly; split tiles write partial slots and the last CTA
 //               to arrive sums them in a fixed order (deterministic).
@@ -39,6 +40,13 @@ constexpr int kMaxStages = 8;         // smem ring depth limit (one TMEM A buffe
 constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
 constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
 constexpr int kDeferMinMpad = 128;    // from this many padded rows, split tiles may be summed by a second kernel
+// From kWideMinMpad padded rows (a ring of two or three stages, so a unit's
+// restore sits on the critical path) the decode warps form one group of
+// kWideSplit warps per lane quarter instead of kDecGroups groups: one unit at
+// a time, each restored kWideSplit times sooner.
+constexpr int kWideMinMpad = 128;
+constexpr int kWideSplit = kDecGroups * kDecSplit;
+static_assert(kWideSplit == 1 || kWideSplit == 2 || kWideSplit == 4, "wide decode layout");
 
 struct GemmParams {
   int M, Mpad, N, K, KB, tiles, grid, stages, issuers;
@@ -116,7 +124,7 @@ struct Bars {
   uint64_t* gather;
 };
 
-template <bool kW12, bool kArgmax>
+template <bool kW12, bool kArgmax, bool kWide>
 __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                 const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_x,
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       mbar_init(&B.empty[s], 1);
     }
     if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
-      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * kDecSplit);
+      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * (kWide ? kWideSplit : kDecSplit));
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&B.acc_full[a], P.issuers);  // one commit per MMA issuer per segment
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       d.in_smem = *ent_in_smem;
       d.status = P.status;
       const uint32_t e_end = *ent_end;
-      const uint32_t seen = decode_units(
+      const uint32_t seen = decode_units<kWide ? 1 : kDecGroups, kWide ? kWideSplit : kDecSplit>(
           d, warp - 4, wait,
           [&](int, uint32_t o0, uint32_t o1) {
             return o1 < o0 || int64_t(o1) > P.n_exc || o0 < d.e_base || o1 > e_end;
@@ -755,14 +763,15 @@ static int launch_impl(const GemmShape& sh, const GemmParams& P0, const CUtensor
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
   P.issuers = issuers;
-  auto kern = gemm_kernel<kW12, kArgmax>;
-  static bool attr_set[64] = {false};  // per device; setting it twice is harmless
+  const bool wide = kW12 && sh.Mpad >= kWideMinMpad;
+  auto kern = wide ? gemm_kernel<kW12, kArgmax, kW12> : gemm_kernel<kW12, kArgmax, false>;
+  static bool attr_set[2][64] = {};  // per kernel and device; setting it twice is harmless
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
-  if (!attr_set[dev]) {
+  if (!attr_set[wide][dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
       return W12_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[wide][dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(P.grid));
