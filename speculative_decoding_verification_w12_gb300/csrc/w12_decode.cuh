@@ -31,6 +31,13 @@ constexpr int kDecGroups = W12_DEC_GROUPS;       // decode groups: group g takes
 constexpr int kDecSplit = W12_DEC_SPLIT;         // warps sharing one unit row
 constexpr int kAColsPerBuf = 64;                 // 128 K values = 64 TMEM columns of bf16 pairs
 constexpr uint32_t kInvalidEnt = 0xFFFFFFFFu;
+// From kWideMinMpad padded rows (a ring of two or three stages, so a unit's
+// restore sits on the critical path) the kernels lay the same decode warps
+// out as one group of kWideSplit warps per lane quarter instead of kDecGroups
+// groups: one unit at a time, each restored kWideSplit times sooner.
+constexpr int kWideMinMpad = 128;
+constexpr int kWideSplit = kDecGroups * kDecSplit;
+static_assert(kWideSplit == 1 || kWideSplit == 2 || kWideSplit == 4, "wide decode layout");
 
 // A CTA's exception window over units [ub, ub + n) of one problem, staged by
 // one warp (all 32 lanes): the n + 1 offsets exc_off[ub ..] into soff (n + 1

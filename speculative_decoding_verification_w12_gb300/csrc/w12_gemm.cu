@@ -40,13 +40,6 @@ constexpr int kMaxStages = 8;         // smem ring depth limit (one TMEM A buffe
 constexpr int kEpiBar = 1;            // named barrier id of the epilogue warps
 constexpr int kScratchStride = 129;   // floats per column in the argmax transpose buffer
 constexpr int kDeferMinMpad = 128;    // from this many padded rows, split tiles may be summed by a second kernel
-// From kWideMinMpad padded rows (a ring of two or three stages, so a unit's
-// restore sits on the critical path) the decode warps form one group of
-// kWideSplit warps per lane quarter instead of kDecGroups groups: one unit at
-// a time, each restored kWideSplit times sooner.
-constexpr int kWideMinMpad = 128;
-constexpr int kWideSplit = kDecGroups * kDecSplit;
-static_assert(kWideSplit == 1 || kWideSplit == 2 || kWideSplit == 4, "wide decode layout");
 
 struct GemmParams {
   int M, Mpad, N, K, KB, tiles, grid, stages, issuers;

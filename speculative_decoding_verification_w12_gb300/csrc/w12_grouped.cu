@@ -191,7 +191,7 @@ struct Bars {
   uint64_t* gather;
 };
 
-template <bool kW12, bool kArgmax, int kMode>
+template <bool kW12, bool kArgmax, int kMode, bool kWide>
 __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps TM, const __grid_constant__ GemmParams P) {
   using C = Cfg<kW12>;
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       mbar_init(&B.empty[s], 1);
     }
     if (kW12) {  // decoded-operand handshakes exist only when there are decode warps
-      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * kDecSplit);
+      for (int a = 0; a < S; ++a) mbar_init(&B.a_full[a], 128 * (kWide ? kWideSplit : kDecSplit));
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&B.acc_full[a], P.issuers);  // one commit per MMA issuer per segment
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       // One problem: the CTA's window of the problem's entries. Job table:
       // each job's window, positions [e0, e1) of the staged buffer for entries
       // g0 .. of the job's problem.
-      const uint32_t seen = decode_units(
+      const uint32_t seen = decode_units<kWide ? 1 : kDecGroups, kWide ? kWideSplit : kDecSplit>(
           d, warp - 4, wait,
           [&](int i, uint32_t o0, uint32_t o1) {
             if (single) return o1 < o0 || int64_t(o1) > P.pr[pc].n_exc || o0 < d.e_base || o1 > e_end;
@@ -819,8 +819,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
       const int c_first = Gf == 0 ? cl : unit_owner(tile_u0, Uf, Gf);
       const int c_last = Gf == 0 ? cl : unit_owner(tile_u0 + KBp - 1, Uf, Gf);
       const int nsplit = c_last - c_first + 1;
-      // Partial slots are laid out [chunk][row][16] floats: each thread's 16
-      // values of a chunk are 64 contiguous bytes (four 16-byte accesses).
+      // Partial slots are laid out [chunk][quarter][row][4] floats: the 16
+      // values a thread holds for a chunk are four 16-byte pieces 2 KB apart,
+      // so each warp-wide access covers 512 contiguous bytes (whole sectors).
       // CTA cc has two slots per phase: its first piece in the phase, and
       // its last.
       auto slot_of = [&](int cc) {
@@ -858,13 +859,13 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
         pref = *pref_flag;
         if (pref) {
           const float4* s0 =
-              reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + 1 - me)) * P.Mpad * 128) + size_t(row) * 4;
+              reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + 1 - me)) * P.Mpad * 128) + row;
           // Parked in this thread's own column of the transpose buffer (free
           // until this segment's epilogue writes the same places).
           float* sc = scratch + row;
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const float4 f = __ldcg(s0 + x);
+            const float4 f = __ldcg(s0 + x * 128);
             sc[(4 * x) * kScratchStride] = f.x;
             sc[(4 * x + 1) * kScratchStride] = f.y;
             sc[(4 * x + 2) * kScratchStride] = f.z;
@@ -937,9 +938,9 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
           for (int mc = 0; mc < nchunks; ++mc) {
             float v[16];
             load_acc(mc, v);
-            float4* dst = my + (size_t(mc) * 128 + row) * 4;
+            float4* dst = my + size_t(mc) * 512 + row;
 #pragma unroll
-            for (int x = 0; x < 4; ++x) dst[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+            for (int x = 0; x < 4; ++x) dst[x * 128] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
           }
         }
         tc_fence_before();
@@ -997,12 +998,12 @@ __global__ void __launch_bounds__(Cfg<kW12>::kThreads, 1)
                 load_acc(mc, q);
               } else {
                 const float4* src =
-                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nb + b2) * 8192u) + row * 4
+                    gather ? reinterpret_cast<const float4*>(smem + uint32_t(j++ * nb + b2) * 8192u) + row
                            : reinterpret_cast<const float4*>(P.parts + size_t(slot_of(c_first + sp)) * P.Mpad * 128) +
-                                 (size_t(mc) * 128 + row) * 4;
+                                 size_t(mc) * 512 + row;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
-                  const float4 f = gather ? src[x] : __ldcg(src + x);
+                  const float4 f = gather ? src[x * 128] : __ldcg(src + x * 128);
                   q[4 * x] = f.x, q[4 * x + 1] = f.y, q[4 * x + 2] = f.z, q[4 * x + 3] = f.w;
                 }
               }
@@ -1057,14 +1058,17 @@ static int launch_impl(int Mpad, GemmParams& P, const GemmMaps& TM, cudaStream_t
   if (plan.total > uint32_t(smem_max)) return W12_ERR_UNSUPPORTED;
   P.stages = stages;
   P.issuers = issuers;
-  auto kern = gemm_kernel<kW12, kArgmax, kMode>;
-  static bool attr_set[64] = {false};  // per device; setting it twice is harmless
+  // Large M: one decode group of the widest split (a unit's restore sits on
+  // the critical path of a two- or three-stage ring).
+  const bool wide = kW12 && Mpad >= kWideMinMpad;
+  auto kern = wide ? gemm_kernel<kW12, kArgmax, kMode, kW12> : gemm_kernel<kW12, kArgmax, kMode, false>;
+  static bool attr_set[2][64] = {};  // per kernel and device; setting it twice is harmless
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W12_ERR_CUDA;
-  if (!attr_set[dev]) {
+  if (!attr_set[wide][dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess)
       return W12_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[wide][dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(P.grid));
