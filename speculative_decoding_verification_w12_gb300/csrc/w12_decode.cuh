@@ -195,12 +195,45 @@ __device__ __forceinline__ uint32_t decode_units(const DecodeCtx& c, int dw, Wai
       decode8(a[cc].y, b[cc].y, g[cc].y, E2, w + 4);
       decode8(a[cc].z, b[cc].z, g[cc].z, E2, w + 8);
       decode8(a[cc].w, b[cc].w, g[cc].w, E2, w + 12);
-      uint32_t mk = cur.mask[cc];
-      while (mk) {
-        const int src = __ffs(mk) - 1;
-        mk &= mk - 1;
-        const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
-        if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+      if (kSplitW <= 2) {
+        if (cur.mask[cc] != 0u) {
+          // Patch through shared memory: the chunk's 16 words go to bytes of
+          // the stage that only this thread reads and has already loaded (its
+          // own row's slices of the planes), the lane holding each exception
+          // of the chunk stores its 16 bits at the target (row, column), and
+          // the words are read back. Scratch slot k (16 bytes) is plane
+          // k / kChunksPerThread, chunk slice h * kChunksPerThread + k %
+          // kChunksPerThread of the row, in the planes' swizzle.
+          uint8_t* const stw = const_cast<uint8_t*>(st);
+          auto slot_addr = [&](uint32_t r, uint32_t k) {
+            return stw + (k / kChunksPerThread) * 8192u + r * 64u +
+                   (((uint32_t(h * kChunksPerThread) + k % kChunksPerThread) ^ ((r >> 1) & 3u)) << 4);
+          };
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(slot_addr(uint32_t(row), uint32_t(k))) =
+                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          __syncwarp();
+          if ((cur.mask[cc] >> lane) & 1u) {
+            const uint32_t col = (cur.ent >> 16) & 31u;  // byte 2 * col of the chunk's 64
+            const uint32_t r = uint32_t(q * 32) + ((cur.ent >> 23) & 31u);
+            *reinterpret_cast<uint16_t*>(slot_addr(r, col >> 3) + ((col & 7u) << 1)) = uint16_t(cur.ent & 0xFFFFu);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = *reinterpret_cast<const uint4*>(slot_addr(uint32_t(row), uint32_t(k)));
+            w[4 * k] = v.x, w[4 * k + 1] = v.y, w[4 * k + 2] = v.z, w[4 * k + 3] = v.w;
+          }
+        }
+      } else {
+        uint32_t mk = cur.mask[cc];
+        while (mk) {
+          const int src = __ffs(mk) - 1;
+          mk &= mk - 1;
+          const uint32_t e = __shfl_sync(0xFFFFFFFFu, cur.ent, src);
+          if (uint32_t(lane) == ((e >> 23) & 31u)) patch_word(w, (e >> 16) & 31u, e & 0xFFFFu);
+        }
       }
       if (cur.o1 - cur.o0 > 32) {
         // Rare: more than 32 exceptions in the unit; walk the rest in batches.
