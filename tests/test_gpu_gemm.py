@@ -72,7 +72,7 @@ def test_split_k_shapes(N, K):
     assert_gemm_close(Yr, Y64, "bf16")
 
 
-@pytest.mark.parametrize("M", [16, 128])
+@pytest.mark.parametrize("M", [16, 128, 256])
 def test_exception_heavy_weights(M):
     """Dense exceptions: zero groups, >32 exceptions per unit, specials."""
     g = S.rng(5)
