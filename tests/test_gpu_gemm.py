@@ -72,6 +72,48 @@ def test_split_k_shapes(N, K):
     assert_gemm_close(Yr, Y64, "bf16")
 
 
+# Exception placements that exercise every way the decoders patch a value in:
+# a full 32-value row chunk (32 lanes writing into one row), one exception in
+# each of 32 rows of a lane quarter, both halves of one 32-bit word, the first
+# and last column and row of a unit, and a unit with more than 32 exceptions.
+_PLANTED = [
+    [(5, c) for c in range(32, 64)],                          # unit (0, 0): row 5, chunk 1 whole
+    [(64 + j, 128 + 96 + j) for j in range(32)],              # unit (0, 1): quarter 2, chunk 3, one per row
+    [(130, 0), (130, 1), (130, 30), (130, 31), (255, 127), (255, 64), (128, 0)],   # unit (1, 0)
+    [(200, c) for c in range(128, 168)],                      # unit (1, 1): 40 in one row
+]
+
+
+@pytest.mark.parametrize("M", [16, 128, 256])
+def test_exception_positions_exact(M):
+    """Planted exceptions read back exactly through one-hot rows of X (Y = selected columns of W^T)."""
+    N = K = 256
+    W = S.weights_bf16(N, K, seed=31)
+    pos = [p for unit in _PLANTED for p in unit]
+    for r, c in pos:
+        W[r, c] = 0                                           # zero in a normal group: an exception
+    W[200, 168:172] = np.array([0x0001, 0x8001, 0x7F7F, 0xFF7F], dtype=np.uint16)   # subnormals, extremes
+    pk = O.pack(W)
+    ent = pk["exc_ent"]
+    got = {(int(u // 2) * 128 + int((e >> 23) & 127), int(u % 2) * 128 + int((e >> 16) & 127))
+           for u in range(4) for e in ent[pk["exc_off"][u]:pk["exc_off"][u + 1]]}
+    assert set(pos) <= got, "every planted zero is an exception"
+    assert pk["exc_off"][4] - pk["exc_off"][3] > 32
+    if M == K:
+        cols = np.arange(K)
+    else:
+        want = sorted({c for _, c in pos} | {168, 169, 170, 171})
+        cols = np.array((want + [c for c in range(K) if c not in want])[:M])
+    X = np.zeros((M, K), dtype=np.uint16)
+    X[np.arange(M), cols] = 0x3F80                            # 1.0
+    Y64 = O.gemm(X, pk)
+    np.testing.assert_array_equal(Y64, S.bf16_bits_to_f32(W[:, cols]).T.astype(np.float64))
+    st = new_status()
+    Y = w12.gemm(to_dev_bf16(X), w12.pack(to_dev_bf16(W)), status=st).cpu().numpy()
+    assert status_value(st) == 0
+    np.testing.assert_array_equal(Y.astype(np.float64), Y64)
+
+
 @pytest.mark.parametrize("M", [16, 128, 256])
 def test_exception_heavy_weights(M):
     """Dense exceptions: zero groups, >32 exceptions per unit, specials."""
